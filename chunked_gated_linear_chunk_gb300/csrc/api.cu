@@ -1,0 +1,375 @@
+// api.cu -- the C ABI (include/glacore.h): validation, workspace layout,
+// segment preparation and kernel launches.  All compute runs in the
+// kernels; this file only checks arguments and enqueues work.
+#include <stdio.h>
+#include <string.h>
+
+#include "internal.cuh"
+#include "tc.cuh"
+
+namespace glacore {
+
+__device__ int g_device_error = 0;
+
+// Device address of g_device_error for the current device (looked up once
+// per device; kernels receive it as an argument).
+static int *device_error_ptr() {
+  static int *cache[128] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  if (!cache[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = (int *)ptr;
+  }
+  return cache[dev];
+}
+
+// ---- segment preparation (one CTA; documents numbered row-major) ------
+//
+// JLA product page (karlex.ai/jla): segment_ids make a packed batch train
+// exactly as its documents one by one.  A document starts at t = 0 of each
+// row and wherever the id changes from the previous token of the row.
+
+__device__ __forceinline__ int64_t block_excl_scan(int64_t x, int64_t *warp_buf, int64_t &total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_buf[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    int64_t s = lane < nw ? warp_buf[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) warp_buf[lane] = s;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int64_t before = w ? warp_buf[w - 1] : 0;
+  total = warp_buf[nw - 1];
+  __syncthreads();
+  return before + inc - x;
+}
+
+__global__ void __launch_bounds__(1024) prep_kernel(const int32_t *seg, int64_t B, int64_t T,
+                                                    int64_t n_seqs, int chunk, int64_t *start,
+                                                    int64_t *cbase, int *err) {
+  __shared__ int64_t wbuf[32];
+  const int64_t BT = B * T;
+  int64_t off = 0;
+  for (int64_t base = 0; base < BT; base += blockDim.x) {
+    const int64_t pos = base + threadIdx.x;
+    int64_t flag = 0;
+    if (pos < BT) flag = (pos % T == 0) || (seg[pos] != seg[pos - 1]);
+    int64_t tot;
+    const int64_t idx = off + block_excl_scan(flag, wbuf, tot);
+    if (flag && idx < n_seqs) start[idx] = pos;
+    off += tot;
+  }
+  const int64_t count = off;
+  if (threadIdx.x == 0 && count != n_seqs) set_device_error(err, GLACORE_ERR_DOCS);
+  // documents that segment_ids does not have become empty; the table always
+  // ends at BT so that every kernel stays inside the token range
+  for (int64_t i = count + threadIdx.x; i < n_seqs; i += blockDim.x) start[i] = BT;
+  if (threadIdx.x == 0) start[n_seqs] = BT;
+  __syncthreads();
+  int64_t coff = 0;
+  for (int64_t base = 0; base < n_seqs; base += blockDim.x) {
+    const int64_t d = base + threadIdx.x;
+    int64_t nch = 0;
+    if (d < n_seqs) nch = (start[d + 1] - start[d] + chunk - 1) / chunk;
+    int64_t tot;
+    const int64_t ex = block_excl_scan(nch, wbuf, tot);
+    if (d < n_seqs) cbase[d] = coff + ex;
+    coff += tot;
+  }
+  if (threadIdx.x == 0) cbase[n_seqs] = coff;
+}
+
+__global__ void count_kernel(const int32_t *seg, int64_t B, int64_t T, unsigned long long *out) {
+  const int64_t BT = B * T;
+  unsigned long long local = 0;
+  for (int64_t pos = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; pos < BT;
+       pos += (int64_t)gridDim.x * blockDim.x)
+    local += (pos % T == 0) || (seg[pos] != seg[pos - 1]);
+  for (int o = 16; o; o >>= 1) local += __shfl_down_sync(0xffffffffu, local, o);
+  if ((threadIdx.x & 31) == 0 && local) atomicAdd(out, local);
+}
+
+cudaError_t launch_prep(const int32_t *seg, int64_t B, int64_t T, int64_t n_seqs, int chunk,
+                        int64_t *start, int64_t *cbase, int *err, cudaStream_t st) {
+  prep_kernel<<<1, 1024, 0, st>>>(seg, B, T, n_seqs, chunk, start, cbase, err);
+  return cudaGetLastError();
+}
+
+// ---- argument checks ----------------------------------------------------
+
+namespace {
+
+struct Layout {
+  bool tc;             // tensor-core path
+  int chunk;           // chunk length of the state workspace / doc table
+  size_t off_start, off_cbase;  // doc tables (segments only)
+  size_t off_states, off_final, off_acc_q, off_acc_k, off_tc;
+  size_t total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+glacore_status check_problem(const glacore_problem *p, bool head_gate) {
+  if (!p) return GLACORE_ERR_INVALID_ARG;
+  if (p->B < 1 || p->T < 0 || p->H < 1 || p->Hqk < 1 || p->K < 1 || p->V < 1)
+    return GLACORE_ERR_INVALID_ARG;
+  if (p->K > 256 || p->V > 256) return GLACORE_ERR_INVALID_ARG;
+  if (p->H % p->Hqk) return GLACORE_ERR_INVALID_ARG;
+  if (p->dtype != GLACORE_F32 && p->dtype != GLACORE_BF16) return GLACORE_ERR_INVALID_ARG;
+  if (p->reserved0 != 0) return GLACORE_ERR_INVALID_ARG;
+  if (p->chunk_size < 0) return GLACORE_ERR_INVALID_ARG;
+  if (p->chunk_size != 0 && p->chunk_size != 64 && p->chunk_size != 128)
+    return GLACORE_ERR_UNSUPPORTED;
+  if (p->B > (int64_t)1 << 31 || p->T > (int64_t)1 << 31 || p->H > 65535)
+    return GLACORE_ERR_INVALID_ARG;
+  const int64_t BT = p->B * p->T;
+  if (!p->segment_ids) {
+    if (p->n_seqs != (p->T > 0 ? p->B : 0)) return GLACORE_ERR_INVALID_ARG;
+  } else {
+    if (p->n_seqs < (BT > 0 ? 1 : 0) || p->n_seqs > BT) return GLACORE_ERR_INVALID_ARG;
+  }
+  if (BT > 0 && (!p->q || !p->k || !p->v || !p->g)) return GLACORE_ERR_INVALID_ARG;
+  if (!(p->scale == p->scale)) return GLACORE_ERR_INVALID_ARG;  // NaN scale
+  (void)head_gate;
+  return GLACORE_OK;
+}
+
+bool simt_supported(const glacore_problem *p) { return p->K <= 128 && p->V <= 128; }
+
+Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
+  Layout L;
+  memset(&L, 0, sizeof(L));
+  L.tc = tc::supported(p, head_gate);
+  L.chunk = L.tc ? tc::chunk_of(p) : simt::SC;
+  const int64_t BT = p->B * p->T, n = p->n_seqs;
+  size_t off = 0;
+  if (p->segment_ids) {
+    L.off_start = off;
+    off = align256(off + sizeof(int64_t) * (n + 1));
+    L.off_cbase = off;
+    off = align256(off + sizeof(int64_t) * (n + 1));
+  }
+  if (L.tc) {
+    L.off_tc = off;
+    off = align256(off + tc::workspace_bytes(p, head_gate, backward));
+  } else if (backward) {
+    const int64_t slots = p->segment_ids ? (BT + L.chunk - 1) / L.chunk + n
+                                         : p->B * ((p->T + L.chunk - 1) / L.chunk);
+    L.off_states = off;
+    off = align256(off + sizeof(float) * (size_t)slots * p->H * p->K * p->V);
+    L.off_final = off;
+    off = align256(off + sizeof(float) * (size_t)n * p->H * p->K * p->V);
+    if (p->Hqk != p->H) {
+      L.off_acc_q = off;
+      off = align256(off + sizeof(float) * (size_t)BT * p->Hqk * p->K);
+      L.off_acc_k = off;
+      off = align256(off + sizeof(float) * (size_t)BT * p->Hqk * p->K);
+    }
+  }
+  L.total = off;
+  return L;
+}
+
+glacore_status check_ws(const glacore_problem *p, const Layout &L) {
+  if (L.total == 0) return GLACORE_OK;
+  if (!p->workspace || p->workspace_bytes < L.total) return GLACORE_ERR_WORKSPACE;
+  if ((uintptr_t)p->workspace & 255) return GLACORE_ERR_WORKSPACE;
+  return GLACORE_OK;
+}
+
+Prob make_prob(const glacore_problem *p, bool head_gate) {
+  Prob q;
+  q.BT = p->B * p->T;
+  q.H = p->H;
+  q.Hqk = p->Hqk;
+  q.K = p->K;
+  q.V = p->V;
+  q.gate_head = head_gate ? 1 : 0;
+  q.scale = p->scale;
+  q.q = p->q;
+  q.k = p->k;
+  q.v = p->v;
+  q.g = p->g;
+  q.h0 = p->initial_state;
+  q.err = device_error_ptr();
+  return q;
+}
+
+glacore_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? GLACORE_OK : GLACORE_ERR_CUDA;
+}
+
+Docs make_docs(const glacore_problem *p, const Layout &L, char *ws) {
+  Docs d;
+  d.T = p->T;
+  d.n = p->n_seqs;
+  d.chunk = L.chunk;
+  d.start = p->segment_ids ? (const int64_t *)(ws + L.off_start) : nullptr;
+  d.cbase = p->segment_ids ? (const int64_t *)(ws + L.off_cbase) : nullptr;
+  return d;
+}
+
+glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float *ht,
+                       cudaStream_t st) {
+  glacore_status s = check_problem(p, head_gate);
+  if (s) return s;
+  const int64_t BT = p->B * p->T;
+  if (BT > 0 && !o) return GLACORE_ERR_INVALID_ARG;
+  const Layout L = layout(p, head_gate, false);
+  if (!L.tc && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
+  if ((s = check_ws(p, L))) return s;
+  if (L.tc && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
+                aligned16(o) && aligned16(ht) && aligned16(p->initial_state)))
+    return GLACORE_ERR_INVALID_ARG;
+  if (BT == 0) return GLACORE_OK;
+  char *ws = (char *)p->workspace;
+  if (p->segment_ids) {
+    cudaError_t e = launch_prep(p->segment_ids, p->B, p->T, p->n_seqs, L.chunk,
+                                (int64_t *)(ws + L.off_start), (int64_t *)(ws + L.off_cbase),
+                                device_error_ptr(), st);
+    if (e != cudaSuccess) return GLACORE_ERR_CUDA;
+  }
+  const Docs docs = make_docs(p, L, ws);
+  const Prob pr = make_prob(p, head_gate);
+  if (L.tc) return cuda_status(tc::fwd(pr, docs, p, o, ht, ws + L.off_tc, st));
+  return cuda_status(simt::launch_fwd(pr, docs, p->dtype, o, ht, nullptr, st));
+}
+
+glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
+                       const float *dht, void *dq, void *dk, void *dv, float *dg, float *dh0,
+                       cudaStream_t st) {
+  glacore_status s = check_problem(p, head_gate);
+  if (s) return s;
+  const int64_t BT = p->B * p->T;
+  if (BT > 0 && (!dO || !dq || !dk || !dv || !dg)) return GLACORE_ERR_INVALID_ARG;
+  const Layout L = layout(p, head_gate, true);
+  if (!L.tc && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
+  if ((s = check_ws(p, L))) return s;
+  if (L.tc && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
+                aligned16(dO) && aligned16(dht) && aligned16(dq) && aligned16(dk) &&
+                aligned16(dv) && aligned16(dg) && aligned16(dh0) &&
+                aligned16(p->initial_state)))
+    return GLACORE_ERR_INVALID_ARG;
+  if (BT == 0) return GLACORE_OK;
+  char *ws = (char *)p->workspace;
+  if (p->segment_ids) {
+    cudaError_t e = launch_prep(p->segment_ids, p->B, p->T, p->n_seqs, L.chunk,
+                                (int64_t *)(ws + L.off_start), (int64_t *)(ws + L.off_cbase),
+                                device_error_ptr(), st);
+    if (e != cudaSuccess) return GLACORE_ERR_CUDA;
+  }
+  const Docs docs = make_docs(p, L, ws);
+  const Prob pr = make_prob(p, head_gate);
+  if (L.tc)
+    return cuda_status(tc::bwd(pr, docs, p, dO, dht, dq, dk, dv, dg, dh0, ws + L.off_tc, st));
+  float *states = (float *)(ws + L.off_states);
+  float *fin = (float *)(ws + L.off_final);
+  cudaError_t e = simt::launch_fwd(pr, docs, p->dtype, nullptr, fin, states, st);
+  if (e != cudaSuccess) return GLACORE_ERR_CUDA;
+  float *accq = nullptr, *acck = nullptr;
+  if (p->Hqk != p->H) {
+    accq = (float *)(ws + L.off_acc_q);
+    acck = (float *)(ws + L.off_acc_k);
+    const size_t nb = sizeof(float) * (size_t)BT * p->Hqk * p->K;
+    if (cudaMemsetAsync(accq, 0, nb, st) != cudaSuccess) return GLACORE_ERR_CUDA;
+    if (cudaMemsetAsync(acck, 0, nb, st) != cudaSuccess) return GLACORE_ERR_CUDA;
+  }
+  e = simt::launch_bwd(pr, docs, p->dtype, dO, dht, states, fin, dq, dk, accq, acck, dv, dg,
+                       dh0, st);
+  if (e != cudaSuccess) return GLACORE_ERR_CUDA;
+  if (accq) {
+    const int64_t n = BT * p->Hqk * p->K;
+    if (simt::launch_convert(accq, dq, p->dtype, n, st) != cudaSuccess) return GLACORE_ERR_CUDA;
+    if (simt::launch_convert(acck, dk, p->dtype, n, st) != cudaSuccess) return GLACORE_ERR_CUDA;
+  }
+  return GLACORE_OK;
+}
+
+size_t ws_size(const glacore_problem *p, bool head_gate, bool backward) {
+  if (check_problem(p, head_gate) != GLACORE_OK) return 0;
+  return layout(p, head_gate, backward).total;
+}
+
+}  // namespace
+}  // namespace glacore
+
+using namespace glacore;
+
+extern "C" {
+
+size_t gla_fwd_workspace_size(const glacore_problem *p) { return ws_size(p, false, false); }
+size_t gla_bwd_workspace_size(const glacore_problem *p) { return ws_size(p, false, true); }
+size_t ssd_fwd_workspace_size(const glacore_problem *p) { return ws_size(p, true, false); }
+size_t ssd_bwd_workspace_size(const glacore_problem *p) { return ws_size(p, true, true); }
+
+glacore_status gla_fwd(const glacore_problem *p, void *o, float *final_state,
+                       glacore_stream_t stream) {
+  return run_fwd(p, false, o, final_state, (cudaStream_t)stream);
+}
+glacore_status ssd_fwd(const glacore_problem *p, void *o, float *final_state,
+                       glacore_stream_t stream) {
+  return run_fwd(p, true, o, final_state, (cudaStream_t)stream);
+}
+glacore_status gla_bwd(const glacore_problem *p, const void *do_, const float *dht, void *dq,
+                       void *dk, void *dv, float *dg, float *dh0, glacore_stream_t stream) {
+  return run_bwd(p, false, do_, dht, dq, dk, dv, dg, dh0, (cudaStream_t)stream);
+}
+glacore_status ssd_bwd(const glacore_problem *p, const void *do_, const float *dht, void *dq,
+                       void *dk, void *dv, float *dg, float *dh0, glacore_stream_t stream) {
+  return run_bwd(p, true, do_, dht, dq, dk, dv, dg, dh0, (cudaStream_t)stream);
+}
+
+glacore_status glacore_count_docs(const int32_t *segment_ids, int64_t B, int64_t T,
+                                  int64_t *n_docs, glacore_stream_t stream) {
+  if (!n_docs || B < 1 || T < 0 || (B * T > 0 && !segment_ids)) return GLACORE_ERR_INVALID_ARG;
+  if (((uintptr_t)n_docs & 7) != 0) return GLACORE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(n_docs, 0, sizeof(int64_t), st) != cudaSuccess) return GLACORE_ERR_CUDA;
+  if (B * T == 0) return GLACORE_OK;
+  count_kernel<<<256, 256, 0, st>>>(segment_ids, B, T, (unsigned long long *)n_docs);
+  return cuda_status(cudaGetLastError());
+}
+
+glacore_status glacore_get_device_error(glacore_stream_t stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  int h = 0, zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, g_device_error, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                st) != cudaSuccess)
+    return GLACORE_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                              st) != cudaSuccess)
+    return GLACORE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GLACORE_ERR_CUDA;
+  return (glacore_status)h;
+}
+
+const char *glacore_status_string(glacore_status s) {
+  switch (s) {
+    case GLACORE_OK: return "ok";
+    case GLACORE_ERR_INVALID_ARG: return "invalid argument";
+    case GLACORE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GLACORE_ERR_CUDA: return "CUDA runtime error";
+    case GLACORE_ERR_TIMEOUT: return "bounded device wait ran out";
+    case GLACORE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case GLACORE_ERR_DOCS: return "segment_ids holds a different number of documents than n_seqs";
+  }
+  return "unknown status";
+}
+
+int glacore_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// internal.cuh -- declarations shared by the host library and its kernels.
+// Nothing here is part of the public ABI (include/glacore.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/glacore.h"
+
+namespace glacore {
+
+// Device error word: the first device-detected error code (glacore_status)
+// is kept until glacore_get_device_error reads and clears it.  Kernels get
+// its address as an argument (the word itself lives in api.cu).
+__device__ __forceinline__ void set_device_error(int *err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Document table.  Without segment_ids every batch row is one document
+// (start = d * T).  With segment_ids the prep kernel fills `start`
+// ([n+1] flattened token offsets) and `cbase` ([n+1] first chunk slot of
+// each document for the state workspace, for chunk length `chunk`).
+struct Docs {
+  const int64_t *start;  // nullptr: rows
+  const int64_t *cbase;  // nullptr: rows
+  int64_t T;             // row length
+  int64_t n;             // number of documents (grid size)
+  int chunk;             // chunk length the cbase table was built for
+
+  __device__ __forceinline__ void range(int64_t d, int64_t &s, int64_t &e) const {
+    if (start) {
+      s = start[d];
+      e = start[d + 1];
+    } else {
+      s = d * T;
+      e = s + T;
+    }
+  }
+  __device__ __forceinline__ int64_t chunk_base(int64_t d) const {
+    return cbase ? cbase[d] : d * ((T + chunk - 1) / chunk);
+  }
+};
+
+// Problem as the kernels see it (token axis flattened: BT = B * T).
+struct Prob {
+  int64_t BT, H, Hqk, K, V;
+  int gate_head;  // 0: g[BT,H,K]; 1: g[BT,H]
+  float scale;
+  const void *q, *k, *v;
+  const float *g;
+  const float *h0;
+  int *err;  // device error word
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ---- SIMT path (fp32 arithmetic; any K, V with K * V <= 16384) ----------
+namespace simt {
+constexpr int SC = 16;  // chunk length used by the SIMT kernels
+constexpr int SV = 32;  // value columns per forward CTA
+
+// Forward / state pass.  o may be null (state pass).  ws_states: if non-null,
+// the fp32 state entering every chunk is written to
+// ws_states[(cbase + j) * H + h][K][V].  ht: final state or null.
+cudaError_t launch_fwd(const Prob &p, const Docs &docs, int dtype, void *o, float *ht,
+                       float *ws_states, cudaStream_t st);
+// Backward gradient pass over chunks in reverse (reads ws_states and the
+// final states written by the state pass).
+cudaError_t launch_bwd(const Prob &p, const Docs &docs, int dtype, const void *dO,
+                       const float *dht, const float *ws_states, const float *ws_final,
+                       void *dq, void *dk, float *dq_acc, float *dk_acc, void *dv, float *dg,
+                       float *dh0, cudaStream_t st);
+cudaError_t launch_convert(const float *src, void *dst, int dtype, int64_t n, cudaStream_t st);
+size_t fwd_smem(int64_t K);
+size_t bwd_smem(int64_t K, int64_t V);
+}  // namespace simt
+
+// ---- segment prep ------------------------------------------------------
+cudaError_t launch_prep(const int32_t *seg, int64_t B, int64_t T, int64_t n_seqs, int chunk,
+                        int64_t *start, int64_t *cbase, int *err, cudaStream_t st);
+
+}  // namespace glacore

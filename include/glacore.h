@@ -1,0 +1,163 @@
+/*
+ * glacore.h -- C ABI of the chunk-parallel gated linear attention library
+ * (GLA and Mamba-2 SSD, forward and backward) for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (FLAT blog, trainstation-project.github.io/blog/flat,
+ * section "Linear Attention / Forward Recurrence" and its architecture
+ * table; JLA product page, karlex.ai/jla, for segment_ids and states):
+ *
+ *     S_t = diag(exp(g_t)) S_{t-1} + k_t v_t^T,     o_t = scale * S_t^T q_t
+ *
+ * with S a K x V state per (document, head).  GLA: g is a log-decay per key
+ * channel, g[B,T,H,K].  Mamba-2 SSD: one scalar log-decay per head,
+ * g[B,T,H].  A document starts at t = 0 of every batch row and wherever
+ * segment_ids[b,t] != segment_ids[b,t-1]; the state restarts there from the
+ * document's initial state (or zero).  Documents are numbered 0..n_seqs-1
+ * in row-major order of their first token.  The first token of a document
+ * decays the initial state: S_{t0} = diag(exp(g_{t0})) h0 + k v^T.
+ *
+ * Backward (FLAT blog, "Backward Recurrence" and "Backward Kernels"): the
+ * state gradient runs backwards in time; the gate gradient is the suffix
+ * sum over the document of q (.) dq - k (.) dk plus the final-state term
+ * (S_T (.) dht) 1_V.  States are recomputed inside the backward call; the
+ * forward stores nothing for it.
+ *
+ * Conventions (all entry points):
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The
+ *    library allocates no memory, never synchronises the stream (except
+ *    glacore_get_device_error, which says so) and
+ *    enqueues all work on `stream` (NULL = legacy default stream).
+ *  - Layouts are contiguous row-major.  Offsets are computed in 64-bit.
+ *      q, k        [B, T, Hqk, K]   (dtype)
+ *      v, o, do    [B, T, H, V]     (dtype)
+ *      g, dg       GLA: [B, T, H, K] fp32;  SSD: [B, T, H] fp32  (g <= 0)
+ *      segment_ids [B, T] int32 or NULL (then every row is one document)
+ *      states      [n_seqs, H, K, V] fp32 (initial_state, final_state,
+ *                  dht, dh0)
+ *      dq, dk      [B, T, Hqk, K] (dtype); summed over the H/Hqk heads that
+ *                  share q and k.  dv [B, T, H, V] (dtype).
+ *  - Every output is fully overwritten (no read-modify-write of outputs).
+ *  - Host-side validation runs before any launch; on failure nothing is
+ *    enqueued and an error status is returned.
+ *  - Inconsistencies that only the device can see (the number of documents
+ *    in segment_ids differs from n_seqs) set a device error word instead of
+ *    trapping; read it with glacore_get_device_error.
+ *  - Pointers passed to the tensor-core path must be 16-byte aligned.
+ *  - Calls on different streams may run concurrently provided they use
+ *    different workspace buffers.
+ */
+#ifndef GLACORE_H
+#define GLACORE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *glacore_stream_t;
+
+typedef enum {
+  GLACORE_OK = 0,
+  GLACORE_ERR_INVALID_ARG = 1, /* bad size, NULL required pointer, misalignment */
+  GLACORE_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. chunk_size) */
+  GLACORE_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+  GLACORE_ERR_TIMEOUT = 4,     /* a bounded device wait ran out */
+  GLACORE_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than *_workspace_size */
+  GLACORE_ERR_DOCS = 6         /* device: document count != n_seqs */
+} glacore_status;
+
+typedef enum { GLACORE_F32 = 0, GLACORE_BF16 = 1 } glacore_dtype;
+
+/* One problem description, shared by the forward and backward entries.
+ *   B, T        batch rows and tokens per row (T >= 0; B >= 1)
+ *   H           value heads; Hqk heads of q/k (GLA: Hqk == H; SSD: H % Hqk == 0)
+ *   K, V        key and value head dims (1..256)
+ *   dtype       element type of q, k, v, o, do, dq, dk, dv
+ *   chunk_size  chunk length of the chunk-parallel form: 64 (default) or
+ *               128; 0 selects 64.  Results do not depend on it beyond
+ *               rounding.
+ *   scale       output scale (GLA usually K^-1/2; Mamba-2: 1)
+ *   n_seqs      number of documents: B when segment_ids is NULL
+ *   initial_state  [n_seqs,H,K,V] fp32 or NULL (zero)
+ *   workspace   device scratch of at least *_workspace_size(problem) bytes
+ *               (may be NULL when that size is 0); 256-byte aligned */
+typedef struct glacore_problem {
+  int64_t B, T, H, Hqk, K, V;
+  int32_t dtype;
+  int32_t chunk_size;
+  float scale;
+  int32_t reserved0; /* must be 0 */
+  const void *q, *k, *v;
+  const float *g;
+  const int32_t *segment_ids;
+  int64_t n_seqs;
+  const float *initial_state;
+  void *workspace;
+  size_t workspace_bytes;
+} glacore_problem;
+
+/* Scratch bytes needed by the matching call (0 if none).  Returns 0 and
+ * does nothing else for an invalid problem (the call itself reports it). */
+size_t gla_fwd_workspace_size(const glacore_problem *p);
+size_t gla_bwd_workspace_size(const glacore_problem *p);
+size_t ssd_fwd_workspace_size(const glacore_problem *p);
+size_t ssd_bwd_workspace_size(const glacore_problem *p);
+
+/* GLA forward (per-key-channel gate, g [B,T,H,K]).
+ *   o            [B,T,H,V] dtype, written
+ *   final_state  [n_seqs,H,K,V] fp32, written, or NULL (not returned)
+ * FLAT blog, "Pallas Kernels for Linear Attention / Forward Kernels" (fused
+ * block-recurrent forward: intra-chunk masked product plus the readout of
+ * the carried state, state kept on chip across chunks). */
+glacore_status gla_fwd(const glacore_problem *p, void *o, float *final_state,
+                       glacore_stream_t stream);
+
+/* GLA backward.
+ *   do_   [B,T,H,V] dtype: dL/do
+ *   dht   [n_seqs,H,K,V] fp32: dL/dfinal_state, or NULL (zero)
+ *   dq, dk [B,T,Hqk,K], dv [B,T,H,V] (dtype), dg like g (fp32): written
+ *   dh0   [n_seqs,H,K,V] fp32: dL/dinitial_state, written; may be NULL
+ * FLAT blog, "Backward Recurrence" and "Backward Kernels" (a state pass
+ * that reruns the forward recurrence, then a gradient pass over the chunks
+ * in reverse carrying the state gradient; gate gradient as a suffix sum). */
+glacore_status gla_bwd(const glacore_problem *p, const void *do_,
+                       const float *dht, void *dq, void *dk, void *dv,
+                       float *dg, float *dh0, glacore_stream_t stream);
+
+/* Mamba-2 SSD: the same two calls with one scalar log-decay per head
+ * (g and dg are [B,T,H]); q = C, k = B, v = x; q/k may be shared by
+ * H/Hqk heads.  FLAT blog, section "Mamba-2" (scalar data-dependent gate
+ * evaluated in log space). */
+glacore_status ssd_fwd(const glacore_problem *p, void *o, float *final_state,
+                       glacore_stream_t stream);
+glacore_status ssd_bwd(const glacore_problem *p, const void *do_,
+                       const float *dht, void *dq, void *dk, void *dv,
+                       float *dg, float *dh0, glacore_stream_t stream);
+
+/* Counts the documents in segment_ids [B,T] (device pointer) and writes
+ * the count, as int64, to *n_docs (DEVICE pointer, 8-byte aligned).
+ * Asynchronous on `stream`; the caller reads the count after the stream
+ * reaches it.  Used to size final_state / dh0 before a call. */
+glacore_status glacore_count_docs(const int32_t *segment_ids, int64_t B,
+                                  int64_t T, int64_t *n_docs,
+                                  glacore_stream_t stream);
+
+/* Reads and clears the library's device error word (set by kernels for
+ * GLACORE_ERR_DOCS or GLACORE_ERR_TIMEOUT).  Synchronises `stream`.
+ * Returns GLACORE_OK if no device error was recorded. */
+glacore_status glacore_get_device_error(glacore_stream_t stream);
+
+/* Static English description of a status code. */
+const char *glacore_status_string(glacore_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int glacore_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLACORE_H */

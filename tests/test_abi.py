@@ -1,0 +1,117 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_gated_linear_chunk_gb300 as glc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "glacore.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:size_t|glacore_status|const char \*|int)\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gla_fwd", "gla_bwd", "ssd_fwd", "ssd_bwd", "gla_fwd_workspace_size",
+              "glacore_status_string", "glacore_get_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = glc.load()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(glc.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings_and_version():
+    lib = glc.load()
+    assert lib.glacore_version() >= 100
+    for s in range(7):
+        assert lib.glacore_status_string(s)
+    assert b"unknown" in lib.glacore_status_string(99)
+
+
+def make_problem(**over):
+    p = glc.Problem(B=2, T=100, H=4, Hqk=4, K=128, V=128, dtype=glc.BF16, chunk_size=64, scale=0.1,
+                    reserved0=0, q=256, k=512, v=768, g=1024, segment_ids=None, n_seqs=2,
+                    initial_state=None, workspace=None, workspace_bytes=0)
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+BAD = [
+    dict(B=0), dict(T=-1), dict(H=0), dict(K=0), dict(V=300), dict(Hqk=3), dict(dtype=7),
+    dict(reserved0=1), dict(chunk_size=-64), dict(n_seqs=3), dict(q=None), dict(g=None),
+    dict(scale=float("nan")),
+]
+
+
+@pytest.mark.parametrize("over", BAD)
+def test_invalid_arguments_rejected_before_launch(over):
+    lib = glc.load()
+    p = make_problem(**over)
+    null = ctypes.c_void_p(0)
+    o = ctypes.c_void_p(4096)
+    assert lib.gla_fwd(ctypes.byref(p), o, null, null) == glc.ERR_INVALID_ARG
+    assert lib.gla_bwd(ctypes.byref(p), o, null, o, o, o, o, null, null) == glc.ERR_INVALID_ARG
+    assert lib.gla_fwd_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_unsupported_chunk_size():
+    lib = glc.load()
+    p = make_problem(chunk_size=32)
+    assert lib.gla_fwd(ctypes.byref(p), ctypes.c_void_p(4096), None, None) == glc.ERR_UNSUPPORTED
+
+
+def test_missing_outputs_rejected():
+    lib = glc.load()
+    p = make_problem()
+    assert lib.gla_fwd(ctypes.byref(p), None, None, None) == glc.ERR_INVALID_ARG
+    o = ctypes.c_void_p(4096)
+    assert lib.gla_bwd(ctypes.byref(p), o, None, o, None, o, o, None, None) == glc.ERR_INVALID_ARG
+
+
+def test_workspace_checked():
+    lib = glc.load()
+    p = make_problem()
+    need = lib.gla_bwd_workspace_size(ctypes.byref(p))
+    assert need > 0
+    o = ctypes.c_void_p(4096)
+    assert lib.gla_bwd(ctypes.byref(p), o, None, o, o, o, o, None, None) == glc.ERR_WORKSPACE
+    p.workspace = 4096 + 16  # misaligned
+    p.workspace_bytes = need
+    assert lib.gla_bwd(ctypes.byref(p), o, None, o, o, o, o, None, None) == glc.ERR_WORKSPACE
+
+
+def test_segments_need_positive_doc_count():
+    lib = glc.load()
+    p = make_problem(segment_ids=2048, n_seqs=0)
+    assert lib.gla_fwd(ctypes.byref(p), ctypes.c_void_p(4096), None, None) == glc.ERR_INVALID_ARG
+    p = make_problem(segment_ids=2048, n_seqs=201)  # more documents than tokens
+    assert lib.gla_fwd(ctypes.byref(p), ctypes.c_void_p(4096), None, None) == glc.ERR_INVALID_ARG
+
+
+def test_empty_problem_is_a_no_op():
+    lib = glc.load()
+    p = make_problem(T=0, n_seqs=0, q=None, k=None, v=None, g=None)
+    assert lib.gla_fwd(ctypes.byref(p), None, None, None) == glc.OK
+    assert lib.gla_bwd_workspace_size(ctypes.byref(p)) >= 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+
+    x = torch.zeros(1, 4, 1, 8)
+    with pytest.raises(ValueError):
+        glc.gla_fwd(x, x, x, torch.zeros(1, 4, 1, 8))
