@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""GLA forward + backward throughput on GB300 (one JSON line on stdout).
+
+Workload: GLA, B=4 H=16 T=2048 K=V=128, bf16 q/k/v/do, fp32 gates, chunk 64,
+no initial or final state (seeded synthetic inputs, see
+chunked_gated_linear_chunk_gb300/inputs.py).  One step = gla_fwd + gla_bwd
+over that batch.  Inputs are resident in HBM; L2 is flushed (a write of
+twice the L2 size) before every timed step, outside the timed interval.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl glacore|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(weak scaling, no collective on the data path); the step time is the max
+over ranks and `value` counts the tokens of all ranks.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead
+(rank 0 only): each step is a bounded sample of the workload (one batch row,
+all heads), reported in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GLA fwd+bwd tokens/s & TFLOP/s (B4 H16 T2048 d128 bf16), % roofline, 1 GB300"
+UNIT = "tokens/s"
+WORKLOAD_INDEX = 2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def shape_of(w, n_docs=None):
+    from chunked_gated_linear_chunk_gb300 import roofline as rf
+
+    return rf.Shape(B=w.B, T=w.T, H=w.H, Hqk=w.Hqk, K=w.K, V=w.V, elem=2 if w.dtype == "bf16" else 4,
+                    gate="channel" if w.kind == "gla" else "head", n_docs=n_docs if n_docs is not None else w.B,
+                    initial_state=w.initial_state, final_state=w.final_state, dht=w.final_state, chunk=w.chunk)
+
+
+def aggregate(step_ms_per_rank, tokens_per_rank_step, steps):
+    """Whole-job throughput: the slowest rank's time, the tokens of all ranks."""
+    t = max(step_ms_per_rank)
+    n = len(step_ms_per_rank)
+    return t, n * tokens_per_rank_step / (t / 1e3), steps
+
+
+# ---------------------------------------------------------------- clocks ----
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            sel = []
+            try:
+                import torch
+
+                uuid = torch.cuda.get_device_properties(self.device_index).uuid
+                sel = ["-i", "GPU-" + str(uuid)]
+            except Exception:
+                sel = []
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50", *sel],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self, t_start=None):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        # samples after the first 0.3 s warm-up of the sampler cover the timed loop
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ----------------------------------------------------------- CPU oracle ----
+def oracle_sample(d, rows, threads=None):
+    """Times the oracle fwd+bwd on batch rows `rows` (all heads); returns seconds."""
+    import oracle
+
+    sl = lambda t: None if t is None else t[rows[0]:rows[-1] + 1]
+    t0 = time.perf_counter()
+    oracle.fwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), d["scale"], None, None, threads=threads)
+    oracle.bwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), sl(d["do"]), d["scale"], None, None, None,
+               threads=threads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from chunked_gated_linear_chunk_gb300 import inputs
+
+    d = inputs.make(w)
+    cores = os.cpu_count() or 1
+    threads = min(cores, w.H)
+    for _ in range(args.warmup):
+        oracle_sample(d, [0], threads)
+    times = [oracle_sample(d, [0], threads) for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    tokens = w.T  # one batch row, all heads
+    value = tokens / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": w.chunk,
+                   "sample": "one batch row (T tokens, all heads) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"fp64 token-by-token oracle fwd+bwd on batch row 0 ({w.T} tokens x {w.H} heads) per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------- GPU arm ----
+def run_glacore(args, w):
+    import torch
+
+    import chunked_gated_linear_chunk_gb300 as glc
+    from chunked_gated_linear_chunk_gb300 import inputs
+    from chunked_gated_linear_chunk_gb300 import roofline as rf
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    glc.load()
+    d = inputs.make(w)
+    x = inputs.to_device(d, dev)
+    scale = d["scale"]
+    o = torch.empty_like(x["v"])
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    dg = torch.empty_like(x["g"])
+    # size the workspaces through the ABI
+    p, _ = glc._problem(x["q"], x["k"], x["v"], x["g"], scale, None, None, 64, None, False)
+    nf, nb = glc.workspace_size(p, "gla_fwd"), glc.workspace_size(p, "gla_bwd")
+    fws = torch.empty(max(nf, 256), dtype=torch.uint8, device=dev)
+    bws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step():
+        glc.gla_fwd(x["q"], x["k"], x["v"], x["g"], scale, out=o, workspace=fws)
+        glc.gla_bwd(x["q"], x["k"], x["v"], x["g"], x["do"], scale, outs=(dq, dk, dv, dg, None), workspace=bws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    glc.get_device_error()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    tfs = [glc.LaunchTimer(4) for _ in range(K)]
+    tbs = [glc.LaunchTimer(6) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            starts[i].record()
+            with tfs[i]:
+                glc.gla_fwd(x["q"], x["k"], x["v"], x["g"], scale, out=o, workspace=fws)
+            with tbs[i]:
+                glc.gla_bwd(x["q"], x["k"], x["v"], x["g"], x["do"], scale, outs=(dq, dk, dv, dg, None),
+                            workspace=bws)
+            ends[i].record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    glc.get_device_error()
+    clocks = clk.summary()
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = statistics.mean(step_ms)
+    # per-kernel durations from the library's launch events
+    per_kernel = {}
+    launches = 0
+    fwd_ms, bwd_ms = [], []
+    for i in range(K):
+        prev = starts[i]
+        for lab, ev in zip(tfs[i].labels, tfs[i].events):
+            per_kernel.setdefault(lab, []).append(prev.elapsed_time(ev))
+            prev = ev
+        fwd_ms.append(starts[i].elapsed_time(prev))
+        fprev = prev
+        for lab, ev in zip(tbs[i].labels, tbs[i].events):
+            per_kernel.setdefault(lab, []).append(prev.elapsed_time(ev))
+            prev = ev
+        bwd_ms.append(fprev.elapsed_time(prev))
+        launches += len(tfs[i].labels) + len(tbs[i].labels)
+
+    if world > 1:
+        t = torch.tensor([ms_local], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    else:
+        ms = ms_local
+    tokens = w.B * w.T
+    value = world * tokens / (ms / 1e3)
+
+    peaks, peak_kind = load_peaks()
+    shp = shape_of(w)
+    flops = rf.fwd_flops(shp) + rf.bwd_flops(shp)
+    nbytes = rf.fwd_bytes(shp) + rf.bwd_bytes(shp)
+    t_roof = rf.roofline_time_s(flops, nbytes, peaks["bf16_tflops"], peaks["hbm_gbs"])
+    kern_us = {k: 1e3 * statistics.mean(v) for k, v in per_kernel.items()}
+    dom = max(kern_us, key=kern_us.get)
+    dom_bytes = rf.kernel_bytes(shp, dom)
+    achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tinfo = json.load(open(tpath)).get(dom)
+            if tinfo and tinfo.get("source_sha") == kernel_source_sha():
+                traffic = tinfo.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, d, x, scale, (o, dq, dk, dv, dg), fws, bws, dev, world)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rows = list(range(w.B))
+        threads = os.cpu_count() or 1
+        secs = oracle_sample(d, rows, threads)
+        cpu = {"value": len(rows) * w.T / secs, "unit": UNIT, "cores": min(threads, len(rows) * w.H),
+               "kind": "oracle",
+               "sample": f"fp64 token-by-token oracle fwd+bwd over the whole batch ({w.B}x{w.T} tokens, "
+                         f"{w.H} heads), {secs:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": w.chunk,
+                   "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}"},
+        "tflops": flops / (ms * 1e-3) / 1e12,
+        "step_roofline": {"roofline_us": t_roof * 1e6, "measured_us": ms * 1e3, "frac": t_roof / (ms * 1e-3),
+                          "peak": peak_kind},
+        "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms),
+        "kernels_us": kern_us,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_bytes, "peak_kind": peak_kind},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, d, x, scale, outs, fws, bws, dev, world):
+    import torch
+
+    import chunked_gated_linear_chunk_gb300 as glc
+
+    names_in = ("q", "k", "v", "g", "do")
+    host_in = {n: d[n].pin_memory() for n in names_in}
+    host_out = [t.detach().to("cpu").pin_memory() for t in outs]
+    o, dq, dk, dv, dg = outs
+    K = max(3, min(args.steps, 50))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    def one(i=None):
+        if i is not None:
+            starts[i].record()
+        for n in names_in:
+            x[n].copy_(host_in[n], non_blocking=True)
+        glc.gla_fwd(x["q"], x["k"], x["v"], x["g"], scale, out=o, workspace=fws)
+        glc.gla_bwd(x["q"], x["k"], x["v"], x["g"], x["do"], scale, outs=(dq, dk, dv, dg, None), workspace=bws)
+        for hdst, dsrc in zip(host_out, outs):
+            hdst.copy_(dsrc, non_blocking=True)
+        if i is not None:
+            ends[i].record()
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    for i in range(K):
+        one(i)
+    torch.cuda.synchronize()
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in names_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    return {"value": world * w.B * w.T / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K}
+
+
+def kernel_source_sha():
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_gated_linear_chunk_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="glacore", choices=["glacore", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    from chunked_gated_linear_chunk_gb300 import inputs
+
+    w = inputs.WORKLOADS[WORKLOAD_INDEX]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_glacore(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -40,6 +40,7 @@ EXPORTS = (
     "gla_fwd", "gla_bwd", "ssd_fwd", "ssd_bwd", "gla_fwd_workspace_size", "gla_bwd_workspace_size",
     "ssd_fwd_workspace_size", "ssd_bwd_workspace_size", "glacore_count_docs",
     "glacore_get_device_error", "glacore_status_string", "glacore_version",
+    "glacore_set_timing_events", "glacore_timing_count", "glacore_timing_label",
 )
 
 
@@ -105,6 +106,12 @@ def load(path: str | None = None):
         lib.glacore_status_string.argtypes = [ctypes.c_int]
         lib.glacore_version.restype = ctypes.c_int
         lib.glacore_version.argtypes = []
+        lib.glacore_set_timing_events.restype = None
+        lib.glacore_set_timing_events.argtypes = [P, ctypes.c_int]
+        lib.glacore_timing_count.restype = ctypes.c_int
+        lib.glacore_timing_count.argtypes = []
+        lib.glacore_timing_label.restype = ctypes.c_char_p
+        lib.glacore_timing_label.argtypes = [ctypes.c_int]
         if path is None:
             _lib = lib
         return lib
@@ -161,6 +168,33 @@ def count_docs(segment_ids: torch.Tensor) -> int:
     out = torch.empty(1, dtype=torch.int64, device=seg.device)
     _check(load().glacore_count_docs(_ptr(seg), B, T, _ptr(out), _stream(seg.device)), "count_docs")
     return int(out.item())
+
+
+class LaunchTimer:
+    """Per-kernel CUDA-event timing through the library's measurement hook.
+
+    ``with LaunchTimer(n) as t: gla_fwd(...)`` records one event after each
+    kernel launch of the call; ``t.labels`` names the kernels and
+    ``t.events`` holds the torch events (elapsed times are read after a
+    synchronize)."""
+
+    def __init__(self, n: int = 8):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in self.events:  # create the underlying CUDA events
+            e.record()
+        self._arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in self.events])
+        self.labels = []
+
+    def __enter__(self):
+        load().glacore_set_timing_events(ctypes.cast(self._arr, ctypes.c_void_p), len(self.events))
+        return self
+
+    def __exit__(self, *exc):
+        lib = load()
+        n = lib.glacore_timing_count()
+        self.labels = [lib.glacore_timing_label(i).decode() for i in range(n)]
+        lib.glacore_set_timing_events(None, 0)
+        return False
 
 
 def get_device_error():

@@ -11,6 +11,21 @@ namespace glacore {
 
 __device__ int g_device_error = 0;
 
+// Optional per-launch timing marks (measurement hook used by the bench):
+// after each kernel launch of a call, the next caller-provided event is
+// recorded on the call's stream.  Thread-local; off unless set.
+static thread_local cudaEvent_t *t_events = nullptr;
+static thread_local int t_nev = 0, t_used = 0;
+static thread_local const char *t_labels[64];
+
+void mark_launch(const char *label, cudaStream_t st) {
+  if (t_events && t_used < t_nev) {
+    cudaEventRecord(t_events[t_used], st);
+    if (t_used < 64) t_labels[t_used] = label;
+    ++t_used;
+  }
+}
+
 // Device address of g_device_error for the current device (looked up once
 // per device; kernels receive it as an argument).
 static int *device_error_ptr() {
@@ -105,6 +120,7 @@ __global__ void count_kernel(const int32_t *seg, int64_t B, int64_t T, unsigned 
 cudaError_t launch_prep(const int32_t *seg, int64_t B, int64_t T, int64_t n_seqs, int chunk,
                         int64_t *start, int64_t *cbase, int *err, cudaStream_t st) {
   prep_kernel<<<1, 1024, 0, st>>>(seg, B, T, n_seqs, chunk, start, cbase, err);
+  mark_launch("segment_prep", st);
   return cudaGetLastError();
 }
 
@@ -153,7 +169,7 @@ bool simt_supported(const glacore_problem *p) { return p->K <= 128 && p->V <= 12
 Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
   Layout L;
   memset(&L, 0, sizeof(L));
-  L.tc = tc::supported(p, head_gate);
+  L.tc = tc::supported(p, head_gate, backward);
   L.chunk = L.tc ? tc::chunk_of(p) : simt::SC;
   const int64_t BT = p->B * p->T, n = p->n_seqs;
   size_t off = 0;
@@ -318,18 +334,22 @@ size_t ssd_bwd_workspace_size(const glacore_problem *p) { return ws_size(p, true
 
 glacore_status gla_fwd(const glacore_problem *p, void *o, float *final_state,
                        glacore_stream_t stream) {
+  t_used = 0;
   return run_fwd(p, false, o, final_state, (cudaStream_t)stream);
 }
 glacore_status ssd_fwd(const glacore_problem *p, void *o, float *final_state,
                        glacore_stream_t stream) {
+  t_used = 0;
   return run_fwd(p, true, o, final_state, (cudaStream_t)stream);
 }
 glacore_status gla_bwd(const glacore_problem *p, const void *do_, const float *dht, void *dq,
                        void *dk, void *dv, float *dg, float *dh0, glacore_stream_t stream) {
+  t_used = 0;
   return run_bwd(p, false, do_, dht, dq, dk, dv, dg, dh0, (cudaStream_t)stream);
 }
 glacore_status ssd_bwd(const glacore_problem *p, const void *do_, const float *dht, void *dq,
                        void *dk, void *dv, float *dg, float *dh0, glacore_stream_t stream) {
+  t_used = 0;
   return run_bwd(p, true, do_, dht, dq, dk, dv, dg, dh0, (cudaStream_t)stream);
 }
 
@@ -371,5 +391,15 @@ const char *glacore_status_string(glacore_status s) {
 }
 
 int glacore_version(void) { return 100; }
+
+void glacore_set_timing_events(void *events, int n_events) {
+  t_events = (cudaEvent_t *)events;
+  t_nev = events ? n_events : 0;
+  t_used = 0;
+}
+int glacore_timing_count(void) { return t_used; }
+const char *glacore_timing_label(int i) {
+  return (i >= 0 && i < t_used && i < 64) ? t_labels[i] : "";
+}
 
 }  // extern "C"

@@ -82,6 +82,9 @@ size_t fwd_smem(int64_t K);
 size_t bwd_smem(int64_t K, int64_t V);
 }  // namespace simt
 
+// Records the next caller-provided timing event (if any) after a launch.
+void mark_launch(const char *label, cudaStream_t st);
+
 // ---- segment prep ------------------------------------------------------
 cudaError_t launch_prep(const int32_t *seg, int64_t B, int64_t T, int64_t n_seqs, int chunk,
                         int64_t *start, int64_t *cbase, int *err, cudaStream_t st);

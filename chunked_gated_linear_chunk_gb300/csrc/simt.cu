@@ -308,10 +308,12 @@ cudaError_t launch_fwd(const Prob &p, const Docs &docs, int dtype, void *o, floa
     auto k = fwd_kernel<__nv_bfloat16>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, st>>>(p, docs, (__nv_bfloat16 *)o, ht, ws_states);
+    mark_launch(o ? "simt_fwd" : "simt_state_pass", st);
   } else {
     auto k = fwd_kernel<float>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, st>>>(p, docs, (float *)o, ht, ws_states);
+    mark_launch(o ? "simt_fwd" : "simt_state_pass", st);
   }
   return cudaGetLastError();
 }
@@ -329,12 +331,14 @@ cudaError_t launch_bwd(const Prob &p, const Docs &docs, int dtype, const void *d
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, st>>>(p, docs, (const T *)dO, dht, ws_states, ws_final, (T *)dq,
                                (T *)dk, dq_acc, dk_acc, (T *)dv, dg, dh0);
+    mark_launch("simt_bwd", st);
   } else {
     using T = float;
     auto k = bwd_kernel<T>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, st>>>(p, docs, (const T *)dO, dht, ws_states, ws_final, (T *)dq,
                                (T *)dk, dq_acc, dk_acc, (T *)dv, dg, dh0);
+    mark_launch("simt_bwd", st);
   }
   return cudaGetLastError();
 }
@@ -346,6 +350,7 @@ cudaError_t launch_convert(const float *src, void *dst, int dtype, int64_t n, cu
     convert_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(src, (__nv_bfloat16 *)dst, n);
   else
     convert_kernel<float><<<blocks, 256, 0, st>>>(src, (float *)dst, n);
+  mark_launch("convert", st);
   return cudaGetLastError();
 }
 

@@ -8,7 +8,7 @@ namespace tc {
 
 // True when the tcgen05 kernels cover this problem (bf16, K = V = 128,
 // per-key-channel gate with one q/k head per value head).
-bool supported(const glacore_problem *p, bool head_gate);
+bool supported(const glacore_problem *p, bool head_gate, bool backward);
 // Chunk length used by the tcgen05 kernels for this problem.
 int chunk_of(const glacore_problem *p);
 // Scratch the tcgen05 path needs (state workspace of the backward).

@@ -30,13 +30,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// try_wait with a suspend-time hint (ns): the warp sleeps in hardware until
+// the phase completes or the hint elapses, instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
@@ -70,6 +72,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, int
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+// L2 prefetch of a tile (no shared memory involved)
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   (uint64_t)m),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 
 // generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA)
@@ -180,6 +190,17 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // rows = K it is the MN-major layout.
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c, uint32_t rows) {
   return (c >> 6) * rows * 128u + r * 128u + ((((c & 63u) >> 3) ^ (r & 7u)) << 4) + (c & 7u) * 2u;
+}
+
+// Byte offset of fp32 element (r, c) of a tile stored as 32-column blocks
+// (128-byte rows) with the 128-byte swizzle, `rows` rows per block.
+__device__ __forceinline__ uint32_t sw128_off_f32(uint32_t r, uint32_t c, uint32_t rows) {
+  return (c >> 5) * rows * 128u + r * 128u + ((((c & 31u) >> 2) ^ (r & 7u)) << 4) + (c & 3u) * 4u;
+}
+
+// Named barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace ptx

@@ -156,6 +156,18 @@ const char *glacore_status_string(glacore_status s);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int glacore_version(void);
 
+/* Measurement hook.  After this call, every kernel launch made by the next
+ * gla_ / ssd_ entry call on this host thread is followed by a record of the
+ * next event of `events` (cudaEvent_t[n_events], created by the caller) on
+ * the call's stream, so the caller can time each kernel with
+ * cudaEventElapsedTime.  Each entry call restarts at events[0].  Pass NULL
+ * to switch it off.  glacore_timing_count() returns how many events the
+ * last call recorded and glacore_timing_label(i) names the kernel launched
+ * just before events[i] (static string). */
+void glacore_set_timing_events(void *events, int n_events);
+int glacore_timing_count(void);
+const char *glacore_timing_label(int i);
+
 #ifdef __cplusplus
 }
 #endif
