@@ -15,7 +15,7 @@ HEADER = os.path.join(ROOT, "include", "glacore.h")
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*(?:size_t|glacore_status|const char \*|int)\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    names = re.findall(r"^\s*(?:size_t|glacore_status|const char \*|int|void)\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
     return sorted(set(names))
 
 
