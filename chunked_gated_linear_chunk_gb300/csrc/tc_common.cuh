@@ -1,0 +1,170 @@
+// tc_common.cuh -- helpers shared by the tcgen05 GLA kernels (tensor maps,
+// operand descriptors, packed bf16 shared/global stores, swizzled row
+// addressing).  K = V = 128, chunk C = 64.
+#pragma once
+
+#include "tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace glacore {
+namespace tc {
+
+using namespace ptx;
+
+constexpr int C = 64;
+constexpr int KD = 128;
+constexpr int VD = 128;
+constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s: bounded waits
+
+typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                             const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                             const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                             CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeFn)p;
+  }
+  return fn;
+}
+
+// 3-D map over a [BT, heads, D] tensor: dims (D, heads, BT), box
+// (box_x, 1, C tokens), 128-byte swizzle (box_x = 64 bf16 or 32 fp32
+// elements: one 128-byte row per token).
+inline bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t D, int64_t heads,
+                     int64_t BT, int box_x) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  const int es = bf16 ? 2 : 4;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)BT};
+  cuuint64_t strides[2] = {(cuuint64_t)(D * es), (cuuint64_t)(heads * D * es)};
+  cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                   const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ float bf16_at(const uint8_t *tile, uint32_t off) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
+}
+__device__ __forceinline__ void put_bf16(uint8_t *tile, uint32_t off, float x) {
+  *reinterpret_cast<__nv_bfloat16 *>(tile + off) = __float2bfloat16_rn(x);
+}
+
+// K-major descriptor step ks (16 elements along K) of a tile whose K extent
+// is split into 64-element column blocks of `rows` rows each.
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks, uint32_t rows) {
+  return sdesc_sw128(base + (uint32_t)(ks >> 2) * rows * 128u + (uint32_t)(ks & 3) * 32u, 16,
+                     1024);
+}
+// MN-major descriptor step ks (16 rows along K) of a tile of K rows whose
+// M/N extent is split into 64-element column blocks `blk` bytes apart.
+__device__ __forceinline__ uint64_t mdesc(uint32_t base, int ks, uint32_t blk) {
+  return sdesc_sw128(base + (uint32_t)ks * 2048u, blk, 1024);
+}
+
+
+// Per-thread TMEM helpers for 32-column blocks (32x32b shape, .x32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// Masked copy of a C x C fp32 accumulator (M = 64 TMEM layout: row r in
+// lane 32 (r / 16) + r % 16) into a bf16 K-major tile [row][col] with the
+// 128-byte swizzle, keeping col <= row and zeroing the rest.  Called by a
+// whole warp of the epilogue warpgroup (warp quarter qw).
+__device__ __forceinline__ void mask_tile_to_smem(uint32_t t_acc, uint32_t lane_off, int qw, int lane,
+                                                  uint8_t *tile) {
+  const int row = qw * 16 + lane;
+#pragma unroll
+  for (int cb = 0; cb < 4; ++cb) {
+    uint32_t r[16];
+    tmem_ld16(t_acc + lane_off + cb * 16, r);
+    tmem_ld_wait(r);
+    if (lane < 16) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c0 = cb * 16 + hb * 8 + 2 * e;
+          const float x0 = c0 <= row ? __uint_as_float(r[hb * 8 + 2 * e]) : 0.f;
+          const float x1 = c0 + 1 <= row ? __uint_as_float(r[hb * 8 + 2 * e + 1]) : 0.f;
+          w[e] = pack_bf16(x0, x1);
+        }
+        st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
+}  // namespace tc
+}  // namespace glacore

@@ -27,91 +27,10 @@
 // the output tile) put row r in lane 32 * (r / 16) + r % 16.
 #include <stdio.h>
 
-#include "tc.cuh"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace glacore {
 namespace tc {
-
-using namespace ptx;
-
-constexpr int C = 64;
-constexpr int KD = 128;
-constexpr int VD = 128;
-constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s: bounded waits
-
-typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                             const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                             const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                             CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeFn encoder() {
-  static EncodeFn fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeFn)p;
-  }
-  return fn;
-}
-
-// 3-D map over a [BT, heads, D] tensor: dims (D, heads, BT), box
-// (box_x, 1, C tokens), 128-byte swizzle (box_x = 64 bf16 or 32 fp32
-// elements: one 128-byte row per token).
-static bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t D, int64_t heads,
-                     int64_t BT, int box_x) {
-  EncodeFn enc = encoder();
-  if (!enc) return false;
-  const int es = bf16 ? 2 : 4;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)BT};
-  cuuint64_t strides[2] = {(cuuint64_t)(D * es), (cuuint64_t)(heads * D * es)};
-  cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-                   const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-__device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-__device__ __forceinline__ float bf16_at(const uint8_t *tile, uint32_t off) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
-}
-__device__ __forceinline__ void put_bf16(uint8_t *tile, uint32_t off, float x) {
-  *reinterpret_cast<__nv_bfloat16 *>(tile + off) = __float2bfloat16_rn(x);
-}
-
-// K-major descriptor step ks (16 elements along K) of a tile whose K extent
-// is split into 64-element column blocks of `rows` rows each.
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks, uint32_t rows) {
-  return sdesc_sw128(base + (uint32_t)(ks >> 2) * rows * 128u + (uint32_t)(ks & 3) * 32u, 16,
-                     1024);
-}
-// MN-major descriptor step ks (16 rows along K) of a tile of K rows whose
-// M/N extent is split into 64-element column blocks `blk` bytes apart.
-__device__ __forceinline__ uint64_t mdesc(uint32_t base, int ks, uint32_t blk) {
-  return sdesc_sw128(base + (uint32_t)ks * 2048u, blk, 1024);
-}
 
 // =========================================================================
 // Forward: grid (2 * n_docs, H), 448 threads (x = 2 * doc + value half).
@@ -511,13 +430,16 @@ __global__ void __launch_bounds__(448)
 // host side
 // =========================================================================
 
-bool supported(const glacore_problem *p, bool head_gate, bool backward) {
-  if (head_gate || backward) return false;
+bool supported(const glacore_problem *p, bool head_gate, bool) {
+  if (head_gate) return false;
   return p->dtype == GLACORE_BF16 && p->K == KD && p->V == VD && p->Hqk == p->H &&
          (p->chunk_size == 0 || p->chunk_size == 64) && p->B * p->T < ((int64_t)1 << 31);
 }
 int chunk_of(const glacore_problem *) { return C; }
-size_t workspace_bytes(const glacore_problem *, bool, bool) { return 0; }
+size_t bwd_scratch_bytes(const glacore_problem *p);
+size_t workspace_bytes(const glacore_problem *p, bool, bool backward) {
+  return backward ? bwd_scratch_bytes(p) : 0;
+}
 
 cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void *o, float *ht,
                 char *, cudaStream_t st) {
@@ -546,11 +468,6 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   mark_launch("gla_fwd_kernel", st);
   (void)p;
   return cudaGetLastError();
-}
-
-cudaError_t bwd(const Prob &, const Docs &, const glacore_problem *, const void *, const float *,
-                void *, void *, void *, float *, float *, char *, cudaStream_t) {
-  return cudaErrorNotSupported;
 }
 
 }  // namespace tc
