@@ -40,7 +40,7 @@ EXPORTS = (
     "gla_fwd", "gla_bwd", "ssd_fwd", "ssd_bwd", "gla_fwd_workspace_size", "gla_bwd_workspace_size",
     "ssd_fwd_workspace_size", "ssd_bwd_workspace_size", "glacore_count_docs",
     "glacore_get_device_error", "glacore_status_string", "glacore_version",
-    "glacore_set_timing_events", "glacore_timing_count", "glacore_timing_label",
+    "glacore_set_timing_events", "glacore_timing_count", "glacore_timing_label", "gla_bwd_noalloc",
 )
 
 
@@ -89,7 +89,7 @@ def load(path: str | None = None):
             f = getattr(lib, n)
             f.restype = ctypes.c_int
             f.argtypes = [PP, P, P, P]
-        for n in ("gla_bwd", "ssd_bwd"):
+        for n in ("gla_bwd", "ssd_bwd", "gla_bwd_noalloc"):
             f = getattr(lib, n)
             f.restype = ctypes.c_int
             f.argtypes = [PP, P, P, P, P, P, P, P, P]

@@ -137,6 +137,27 @@ glacore_status ssd_bwd(const glacore_problem *p, const void *do_,
                        const float *dht, void *dq, void *dk, void *dv,
                        float *dg, float *dh0, glacore_stream_t stream);
 
+/* gla_bwd without a workspace, for callers that cannot allocate device
+ * memory when they call the backward (for example a host framework that
+ * owns all device memory and gives its plugins no allocator, or a training
+ * loop that forbids allocation after start-up).  The pages have no
+ * counterpart to this entry point.
+ * Same arguments and results as gla_bwd; p->workspace and
+ * p->workspace_bytes are ignored.  The scratch is one fixed device array of
+ * GLACORE_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits; a problem whose gla_bwd_workspace_size exceeds
+ * it is rejected with GLACORE_ERR_WORKSPACE before any launch.  The first
+ * call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the array and it keeps the last call's contents: calls whose
+ * work overlaps on the GPU (other streams, other host threads) race, so the
+ * caller must serialise them.  It makes no cudaMalloc, cudaFree or other
+ * allocating call. */
+#define GLACORE_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
+glacore_status gla_bwd_noalloc(const glacore_problem *p, const void *do_,
+                               const float *dht, void *dq, void *dk, void *dv,
+                               float *dg, float *dh0, glacore_stream_t stream);
+
 /* Counts the documents in segment_ids [B,T] (device pointer) and writes
  * the count, as int64, to *n_docs (DEVICE pointer, 8-byte aligned).
  * Asynchronous on `stream`; the caller reads the count after the stream
