@@ -222,8 +222,8 @@ def run_glacore(args, w):
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    tfs = [glc.LaunchTimer(4) for _ in range(K)]
-    tbs = [glc.LaunchTimer(6) for _ in range(K)]
+    tfs = [glc.LaunchTimer(8) for _ in range(K)]
+    tbs = [glc.LaunchTimer(12) for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()

@@ -46,32 +46,6 @@ static int *device_error_ptr() {
 // exactly as its documents one by one.  A document starts at t = 0 of each
 // row and wherever the id changes from the previous token of the row.
 
-__device__ __forceinline__ int64_t block_excl_scan(int64_t x, int64_t *warp_buf, int64_t &total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int64_t inc = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int64_t y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
-  }
-  if (lane == 31) warp_buf[w] = inc;
-  __syncthreads();
-  if (w == 0) {
-    int64_t s = lane < nw ? warp_buf[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int64_t y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < nw) warp_buf[lane] = s;  // inclusive warp prefix
-  }
-  __syncthreads();
-  const int64_t before = w ? warp_buf[w - 1] : 0;
-  total = warp_buf[nw - 1];
-  __syncthreads();
-  return before + inc - x;
-}
-
 __global__ void __launch_bounds__(1024) prep_kernel(const int32_t *seg, int64_t B, int64_t T,
                                                     int64_t n_seqs, int chunk, int64_t *start,
                                                     int64_t *cbase, int *err) {

@@ -42,6 +42,60 @@ struct Docs {
   }
 };
 
+// A unit of work of the tensor-core kernels: tokens [start, end) of one
+// document, the `piece`-th of the `npieces` consecutive pieces the document
+// is split into (exact sequence split: the state entering a piece comes from
+// a scan over the pieces' local end states).
+struct Unit {
+  int64_t start, end;
+  int32_t doc, piece, npieces, pad;
+};
+
+// Units of a launch: an explicit table (pieces) or, when `table` is null,
+// one unit per document of `docs`.
+struct Units {
+  const Unit *table;
+  Docs docs;
+  __device__ __forceinline__ Unit get(int64_t u) const {
+    if (table) return table[u];
+    Unit r;
+    docs.range(u, r.start, r.end);
+    r.doc = (int32_t)u;
+    r.piece = 0;
+    r.npieces = 1;
+    r.pad = 0;
+    return r;
+  }
+};
+
+// Exclusive block-wide prefix sum (all threads of the block call it; warp
+// sums in `warp_buf[32]`); `total` receives the block total.
+__device__ __forceinline__ int64_t block_excl_scan(int64_t x, int64_t *warp_buf, int64_t &total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_buf[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    int64_t s = lane < nw ? warp_buf[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) warp_buf[lane] = s;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int64_t before = w ? warp_buf[w - 1] : 0;
+  total = warp_buf[nw - 1];
+  __syncthreads();
+  return before + inc - x;
+}
+
 // Problem as the kernels see it (token axis flattened: BT = B * T).
 struct Prob {
   int64_t BT, H, Hqk, K, V;

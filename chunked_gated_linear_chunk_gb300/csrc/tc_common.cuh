@@ -11,9 +11,6 @@ namespace tc {
 
 using namespace ptx;
 
-constexpr int C = 64;
-constexpr int KD = 128;
-constexpr int VD = 128;
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s: bounded waits
 
 typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -123,14 +120,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
-  return v;
+// Plain (compiler-visible) 16-bit shared accesses through a generic pointer,
+// so that independent loads can be batched and scheduled early.
+__device__ __forceinline__ uint16_t ld_u16(const uint8_t *p) {
+  return *reinterpret_cast<const uint16_t *>(p);
 }
-__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
+__device__ __forceinline__ void st_u16(uint8_t *p, uint16_t v) { *reinterpret_cast<uint16_t *>(p) = v; }
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   __nv_bfloat16 h = __float2bfloat16_rn(x);

@@ -27,6 +27,8 @@
 // the output tile) put row r in lane 32 * (r / 16) + r % 16.
 #include <stdio.h>
 
+#include <string.h>
+
 #include "tc_common.cuh"
 
 namespace glacore {
@@ -49,12 +51,15 @@ struct FwdMaps {
   CUtensorMap q, k, v, g;
 };
 struct FwdArgs {
-  Docs docs;
+  Units units;
   int64_t H;
   float scale;
   const float *g;
-  const float *h0;
-  float *ht;
+  const float *h0;    // [n_docs,H,K,V] state entering piece 0, or null
+  const float *sin;   // [units,H,K,V] state entering pieces > 0 (scan output)
+  float *ht;          // [n_docs,H,K,V] final state (written by the last piece)
+  float *lout;        // state-only mode: [units,H,K,V] piece end state from zero
+  float *dout;        // state-only mode: [units,H,K] exp(sum of g over the piece)
   __nv_bfloat16 *o;
   int *err;
 };
@@ -104,7 +109,8 @@ __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
 // Rows t >= L (past the document end) are zeroed.  Writes exp(Gam) of its
 // channels to gam (quarter-0 warps).
 __device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[16], float *gam,
-                                           float *xch, int pw, int lane, int L, float scale) {
+                                           float *xch, int pw, int lane, int L, float scale,
+                                           bool with_q) {
   const int tq = pw >> 1;
   const int c0 = 64 * (pw & 1) + 2 * lane;
   const int t0 = 16 * tq;
@@ -136,17 +142,19 @@ __device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[1
   const float i0 = __frcp_rn(T0), i1 = __frcp_rn(T1);
   const Rows16 rq(q, t0, c0), rk(k, t0, c0);
   uint32_t v[16];
+  if (with_q) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = lds_u32(rq.a[i & 7] + i * 128);
+    for (int i = 0; i < 16; ++i) v[i] = lds_u32(rq.a[i & 7] + i * 128);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    pre0 *= x[i].x;
-    pre1 *= x[i].y;
-    const __nv_bfloat162 qq = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
-    v[i] = (t0 + i < L) ? pack_bf16(scale * __low2float(qq) * pre0, scale * __high2float(qq) * pre1) : 0u;
+    for (int i = 0; i < 16; ++i) {
+      pre0 *= x[i].x;
+      pre1 *= x[i].y;
+      const __nv_bfloat162 qq = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
+      v[i] = (t0 + i < L) ? pack_bf16(scale * __low2float(qq) * pre0, scale * __high2float(qq) * pre1) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sts_u32(rq.a[i & 7] + i * 128, v[i]);
   }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) sts_u32(rq.a[i & 7] + i * 128, v[i]);
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = lds_u32(rk.a[i & 7] + i * 128);
 #pragma unroll
@@ -172,6 +180,11 @@ __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float
                  pack_bf16(S[n + 6], S[n + 7]));
 }
 
+// STATE_ONLY: the piece pass of the exact sequence split -- only the state
+// recurrence from a zero state (no q, no output); writes the piece's end
+// state and its total decay.  Pieces that end their document have nothing
+// to contribute and exit.
+template <bool STATE_ONLY>
 __global__ void __launch_bounds__(448)
     gla_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -183,10 +196,12 @@ __global__ void __launch_bounds__(448)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vb = blockIdx.x & 1, h = blockIdx.y;
-  const int64_t d = blockIdx.x >> 1;
-  int64_t s0, s1;
-  a.docs.range(d, s0, s1);
-  const int nch = (int)((s1 - s0 + C - 1) / C);
+  const int64_t u = blockIdx.x >> 1;
+  const Unit un = a.units.get(u);
+  const int64_t d = un.doc;
+  const int64_t s0 = un.start, s1 = un.end;
+  const bool last_piece = un.piece == un.npieces - 1;
+  const int nch = (STATE_ONLY && last_piece) ? 0 : (int)((s1 - s0 + C - 1) / C);
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -239,17 +254,21 @@ __global__ void __launch_bounds__(448)
           const int tp = (int)(s0 + (int64_t)jp * C);
           for (int x = 0; x < KD; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
           if (jp >= fsm::NS) {
-            tma_prefetch_3d(&maps.q, 0, h, tp);
-            tma_prefetch_3d(&maps.q, 64, h, tp);
+            if (!STATE_ONLY) {
+              tma_prefetch_3d(&maps.q, 0, h, tp);
+              tma_prefetch_3d(&maps.q, 64, h, tp);
+            }
             tma_prefetch_3d(&maps.k, 0, h, tp);
             tma_prefetch_3d(&maps.k, 64, h, tp);
             tma_prefetch_3d(&maps.v, vb * 64, h, tp);
           }
         }
-        mbar_expect_tx(&full[s], 2 * 16384 + 8192);
+        mbar_expect_tx(&full[s], (STATE_ONLY ? 16384 : 2 * 16384) + 8192);
         uint8_t *q = sm + fsm::Q + s * 16384, *k = sm + fsm::K + s * 16384;
-        tma_load_3d(q, &maps.q, 0, h, tok, &full[s]);
-        tma_load_3d(q + 8192, &maps.q, 64, h, tok, &full[s]);
+        if (!STATE_ONLY) {
+          tma_load_3d(q, &maps.q, 0, h, tok, &full[s]);
+          tma_load_3d(q + 8192, &maps.q, 64, h, tok, &full[s]);
+        }
         tma_load_3d(k, &maps.k, 0, h, tok, &full[s]);
         tma_load_3d(k + 8192, &maps.k, 64, h, tok, &full[s]);
         tma_load_3d(sm + fsm::V + s * 8192, &maps.v, vb * 64, h, tok, &full[s]);
@@ -272,6 +291,19 @@ __global__ void __launch_bounds__(448)
           FAIL_AND_BREAK
         }
         ph_prep ^= 1u << st;
+        if (STATE_ONLY) {
+          // U[b] is free once the epilogue has folded chunk j-2 into S
+          if (j >= 2) {
+            if (!mbar_wait(&s_ready[b], (ph_sr >> b) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
+            ph_sr ^= 1u << b;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) mma_bf16(tU, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, ks);
+          mma_commit(&u_full[b]);
+          mma_commit(&empty[st]);
+          continue;
+        }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(ka, ks, 64), idP, ks);
@@ -313,7 +345,8 @@ __global__ void __launch_bounds__(448)
       ph_full ^= 1u << s;
       prep_chunk(sm + fsm::Q + s * 16384, sm + fsm::K + s * 16384, x,
                  reinterpret_cast<float *>(sm + fsm::GAM) + (j & 3) * 128,
-                 reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 512, pw, lane, L, a.scale);
+                 reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 512, pw, lane, L, a.scale,
+                 !STATE_ONLY);
       fence_async_smem();
       mbar_arrive(&prep_done[s]);
       mbar_arrive(&gam_ready[j & 3]);
@@ -328,13 +361,20 @@ __global__ void __launch_bounds__(448)
     const int v0 = vb * 64;
     float S[64];
     {
-      const float *h0 = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD + v0 : nullptr;
+      const float *init = nullptr;
+      if (!STATE_ONLY)
+        init = un.piece == 0 ? (a.h0 ? a.h0 + (d * H + h) * KD * VD : nullptr)
+                             : a.sin + (u * H + h) * KD * VD;
+      if (init) init += (int64_t)c * VD + v0;
 #pragma unroll
-      for (int n = 0; n < 64; ++n) S[n] = h0 ? h0[n] : 0.f;
+      for (int n = 0; n < 64; ++n) S[n] = init ? init[n] : 0.f;
     }
-    store_state_bf16(sm + fsm::S + 16384, c, S);
-    fence_async_smem();
-    mbar_arrive(&s_ready[1]);
+    float decay = 1.f;  // state-only mode: exp(sum of g over the piece)
+    if (!STATE_ONLY) {
+      store_state_bf16(sm + fsm::S + 16384, c, S);
+      fence_async_smem();
+      mbar_arrive(&s_ready[1]);
+    }
     uint32_t ph_p = 0, ph_u = 0, ph_o = 0;
     for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
@@ -342,6 +382,7 @@ __global__ void __launch_bounds__(448)
       const int L = (int)min((int64_t)C, s1 - tok0);
       const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
       // S2: P -> causal mask -> bf16 A operand of the intra-chunk product
+      if (!STATE_ONLY) {
       if (!mbar_wait(&p_full[b], (ph_p >> b) & 1, WAIT_CYCLES)) {
         FAIL_AND_BREAK
       }
@@ -368,6 +409,7 @@ __global__ void __launch_bounds__(448)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[b]);
+      }
       // S3a: state update S <- exp(Gam) (S + kt^T V), bf16 copy for the next readout
       if (!mbar_wait(&u_full[b], (ph_u >> b) & 1, WAIT_CYCLES) ||
           !mbar_wait(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
@@ -383,6 +425,12 @@ __global__ void __launch_bounds__(448)
         tmem_ld_wait(r);
 #pragma unroll
         for (int i = 0; i < 16; ++i) S[cb * 16 + i] = eG * (S[cb * 16 + i] + __uint_as_float(r[i]));
+      }
+      if (STATE_ONLY) {
+        decay *= eG;
+        tc_fence_before();
+        mbar_arrive(&s_ready[b]);
+        continue;
       }
       store_state_bf16(sm + fsm::S + b * 16384, c, S);
       fence_async_smem();
@@ -413,8 +461,14 @@ __global__ void __launch_bounds__(448)
       }
       tc_fence_before();
     }
-    if (a.ht && !*abortp) {
-      float *dst = a.ht + ((d * H + h) * KD + c) * VD + v0;
+    float *dst = nullptr;
+    if (STATE_ONLY && nch > 0) {
+      dst = a.lout + ((u * H + h) * KD + c) * VD + v0;
+      if (vb == 0) a.dout[(u * H + h) * KD + c] = decay;
+    } else if (!STATE_ONLY && a.ht && last_piece) {
+      dst = a.ht + ((d * H + h) * KD + c) * VD + v0;
+    }
+    if (dst && !*abortp) {
 #pragma unroll
       for (int n = 0; n < 64; n += 4)
         *reinterpret_cast<float4 *>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
@@ -436,14 +490,14 @@ bool supported(const glacore_problem *p, bool head_gate, bool) {
          (p->chunk_size == 0 || p->chunk_size == 64) && p->B * p->T < ((int64_t)1 << 31);
 }
 int chunk_of(const glacore_problem *) { return C; }
-size_t bwd_scratch_bytes(const glacore_problem *p);
 size_t workspace_bytes(const glacore_problem *p, bool, bool backward) {
-  return backward ? bwd_scratch_bytes(p) : 0;
+  return tc_layout(p, backward).total;
 }
 
 cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void *o, float *ht,
-                char *, cudaStream_t st) {
+                char *ws, cudaStream_t st) {
   if (docs.n == 0) return cudaSuccess;
+  const TcLayout Lo = tc_layout(p, false);
   FwdMaps maps;
   const int64_t BT = pr.BT;
   if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
@@ -452,7 +506,9 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
       !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32))
     return cudaErrorInvalidValue;
   FwdArgs a;
-  a.docs = docs;
+  memset(&a, 0, sizeof(a));
+  a.units.table = nullptr;
+  a.units.docs = docs;
   a.H = pr.H;
   a.scale = pr.scale;
   a.g = pr.g;
@@ -461,12 +517,56 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   a.o = (__nv_bfloat16 *)o;
   a.err = pr.err;
   const int smem = fsm::BYTES + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gla_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(2 * docs.n), (unsigned)pr.H);
-  gla_fwd_kernel<<<grid, 448, smem, st>>>(maps, a);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gla_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gla_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  const dim3 grid((unsigned)(2 * Lo.max_units), (unsigned)pr.H);
+  if (Lo.pieces) {
+    Unit *ut = (Unit *)(ws + Lo.off_units);
+    int64_t *ub = (int64_t *)(ws + Lo.off_ubase);
+    float *Lb = (float *)(ws + Lo.off_L), *Db = (float *)(ws + Lo.off_D), *Sin = (float *)(ws + Lo.off_sin);
+    if ((e = launch_build_units(docs, Lo.plen, ut, ub, Lo.max_units, st)) != cudaSuccess) return e;
+    a.units.table = ut;
+    FwdArgs as = a;
+    as.lout = Lb;
+    as.dout = Db;
+    as.ht = nullptr;
+    gla_fwd_kernel<true><<<grid, 448, smem, st>>>(maps, as);
+    mark_launch("gla_fwd_piece_state_kernel", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_fwd_scan(docs, ub, pr.H, pr.h0, Lb, Db, Sin, st)) != cudaSuccess) return e;
+    a.sin = Sin;
+  }
+  gla_fwd_kernel<false><<<grid, 448, smem, st>>>(maps, a);
   mark_launch("gla_fwd_kernel", st);
-  (void)p;
+  return cudaGetLastError();
+}
+
+// The forward's state-only piece pass, reused by the backward (tc_gla_bwd.cu).
+cudaError_t fwd_piece_states(const Prob &pr, const Units &units, int64_t max_units, float *Lb,
+                             float *Db, cudaStream_t st) {
+  FwdMaps maps;
+  const int64_t BT = pr.BT;
+  if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
+      !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
+      !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
+      !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32))
+    return cudaErrorInvalidValue;
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.units = units;
+  a.H = pr.H;
+  a.scale = pr.scale;
+  a.g = pr.g;
+  a.lout = Lb;
+  a.dout = Db;
+  a.err = pr.err;
+  const int smem = fsm::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(gla_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  gla_fwd_kernel<true><<<dim3((unsigned)(2 * max_units), (unsigned)pr.H), 448, smem, st>>>(maps, a);
+  mark_launch("gla_fwd_piece_state_kernel", st);
   return cudaGetLastError();
 }
 

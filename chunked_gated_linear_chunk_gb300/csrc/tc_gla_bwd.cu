@@ -27,27 +27,59 @@
 // as in the forward: warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 prep
 // (thread = one key channel x 32 tokens; it stages exp(+-G) into its own
 // TMEM lane), warps 10..13 epilogue.
+#include <string.h>
+
 #include "tc_common.cuh"
 
 namespace glacore {
 namespace tc {
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dO;
+  CUtensorMap q, k, v, dO, dgp;
 };
 struct BwdArgs {
-  Docs docs;
+  Units units;
   int64_t H;
   float scale;
   const float *g;
-  const float *h0;
-  const float *dht;
+  const float *h0;     // [n_docs,H,K,V] or null
+  const float *dht;    // [n_docs,H,K,V] or null
+  const float *sin;    // [units,H,K,V] state entering pieces > 0
+  const float *dhend;  // [units,H,K,V] state gradient leaving pieces but the last
   __nv_bfloat16 *dq, *dk, *dv;
   float *dg, *dh0;
-  float *dgp;   // scratch [BT, H, K] fp32
-  float *bvec;  // scratch [n_docs, H, K] fp32
+  float *dgp;    // scratch [BT, H, K] fp32
+  float *bvec;   // scratch [units, H, K] fp32
+  float *lrout;  // dH-only mode: [units,H,K,V] state gradient at the piece start
+  float *dout;   // dH-only mode: [units,H,K] exp(sum of g over the piece)
+  float *ckpt;   // [slots,H,K,V] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
   int *err;
 };
+
+// Global chunk index of local chunk 0 of a unit (document chunk base plus
+// the piece's offset inside its document).
+__device__ __forceinline__ int64_t unit_chunk0(const Units &us, const Unit &un) {
+  int64_t ds, de;
+  us.docs.range(un.doc, ds, de);
+  return us.docs.chunk_base(un.doc) + (un.start - ds) / C;
+}
+// Checkpoint slot of the boundary after global chunk gc, or -1.  Slots are
+// floor(gc / CKPT_CHUNKS): boundaries of one document are CKPT_CHUNKS chunks
+// apart and documents are disjoint chunk ranges, so slots never collide.
+__device__ __forceinline__ int64_t ckpt_slot(int64_t gc0, int64_t doc_c0, int j, int nch) {
+  if (j >= nch - 1) return -1;  // the unit's end uses the piece / document boundary term
+  const int64_t jd = gc0 - doc_c0 + j;  // chunk index inside the document
+  if ((jd + 1) % CKPT_CHUNKS) return -1;
+  return (gc0 + j) / CKPT_CHUNKS;
+}
+
+// State gradient leaving unit u (its end): dht for the document's last
+// piece, the reverse scan's value otherwise.
+__device__ __forceinline__ const float *dh_end_ptr(const BwdArgs &a, const Unit &un, int64_t u,
+                                                   int64_t h) {
+  if (un.piece == un.npieces - 1) return a.dht ? a.dht + ((int64_t)un.doc * a.H + h) * KD * VD : nullptr;
+  return a.dhend + (u * a.H + h) * KD * VD;
+}
 
 #define BW_FAIL_AND_BREAK         \
   {                               \
@@ -108,17 +140,19 @@ __global__ void __launch_bounds__(448)
     gla_bwd_dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full[asm_::NS], empty[asm_::NS], prep_done[asm_::NS], dp_full[2],
-      dp_ready[2], dq_full[2], u_full, s_ready, eg_ready[2], eg_free[2];
+  __shared__ uint64_t full[asm_::NS], empty[asm_::NS], qfull[asm_::NS], qempty[asm_::NS],
+      prep_done[asm_::NS], dp_full[2], dp_ready[2], dq_full[2], u_full, s_ready, eg_ready[2],
+      eg_free[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int64_t d = blockIdx.x;
+  const int64_t u = blockIdx.x;
   const int64_t H = a.H;
-  int64_t s0, s1;
-  a.docs.range(d, s0, s1);
+  const Unit un = a.units.get(u);
+  const int64_t d = un.doc;
+  const int64_t s0 = un.start, s1 = un.end;
   const int nch = (int)((s1 - s0 + C - 1) / C);
 
   if (warp == 1) {
@@ -128,8 +162,10 @@ __global__ void __launch_bounds__(448)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < asm_::NS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + 128);  // MMA commit + epilogue (reads raw q)
+      mbar_init(&full[i], 1);    // k, v, do (released by the MMA commit)
+      mbar_init(&empty[i], 1);
+      mbar_init(&qfull[i], 1);   // raw q (read only by the epilogue)
+      mbar_init(&qempty[i], 128);
       mbar_init(&prep_done[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
@@ -154,7 +190,7 @@ __global__ void __launch_bounds__(448)
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&maps.q);
+      // ring of k, v, do: released when the chunk's MMAs have completed
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.dO);
@@ -167,19 +203,30 @@ __global__ void __launch_bounds__(448)
         if (j + 2 < nch) {
           const int tp = tok + 2 * C;
           for (int x = 0; x < 128; x += 64) {
-            tma_prefetch_3d(&maps.q, x, h, tp);
             tma_prefetch_3d(&maps.k, x, h, tp);
             tma_prefetch_3d(&maps.v, x, h, tp);
             tma_prefetch_3d(&maps.dO, x, h, tp);
           }
         }
-        mbar_expect_tx(&full[st], 4 * 16384);
+        mbar_expect_tx(&full[st], 3 * 16384);
         for (int x = 0; x < 2; ++x) {
-          tma_load_3d(sm + asm_::Q + st * 16384 + x * 8192, &maps.q, 64 * x, h, tok, &full[st]);
           tma_load_3d(sm + asm_::K + st * 16384 + x * 8192, &maps.k, 64 * x, h, tok, &full[st]);
           tma_load_3d(sm + asm_::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &full[st]);
           tma_load_3d(sm + asm_::DO + st * 16384 + x * 8192, &maps.dO, 64 * x, h, tok, &full[st]);
         }
+      }
+    } else if (lane == 1) {
+      // ring of raw q: released by the epilogue after q (.) dq
+      tma_prefetch_desc(&maps.q);
+      for (int j = 0; j < nch; ++j) {
+        const int st = j % asm_::NS;
+        if (j >= asm_::NS && !mbar_wait(&qempty[st], ((j / asm_::NS) - 1) & 1, WAIT_CYCLES))
+          BW_FAIL_AND_BREAK
+        if (*abortp) break;
+        const int tok = (int)(s0 + (int64_t)j * C);
+        mbar_expect_tx(&qfull[st], 16384);
+        for (int x = 0; x < 2; ++x)
+          tma_load_3d(sm + asm_::Q + st * 16384 + x * 8192, &maps.q, 64 * x, h, tok, &qfull[st]);
       }
     }
   } else if (warp == 1) {
@@ -259,15 +306,18 @@ __global__ void __launch_bounds__(448)
       {
         const float inv = __frcp_rn(cg.total);
         uint8_t *kt = sm + asm_::K + st * 16384;
+        uint16_t kb[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) kb[i] = ld_u16(kt + sw128_off(32 * th + i, c, 64));
         float suf = cg.after;
 #pragma unroll
         for (int i = 31; i >= 0; --i) {
           const int t = 32 * th + i;
-          const uint32_t ad = smem_u32(kt + sw128_off(t, c, 64));
-          const float kv = bf16_bits_to_f32(lds_u16(ad));
-          sts_u16(ad, f32_to_bf16_bits(t < L ? kv * suf * inv : 0.f));
+          kb[i] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[i]) * suf * inv : 0.f);
           suf *= cg.x[i];
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) st_u16(kt + sw128_off(32 * th + i, c, 64), kb[i]);
       }
       tmem_st_wait();
       fence_async_smem();
@@ -282,7 +332,9 @@ __global__ void __launch_bounds__(448)
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     // S (TMEM) = h0, bf16 copy for chunk 0's readout
     {
-      const float *h0 = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
+      const float *h0 = un.piece == 0 ? (a.h0 ? a.h0 + (d * H + h) * KD * VD : nullptr)
+                                      : a.sin + (u * H + h) * KD * VD;
+      if (h0) h0 += (int64_t)c * VD;
       uint8_t *St = sm + asm_::S + 32768;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
@@ -304,6 +356,7 @@ __global__ void __launch_bounds__(448)
       mbar_arrive(&s_ready);
     }
     uint32_t ph_dpf = 0, ph_dqf = 0, ph_egr = 0;
+    const int64_t gc0 = unit_chunk0(a.units, un), doc_c0 = a.units.docs.chunk_base(un.doc);
     // dq epilogue of chunk jj (buffer bb): dq = scale exp(G) acc, suffix of q dq
     auto dq_epilogue = [&](int jj) -> bool {
       const int bb = jj & 1, stt = jj % asm_::NS;
@@ -311,32 +364,41 @@ __global__ void __launch_bounds__(448)
       const int L = (int)min((int64_t)C, s1 - tok0);
       if (!mbar_wait(&dq_full[bb], (ph_dqf >> bb) & 1, WAIT_CYCLES)) return false;
       ph_dqf ^= 1u << bb;
+      if (!mbar_wait(&qfull[stt], (jj / asm_::NS) & 1, WAIT_CYCLES)) return false;
       tc_fence_after();
       const uint8_t *qt = sm + asm_::Q + stt * 16384;
       float suf = 0.f;
 #pragma unroll
-      for (int half = 1; half >= 0; --half) {
-        uint32_t acc[32], eg[32];
-        tmem_ld32(tDQ + 64 * bb + lane_off + 32 * half, acc);
-        tmem_ld_wait32(acc);
-        tmem_ld32(tEG + 64 * bb + lane_off + 32 * half, eg);
-        tmem_ld_wait32(eg);
+      for (int blk = 3; blk >= 0; --blk) {
+        uint32_t acc[16], eg[16];
+        tmem_ld16(tDQ + 64 * bb + lane_off + 16 * blk, acc);
+        tmem_ld16(tEG + 64 * bb + lane_off + 16 * blk, eg);
+        uint16_t qb[16];
 #pragma unroll
-        for (int i = 31; i >= 0; --i) {
-          const int t = 32 * half + i;
-          if (t < L) {
-            const float dq = a.scale * __uint_as_float(eg[i]) * __uint_as_float(acc[i]);
-            const float qv = bf16_bits_to_f32(lds_u16(smem_u32(qt + sw128_off(t, c, 64))));
-            suf += qv * dq;
-            const int64_t off = ((tok0 + t) * H + h) * KD + c;
-            a.dq[off] = __float2bfloat16_rn(dq);
-            a.dgp[off] = suf;
+        for (int i = 0; i < 16; ++i) qb[i] = ld_u16(qt + sw128_off(16 * blk + i, c, 64));
+        tmem_ld_wait(acc);
+        tmem_ld_wait(eg);
+        float dqv[16], sv[16];
+#pragma unroll
+        for (int i = 15; i >= 0; --i) {
+          const int t = 16 * blk + i;
+          dqv[i] = a.scale * __uint_as_float(eg[i]) * __uint_as_float(acc[i]);
+          if (t < L) suf += bf16_bits_to_f32(qb[i]) * dqv[i];
+          sv[i] = suf;
+        }
+        __nv_bfloat16 *dq = a.dq + ((tok0 + 16 * blk) * H + h) * KD + c;
+        float *dgp = a.dgp + ((tok0 + 16 * blk) * H + h) * KD + c;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (16 * blk + i < L) {
+            dq[(int64_t)i * H * KD] = __float2bfloat16_rn(dqv[i]);
+            dgp[(int64_t)i * H * KD] = sv[i];
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&eg_free[bb]);
-      mbar_arrive(&empty[stt]);
+      mbar_arrive(&qempty[stt]);
       return true;
     };
     bool ok = true;
@@ -381,6 +443,21 @@ __global__ void __launch_bounds__(448)
                          pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
         }
         tmem_st_wait();
+        const int64_t slot = ckpt_slot(gc0, doc_c0, j, nch);
+        if (slot >= 0) {  // exact boundary state for pass B's gate-gradient carry
+          float *dst = a.ckpt + ((slot * H + h) * KD + c) * VD;
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t r[32];
+            tmem_ld32(tS + lane_off + 32 * cb, r);
+            tmem_ld_wait32(r);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4 *>(dst + 32 * cb + e) =
+                  make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                              __uint_as_float(r[e + 3]));
+          }
+        }
       }
       fence_async_smem();
       tc_fence_before();
@@ -392,8 +469,9 @@ __global__ void __launch_bounds__(448)
     // final-state term of the gate gradient: bvec = (S_T (.) dht) 1_V
     if (!*abortp && a.bvec) {
       float acc = 0.f;
-      if (a.dht) {
-        const float *dh = a.dht + ((d * H + h) * KD + c) * VD;
+      const float *dhe = dh_end_ptr(a, un, u, h);
+      if (dhe) {
+        const float *dh = dhe + (int64_t)c * VD;
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t r[32];
@@ -403,7 +481,7 @@ __global__ void __launch_bounds__(448)
           for (int i = 0; i < 32; ++i) acc += __uint_as_float(r[i]) * dh[32 * cb + i];
         }
       }
-      a.bvec[(d * H + h) * KD + c] = acc;
+      a.bvec[(u * H + h) * KD + c] = acc;
     }
     (void)ok;
   }
@@ -430,22 +508,28 @@ constexpr uint32_t XCH = 212992;   // 2 x 2 x 128 fp32
 constexpr uint32_t BYTES = 215040;
 }  // namespace bsm
 
+// DH_ONLY: the reverse piece pass of the exact sequence split -- only the
+// state-gradient recurrence from zero at the piece end (needs q, g, do);
+// writes the gradient at the piece start and the piece's total decay.
+// First pieces have nothing to contribute and exit.
+template <bool DH_ONLY>
 __global__ void __launch_bounds__(448)
     gla_bwd_rev_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full[bsm::NS], empty[bsm::NS], prep_done[bsm::NS], pdp_full, pdp_ready,
-      dh_ready, kv_full, eg_ready[2], eg_free[2];
+  __shared__ uint64_t full[bsm::NS], empty[bsm::NS], kfull[bsm::NS], kempty[bsm::NS],
+      prep_done[bsm::NS], pdp_full, pdp_ready, dh_ready, kv_full, eg_ready[2], eg_free[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int64_t d = blockIdx.x;
+  const int64_t u = blockIdx.x;
   const int64_t H = a.H;
-  int64_t s0, s1;
-  a.docs.range(d, s0, s1);
-  const int nch = (int)((s1 - s0 + C - 1) / C);
+  const Unit un = a.units.get(u);
+  const int64_t d = un.doc;
+  const int64_t s0 = un.start, s1 = un.end;
+  const int nch = (DH_ONLY && un.piece == 0) ? 0 : (int)((s1 - s0 + C - 1) / C);
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -454,8 +538,10 @@ __global__ void __launch_bounds__(448)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < bsm::NS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + 128);  // MMA commit + epilogue (reads raw k)
+      mbar_init(&full[i], 1);    // q, v, do (kt is written here too): MMA commit
+      mbar_init(&empty[i], 1);
+      mbar_init(&kfull[i], 1);   // raw k: read by the prep and the epilogue
+      mbar_init(&kempty[i], 128);
       mbar_init(&prep_done[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
@@ -480,16 +566,19 @@ __global__ void __launch_bounds__(448)
   // chunks are visited in reverse: iteration i handles chunk j = nch - 1 - i
   if (warp == 0) {
     if (lane == 0) {
+      // ring of q, v, do (+ kt written by the prep): released by the MMA commit
       tma_prefetch_desc(&maps.q);
-      tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.dO);
+      tma_prefetch_desc(&maps.dgp);
       for (int i = 0; i < nch; ++i) {
         const int j = nch - 1 - i, st = i % bsm::NS;
         if (i >= bsm::NS && !mbar_wait(&empty[st], ((i / bsm::NS) - 1) & 1, WAIT_CYCLES))
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
+        if (i == 0)  // gate-gradient partials of the first chunk the epilogue reads
+          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.dgp, x, h, tok);
         if (j - 2 >= 0) {
           const int tp = tok - 2 * C;
           for (int x = 0; x < 128; x += 64) {
@@ -499,13 +588,28 @@ __global__ void __launch_bounds__(448)
             tma_prefetch_3d(&maps.dO, x, h, tp);
           }
         }
-        mbar_expect_tx(&full[st], 4 * 16384);
+        if (j - 1 >= 0)
+          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.dgp, x, h, tok - C);
+        mbar_expect_tx(&full[st], (DH_ONLY ? 2 : 3) * 16384);
         for (int x = 0; x < 2; ++x) {
           tma_load_3d(sm + bsm::Q + st * 16384 + x * 8192, &maps.q, 64 * x, h, tok, &full[st]);
-          tma_load_3d(sm + bsm::K + st * 16384 + x * 8192, &maps.k, 64 * x, h, tok, &full[st]);
-          tma_load_3d(sm + bsm::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &full[st]);
+          if (!DH_ONLY)
+            tma_load_3d(sm + bsm::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &full[st]);
           tma_load_3d(sm + bsm::DO + st * 16384 + x * 8192, &maps.dO, 64 * x, h, tok, &full[st]);
         }
+      }
+    } else if (lane == 1 && !DH_ONLY) {
+      // ring of raw k: released by the epilogue after k (.) dk
+      tma_prefetch_desc(&maps.k);
+      for (int i = 0; i < nch; ++i) {
+        const int j = nch - 1 - i, st = i % bsm::NS;
+        if (i >= bsm::NS && !mbar_wait(&kempty[st], ((i / bsm::NS) - 1) & 1, WAIT_CYCLES))
+          BW_FAIL_AND_BREAK
+        if (*abortp) break;
+        const int tok = (int)(s0 + (int64_t)j * C);
+        mbar_expect_tx(&kfull[st], 16384);
+        for (int x = 0; x < 2; ++x)
+          tma_load_3d(sm + bsm::K + st * 16384 + x * 8192, &maps.k, 64 * x, h, tok, &kfull[st]);
       }
     }
   } else if (warp == 1) {
@@ -523,6 +627,15 @@ __global__ void __launch_bounds__(448)
         const uint32_t va = sbase + bsm::V + st * 16384, doa = sbase + bsm::DO + st * 16384;
         if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_prep ^= 1u << st;
+        if (DH_ONLY) {
+          if (!mbar_wait(&dh_ready, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDH, mdesc(qa, ks, 8192), mdesc(doa, ks, 8192), idH, 1);
+          mma_commit(&kv_full);
+          mma_commit(&empty[st]);
+          continue;
+        }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(kta, ks, 64), idCC, ks);
@@ -561,22 +674,27 @@ __global__ void __launch_bounds__(448)
       const int L = (int)min((int64_t)C, s1 - tok0);
       ChanGate cg;
       load_gates(cg, a.g, tok0, H, h, c, th, L);
-      if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES) ||
+          (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)))
+        BW_FAIL_AND_BREAK
       ph_full ^= 1u << st;
       exchange_gates(cg, reinterpret_cast<float *>(sm + bsm::XCH) + b * 256, c, th, L);
       const float inv = __frcp_rn(cg.total);
       // qt = scale q exp(G) in place
       {
         uint8_t *q = sm + bsm::Q + st * 16384;
+        uint16_t qb[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) qb[u] = ld_u16(q + sw128_off(32 * th + u, c, 64));
         float pre = cg.before;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const int t = 32 * th + u;
           pre *= cg.x[u];
-          const uint32_t ad = smem_u32(q + sw128_off(t, c, 64));
-          const float qv = bf16_bits_to_f32(lds_u16(ad));
-          sts_u16(ad, f32_to_bf16_bits(t < L ? a.scale * qv * pre : 0.f));
+          qb[u] = f32_to_bf16_bits(t < L ? a.scale * bf16_bits_to_f32(qb[u]) * pre : 0.f);
         }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) st_u16(q + sw128_off(32 * th + u, c, 64), qb[u]);
       }
       // kt = k exp(-G) (separate tile; raw k is kept for k (.) dk); exp(-G) -> TMEM
       if (i >= 2) {
@@ -588,16 +706,23 @@ __global__ void __launch_bounds__(448)
         const uint8_t *k = sm + bsm::K + st * 16384;
         uint8_t *kt = sm + bsm::KT + st * 16384;
         uint32_t r[32];
+        uint16_t kb[32];
+        if (!DH_ONLY) {
+#pragma unroll
+          for (int w = 0; w < 32; ++w) kb[w] = ld_u16(k + sw128_off(32 * th + w, c, 64));
+        }
         float suf = cg.after;
 #pragma unroll
-        for (int u = 31; u >= 0; --u) {
-          const int t = 32 * th + u;
+        for (int w = 31; w >= 0; --w) {
+          const int t = 32 * th + w;
           const float e = suf * inv;  // exp(-G_t)
-          r[u] = __float_as_uint(e);
-          const uint32_t off = sw128_off(t, c, 64);
-          const float kv = bf16_bits_to_f32(lds_u16(smem_u32(k + off)));
-          sts_u16(smem_u32(kt + off), f32_to_bf16_bits(t < L ? kv * e : 0.f));
-          suf *= cg.x[u];
+          r[w] = __float_as_uint(e);
+          if (!DH_ONLY) kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
+          suf *= cg.x[w];
+        }
+        if (!DH_ONLY) {
+#pragma unroll
+          for (int w = 0; w < 32; ++w) st_u16(kt + sw128_off(32 * th + w, c, 64), kb[w]);
         }
         tmem_st32(tEG + 64 * b + lane_off + 32 * th, r);
       }
@@ -614,30 +739,35 @@ __global__ void __launch_bounds__(448)
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     // dH = dht (or 0)
     {
-      const float *dh = a.dht ? a.dht + ((d * H + h) * KD + c) * VD : nullptr;
+      const float *dh = DH_ONLY ? nullptr : dh_end_ptr(a, un, u, h);
+      if (dh) dh += (int64_t)c * VD;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t r[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(dh ? dh[32 * cb + u] : 0.f);
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(dh ? dh[32 * cb + e] : 0.f);
         tmem_st32(tDH + lane_off + 32 * cb, r);
       }
       tmem_st_wait();
     }
-    float carry = a.bvec ? a.bvec[(d * H + h) * KD + c] : 0.f;
+    float carry = (!DH_ONLY && a.bvec) ? a.bvec[(u * H + h) * KD + c] : 0.f;
+    const int64_t gc0 = unit_chunk0(a.units, un), doc_c0 = a.units.docs.chunk_base(un.doc);
+    float decay = 1.f;  // dH-only mode: exp(sum of g over the piece)
     uint32_t ph_egr = 0;
     for (int i = 0; i < nch; ++i) {
       const int j = nch - 1 - i, st = i % bsm::NS, b = i & 1;
       const int64_t tok0 = s0 + (int64_t)j * C;
       const int L = (int)min((int64_t)C, s1 - tok0);
       // (1) masked P and dP -> bf16 operands
-      if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-      tc_fence_after();
-      mask_tile_to_smem(tP, lane_off, qw, lane, sm + bsm::P);
-      mask_tile_to_smem(tDP, lane_off, qw, lane, sm + bsm::DP);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&pdp_ready);
+      if (!DH_ONLY) {
+        if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        tc_fence_after();
+        mask_tile_to_smem(tP, lane_off, qw, lane, sm + bsm::P);
+        mask_tile_to_smem(tDP, lane_off, qw, lane, sm + bsm::DP);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&pdp_ready);
+      }
       // (2) dHh = exp(Gam) dH in TMEM, bf16 copy
       if (!mbar_wait(&eg_ready[b], (ph_egr >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
       ph_egr ^= 1u << b;
@@ -647,15 +777,24 @@ __global__ void __launch_bounds__(448)
         tmem_ld16(tEG + 64 * b + lane_off + 48, e1);
         tmem_ld_wait(e1);
         const float eGam = __frcp_rn(__uint_as_float(e1[15]));  // 1 / exp(-Gam)
+        decay *= eGam;
         uint8_t *Dt = sm + bsm::DH;
+        const int64_t slot = DH_ONLY ? -1 : ckpt_slot(gc0, doc_c0, j, nch);
+        const float *ck = slot >= 0 ? a.ckpt + ((slot * H + h) * KD + c) * VD : nullptr;
+        float bnd = 0.f;
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t r[32];
           tmem_ld32(tDH + lane_off + 32 * cb, r);
           tmem_ld_wait32(r);
+          if (ck) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) bnd += ck[32 * cb + e] * __uint_as_float(r[e]);
+          }
 #pragma unroll
           for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(eGam * __uint_as_float(r[u]));
           tmem_st32(tDH + lane_off + 32 * cb, r);
+          if (!DH_ONLY)
 #pragma unroll
           for (int n = 0; n < 32; n += 8)
             st_shared_v4(smem_u32(Dt + sw128_off(c, 32 * cb + n, 128)),
@@ -665,57 +804,77 @@ __global__ void __launch_bounds__(448)
                          pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
         }
         tmem_st_wait();
+        if (ck) carry = bnd;  // exact (S_end (.) dH_end) 1_V at this boundary
       }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&dh_ready);
       // (3) dk, dg (thread = channel c) and dv (thread = value column c)
-      if (!mbar_wait(&kv_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      if (!mbar_wait(&kv_full, i & 1, WAIT_CYCLES) ||
+          (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)))
+        BW_FAIL_AND_BREAK
       tc_fence_after();
-      {
+      if (!DH_ONLY) {
         const uint8_t *k = sm + bsm::K + st * 16384;
         float sk = 0.f, qtot = 0.f;
 #pragma unroll
-        for (int half = 1; half >= 0; --half) {
-          uint32_t acc[32], eg[32];
-          tmem_ld32(tDK + lane_off + 32 * half, acc);
-          tmem_ld_wait32(acc);
-          tmem_ld32(tEG + 64 * b + lane_off + 32 * half, eg);
-          tmem_ld_wait32(eg);
+        for (int blk = 3; blk >= 0; --blk) {
+          uint32_t acc[16], eg[16];
+          tmem_ld16(tDK + lane_off + 16 * blk, acc);
+          tmem_ld16(tEG + 64 * b + lane_off + 16 * blk, eg);
+          const float *src = a.dgp + ((tok0 + 16 * blk) * H + h) * KD + c;
+          float qp[16];
+          uint16_t kb[16];
 #pragma unroll
-          for (int u = 31; u >= 0; --u) {
-            const int t = 32 * half + u;
-            if (t < L) {
-              const float dk = __uint_as_float(eg[u]) * __uint_as_float(acc[u]);
-              const float kv = bf16_bits_to_f32(lds_u16(smem_u32(k + sw128_off(t, c, 64))));
-              sk += kv * dk;
-              const int64_t off = ((tok0 + t) * H + h) * KD + c;
-              const float qpart = a.dgp[off];
-              if (t == 0) qtot = qpart;
-              a.dk[off] = __float2bfloat16_rn(dk);
-              a.dg[off] = qpart - sk + carry;
+          for (int u = 0; u < 16; ++u) {
+            qp[u] = 16 * blk + u < L ? __ldg(src + (int64_t)u * H * KD) : 0.f;
+            kb[u] = ld_u16(k + sw128_off(16 * blk + u, c, 64));
+          }
+          tmem_ld_wait(acc);
+          tmem_ld_wait(eg);
+          float dkv[16], dgv[16];
+#pragma unroll
+          for (int u = 15; u >= 0; --u) {
+            const int t = 16 * blk + u;
+            dkv[u] = __uint_as_float(eg[u]) * __uint_as_float(acc[u]);
+            if (t < L) sk += bf16_bits_to_f32(kb[u]) * dkv[u];
+            dgv[u] = qp[u] - sk + carry;
+          }
+          if (blk == 0) qtot = qp[0];
+          __nv_bfloat16 *dk = a.dk + ((tok0 + 16 * blk) * H + h) * KD + c;
+          float *dg = a.dg + ((tok0 + 16 * blk) * H + h) * KD + c;
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            if (16 * blk + u < L) {
+              dk[(int64_t)u * H * KD] = __float2bfloat16_rn(dkv[u]);
+              dg[(int64_t)u * H * KD] = dgv[u];
             }
           }
         }
         carry += qtot - sk;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t acc[32];
-          tmem_ld32(tDV + lane_off + 32 * half, acc);
-          tmem_ld_wait32(acc);
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t acc[16];
+          tmem_ld16(tDV + lane_off + 16 * blk, acc);
+          tmem_ld_wait(acc);
+          __nv_bfloat16 *dv = a.dv + ((tok0 + 16 * blk) * H + h) * VD + c;
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int t = 32 * half + u;
-            if (t < L) a.dv[((tok0 + t) * H + h) * VD + c] = __float2bfloat16_rn(__uint_as_float(acc[u]));
-          }
+          for (int u = 0; u < 16; ++u)
+            if (16 * blk + u < L) dv[(int64_t)u * H * VD] = __float2bfloat16_rn(__uint_as_float(acc[u]));
         }
       }
       tc_fence_before();
       mbar_arrive(&eg_free[b]);
-      mbar_arrive(&empty[st]);
+      if (!DH_ONLY) mbar_arrive(&kempty[st]);
     }
-    if (!*abortp && a.dh0) {
-      float *dst = a.dh0 + ((d * H + h) * KD + c) * VD;
+    float *dst = nullptr;
+    if (DH_ONLY && nch > 0) {
+      dst = a.lrout + ((u * H + h) * KD + c) * VD;
+      a.dout[(u * H + h) * KD + c] = decay;
+    } else if (!DH_ONLY && a.dh0 && un.piece == 0) {
+      dst = a.dh0 + ((d * H + h) * KD + c) * VD;
+    }
+    if (!*abortp && dst) {
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t r[32];
@@ -735,24 +894,27 @@ __global__ void __launch_bounds__(448)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-size_t bwd_scratch_bytes(const glacore_problem *p) {
-  const int64_t BT = p->B * p->T;
-  return (size_t)BT * p->H * KD * sizeof(float) + (size_t)p->n_seqs * p->H * KD * sizeof(float) + 256;
-}
+cudaError_t fwd_piece_states(const Prob &pr, const Units &units, int64_t max_units, float *Lb,
+                             float *Db, cudaStream_t st);
 
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,
                 const float *dht, void *dq, void *dk, void *dv, float *dg, float *dh0, char *ws,
                 cudaStream_t st) {
   if (docs.n == 0) return cudaSuccess;
+  const TcLayout Lo = tc_layout(p, true);
   BwdMaps maps;
   const int64_t BT = pr.BT;
+  float *dgp = (float *)(ws + Lo.off_dgp);
   if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
-      !make_map(&maps.dO, dO, true, VD, pr.H, BT, 64))
+      !make_map(&maps.dO, dO, true, VD, pr.H, BT, 64) ||
+      !make_map(&maps.dgp, dgp, false, KD, pr.H, BT, 32))
     return cudaErrorInvalidValue;
   BwdArgs a;
-  a.docs = docs;
+  memset(&a, 0, sizeof(a));
+  a.units.table = nullptr;
+  a.units.docs = docs;
   a.H = pr.H;
   a.scale = pr.scale;
   a.g = pr.g;
@@ -763,19 +925,42 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   a.dv = (__nv_bfloat16 *)dv;
   a.dg = dg;
   a.dh0 = dh0;
-  a.dgp = (float *)ws;
-  a.bvec = (float *)(ws + (size_t)BT * pr.H * KD * sizeof(float));
+  a.dgp = dgp;
+  a.bvec = (float *)(ws + Lo.off_bvec);
+  a.ckpt = (float *)(ws + Lo.off_ckpt);
   a.err = pr.err;
-  dim3 grid((unsigned)docs.n, (unsigned)pr.H);
+  const dim3 grid((unsigned)Lo.max_units, (unsigned)pr.H);
   const int smA = asm_::BYTES + 1024, smB = bsm::BYTES + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gla_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smA);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gla_bwd_rev_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smB);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gla_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smA)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gla_bwd_rev_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gla_bwd_rev_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
+    return e;
+  if (Lo.pieces) {
+    Unit *ut = (Unit *)(ws + Lo.off_units);
+    int64_t *ub = (int64_t *)(ws + Lo.off_ubase);
+    float *Lb = (float *)(ws + Lo.off_L), *Db = (float *)(ws + Lo.off_D);
+    float *Sin = (float *)(ws + Lo.off_sin), *Dhe = (float *)(ws + Lo.off_dhend);
+    if ((e = launch_build_units(docs, Lo.plen, ut, ub, Lo.max_units, st)) != cudaSuccess) return e;
+    a.units.table = ut;
+    // states entering every piece (forward piece pass + scan)
+    if ((e = fwd_piece_states(pr, a.units, Lo.max_units, Lb, Db, st)) != cudaSuccess) return e;
+    if ((e = launch_fwd_scan(docs, ub, pr.H, pr.h0, Lb, Db, Sin, st)) != cudaSuccess) return e;
+    // state gradients leaving every piece (reverse piece pass + scan)
+    BwdArgs ar = a;
+    ar.lrout = Lb;
+    ar.dout = Db;
+    gla_bwd_rev_kernel<true><<<grid, 448, smB, st>>>(maps, ar);
+    mark_launch("gla_bwd_piece_dh_kernel", st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_rev_scan(docs, ub, pr.H, dht, Lb, Db, Dhe, st)) != cudaSuccess) return e;
+    a.sin = Sin;
+    a.dhend = Dhe;
+  }
   gla_bwd_dq_kernel<<<grid, 448, smA, st>>>(maps, a);
   mark_launch("gla_bwd_dq_kernel", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gla_bwd_rev_kernel<<<grid, 448, smB, st>>>(maps, a);
+  gla_bwd_rev_kernel<false><<<grid, 448, smB, st>>>(maps, a);
   mark_launch("gla_bwd_rev_kernel", st);
   (void)p;
   return cudaGetLastError();

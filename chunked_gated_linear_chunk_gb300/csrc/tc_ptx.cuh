@@ -7,6 +7,13 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#ifndef GLACORE_WAIT_HINT_NS
+#define GLACORE_WAIT_HINT_NS 20000
+#endif
+#ifndef GLACORE_WAIT_SPIN
+#define GLACORE_WAIT_SPIN 0
+#endif
+
 namespace glacore {
 namespace ptx {
 
@@ -30,6 +37,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Non-blocking probe of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // try_wait with a suspend-time hint (ns): the warp sleeps in hardware until
 // the phase completes or the hint elapses, instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
@@ -38,15 +56,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+      : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)GLACORE_WAIT_HINT_NS)
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false (and sets nothing) if it has not completed within `max_cycles`
-// SM clock cycles; the caller records the timeout and winds down.
+// Bounded wait for the phase with the given parity to complete: a short
+// spin on the non-blocking probe (fast hand-off when the phase is about to
+// complete), then suspend-hinted waits.  Returns false if the phase has not
+// completed within `max_cycles` SM clock cycles; the caller records the
+// timeout and winds down.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long max_cycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < GLACORE_WAIT_SPIN; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
     if (clock64() - t0 > max_cycles) return false;

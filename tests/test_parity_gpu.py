@@ -82,6 +82,11 @@ SMALL = {
                                     final_state=True),
     "gla_fp32_K64_V32": lambda: case(1, 9, B=1, T=70, H=2, Hqk=2, K=64, V=32),
     "gla_bf16_K64_V64": lambda: case(2, 10, B=1, T=130, H=2, Hqk=2, K=64, V=64),
+    # one (document, head) pair: the tensor-core path splits it into pieces
+    "gla_bf16_pieces_T2000": lambda: case(5, 13, B=1, T=2000, H=1, Hqk=1),
+    "gla_bf16_pieces_T1000_nostate": lambda: case(2, 14, B=1, T=1000, H=1, Hqk=1),
+    "gla_bf16_pieces_packed": lambda: case(4, 15, B=1, T=3000, H=1, Hqk=1, doc_mean=700),
+    "gla_bf16_pieces_B2_H2": lambda: case(5, 16, B=2, T=1500, H=2, Hqk=2),
 }
 
 
