@@ -120,6 +120,44 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// Shared-memory addresses of one column c of a tile with the 128-byte
+// swizzle, rows r0 + i (r0 % 8 == 0): the XOR pattern depends only on the
+// row mod 8, so eight bases cover every row and the row term of at(i)
+// folds into the instruction's immediate once loops are unrolled.
+//   ColBf16: bf16 tile of 64-column blocks, 64 rows each (TMA box 64 x 64)
+//   ColF32:  fp32 tile of 32-column blocks, 64 rows each (TMA box 32 x 64)
+struct ColBf16 {
+  uint32_t a[8];
+  __device__ __forceinline__ ColBf16(uint32_t tile, int r0, int c) {
+    const uint32_t b = tile + (uint32_t)(c >> 6) * 8192u + (uint32_t)r0 * 128u + (uint32_t)(c & 7) * 2u;
+    const uint32_t cc = (uint32_t)(c >> 3) & 7u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = b + ((cc ^ (uint32_t)k) << 4);
+  }
+  __device__ __forceinline__ uint32_t at(int i) const { return a[i & 7] + (uint32_t)i * 128u; }
+};
+struct ColF32 {
+  uint32_t a[8];
+  __device__ __forceinline__ ColF32(uint32_t tile, int r0, int c) {
+    const uint32_t b = tile + (uint32_t)(c >> 5) * 8192u + (uint32_t)r0 * 128u + (uint32_t)(c & 3) * 4u;
+    const uint32_t cc = (uint32_t)(c >> 2) & 7u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = b + ((cc ^ (uint32_t)k) << 4);
+  }
+  __device__ __forceinline__ uint32_t at(int i) const { return a[i & 7] + (uint32_t)i * 128u; }
+};
+__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v));
+}
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v));
+}
+
 // Plain (compiler-visible) 16-bit shared accesses through a generic pointer,
 // so that independent loads can be batched and scheduled early.
 __device__ __forceinline__ uint16_t ld_u16(const uint8_t *p) {
@@ -130,6 +168,64 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// In-register 4 x 4 transposes across groups of 4 lanes.  On entry lane l
+// holds v[t] = value of channel (its own) at token t (t = 0..15).  On exit
+// v[4 s + e] = value of channel 4 (l / 4) + e (of the warp's 32) at token
+// 4 s + (l % 4): each lane then owns 4 consecutive channels of one token, so
+// the epilogue can store 8 or 16 contiguous bytes instead of one element.
+// Butterfly over lane bits 1 and 0 (shfl_xor 2, then 1).
+__device__ __forceinline__ void transpose_4x4_blocks(float (&v)[16], int lane) {
+  const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = b1 ? v[4 * s + j] : v[4 * s + j + 2];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
+      if (b1)
+        v[4 * s + j] = recv;
+      else
+        v[4 * s + j + 2] = recv;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      const float send = b0 ? v[4 * s + j] : v[4 * s + j + 1];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+      if (b0)
+        v[4 * s + j] = recv;
+      else
+        v[4 * s + j + 1] = recv;
+    }
+  }
+}
+
+// Stores 16 tokens x 32 channels held as after transpose_4x4_blocks:
+// `row0` points at (token t_base, channel c_base of the warp), rows `stride`
+// elements apart; rows t_base + t >= L are skipped.
+__device__ __forceinline__ void store_block_f32(float *row0, int64_t stride, const float (&v)[16],
+                                                int lane, int t_in_chunk0, int L) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int t = 4 * s + (lane & 3);
+    if (t_in_chunk0 + t < L)
+      *reinterpret_cast<float4 *>(row0 + (int64_t)t * stride + 4 * (lane >> 2)) =
+          make_float4(v[4 * s], v[4 * s + 1], v[4 * s + 2], v[4 * s + 3]);
+  }
+}
+__device__ __forceinline__ void store_block_bf16(__nv_bfloat16 *row0, int64_t stride, const float (&v)[16],
+                                                 int lane, int t_in_chunk0, int L) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int t = 4 * s + (lane & 3);
+    if (t_in_chunk0 + t < L) {
+      uint2 w;
+      w.x = pack_bf16(v[4 * s], v[4 * s + 1]);
+      w.y = pack_bf16(v[4 * s + 2], v[4 * s + 3]);
+      *reinterpret_cast<uint2 *>(row0 + (int64_t)t * stride + 4 * (lane >> 2)) = w;
+    }
+  }
 }
 
 // Masked copy of a C x C fp32 accumulator (M = 64 TMEM layout: row r in

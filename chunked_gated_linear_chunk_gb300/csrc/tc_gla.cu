@@ -331,16 +331,26 @@ __global__ void __launch_bounds__(448)
     const int pw = warp - 2;
     const int c0 = 64 * (pw & 1) + 2 * lane, t0 = 16 * (pw >> 1);
     uint32_t ph_full = 0;
+    // gates of chunk j+1 are loaded into registers while chunk j is prepared
+    float2 xn[16];
+    auto load_x = [&](int jj, float2 (&x)[16]) {
+      const int64_t tk = s0 + (int64_t)jj * C;
+      const int LL = (int)min((int64_t)C, s1 - tk);
+      const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        x[i] = (t0 + i < LL) ? __ldg(reinterpret_cast<const float2 *>(gp + (int64_t)i * a.H * KD))
+                             : make_float2(0.f, 0.f);
+    };
+    if (nch > 0) load_x(0, xn);
     for (int j = 0; j < nch; ++j) {
       const int s = j % fsm::NS;
       const int64_t tok0 = s0 + (int64_t)j * C;
       const int L = (int)min((int64_t)C, s1 - tok0);
       float2 x[16];
-      const float *gp = a.g + ((tok0 + t0) * a.H + h) * KD + c0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        x[i] = (t0 + i < L) ? __ldg(reinterpret_cast<const float2 *>(gp + (int64_t)i * a.H * KD))
-                            : make_float2(0.f, 0.f);
+      for (int i = 0; i < 16; ++i) x[i] = xn[i];
+      if (j + 1 < nch) load_x(j + 1, xn);
       if (!mbar_wait(&full[s], (ph_full >> s) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
       ph_full ^= 1u << s;
       prep_chunk(sm + fsm::Q + s * 16384, sm + fsm::K + s * 16384, x,

@@ -35,7 +35,7 @@ namespace glacore {
 namespace tc {
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dO, dgp;
+  CUtensorMap q, k, v, dO, dgp, dq, g;
 };
 struct BwdArgs {
   Units units;
@@ -106,6 +106,14 @@ __device__ __forceinline__ void load_gates(ChanGate &cg, const float *g, int64_t
     cg.x[i] = t < L ? __ldg(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
   }
 }
+__device__ __forceinline__ void load_gates_to(float (&x)[32], const float *g, int64_t tok0, int64_t H,
+                                              int h, int c, int th, int L) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int t = 32 * th + i;
+    x[i] = t < L ? __ldg(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
+  }
+}
 __device__ __forceinline__ void exchange_gates(ChanGate &cg, float *xch, int c, int th, int L) {
   float p = 1.f;
 #pragma unroll
@@ -126,23 +134,31 @@ __device__ __forceinline__ void exchange_gates(ChanGate &cg, float *xch, int c, 
 // ===========================================================================
 namespace asm_ {  // shared-memory carve-up (bytes)
 constexpr int NS = 2;
-constexpr uint32_t Q = 0;          // 2 x 16 KB raw q
+constexpr uint32_t Q = 0;          // 2 x 16 KB raw q, then dq in place (store source)
 constexpr uint32_t K = 32768;      // 2 x 16 KB k, then kt in place
 constexpr uint32_t V = 65536;      // 2 x 16 KB
 constexpr uint32_t DO = 98304;     // 2 x 16 KB
-constexpr uint32_t DP = 131072;    // 2 x 8 KB masked dP (bf16 [t][s])
-constexpr uint32_t S = 147456;     // 2 x 32 KB S (bf16 [c][v], K-major A)
-constexpr uint32_t XCH = 212992;   // 2 x 2 x 128 fp32
-constexpr uint32_t BYTES = 215040;
+constexpr uint32_t DP = 131072;    // 8 KB masked dP (bf16 [t][s])
+constexpr uint32_t S = 139264;     // 32 KB S (bf16 [c][v], K-major A)
+constexpr uint32_t STG = 172032;   // 32 KB gate-gradient partials (fp32, store source)
+constexpr uint32_t XCH = 204800;   // 2 x 2 x 128 fp32 gate products
+constexpr uint32_t XQ = 206848;    // 2 x 128 fp32: token-half totals of q (.) dq
+constexpr uint32_t BYTES = 207872;
 }  // namespace asm_
 
+// Thread roles: warp 0 lane 0 TMA loads of k, v, do; lane 1 TMA loads of
+// raw q; lane 2 TMA stores of dq and the gate-gradient partials.  Warp 1
+// MMA + TMEM.  Warps 2..9 per-channel warps (key channel c = lane of the
+// warp's TMEM quarter, token half th): gate work and kt for chunk j, then
+// the dq / q (.) dq epilogue of chunk j-1 for their half, written to shared
+// memory for the TMA stores.  Warps 10..13 mask dP and scale the state.
 __global__ void __launch_bounds__(448)
     gla_bwd_dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[asm_::NS], empty[asm_::NS], qfull[asm_::NS], qempty[asm_::NS],
-      prep_done[asm_::NS], dp_full[2], dp_ready[2], dq_full[2], u_full, s_ready, eg_ready[2],
-      eg_free[2];
+      prep_done[asm_::NS], dp_full, dp_ready, dq_full[2], dq_free[2], u_full, s_ready, eg_ready[2],
+      eg_free[2], out_ready, stg_free;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -164,19 +180,22 @@ __global__ void __launch_bounds__(448)
     for (int i = 0; i < asm_::NS; ++i) {
       mbar_init(&full[i], 1);    // k, v, do (released by the MMA commit)
       mbar_init(&empty[i], 1);
-      mbar_init(&qfull[i], 1);   // raw q (read only by the epilogue)
-      mbar_init(&qempty[i], 128);
+      mbar_init(&qfull[i], 1);   // raw q, then dq (released by the store thread)
+      mbar_init(&qempty[i], 1);
       mbar_init(&prep_done[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&dp_full[i], 1);
-      mbar_init(&dp_ready[i], 128);
       mbar_init(&dq_full[i], 1);
+      mbar_init(&dq_free[i], 256);
       mbar_init(&eg_ready[i], 256);
       mbar_init(&eg_free[i], 128);
     }
+    mbar_init(&dp_full, 1);
+    mbar_init(&dp_ready, 128);
     mbar_init(&u_full, 1);
     mbar_init(&s_ready, 128);
+    mbar_init(&out_ready, 256);
+    mbar_init(&stg_free, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -185,15 +204,15 @@ __global__ void __launch_bounds__(448)
   const uint32_t tbase = tmem_base;
   const uint32_t sbase = smem_u32(sm);
   volatile int *abortp = &abort_flag;
-  // TMEM columns
+  // TMEM columns: dP, dq^T[2], S, exp(G)[2]
   const uint32_t tDP = tbase, tDQ = tbase + 128, tS = tbase + 256, tEG = tbase + 384;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ring of k, v, do: released when the chunk's MMAs have completed
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.dO);
+      tma_prefetch_desc(&maps.g);
       for (int j = 0; j < nch; ++j) {
         const int st = j % asm_::NS;
         if (j >= asm_::NS && !mbar_wait(&empty[st], ((j / asm_::NS) - 1) & 1, WAIT_CYCLES))
@@ -207,6 +226,7 @@ __global__ void __launch_bounds__(448)
             tma_prefetch_3d(&maps.v, x, h, tp);
             tma_prefetch_3d(&maps.dO, x, h, tp);
           }
+          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
         }
         mbar_expect_tx(&full[st], 3 * 16384);
         for (int x = 0; x < 2; ++x) {
@@ -216,7 +236,6 @@ __global__ void __launch_bounds__(448)
         }
       }
     } else if (lane == 1) {
-      // ring of raw q: released by the epilogue after q (.) dq
       tma_prefetch_desc(&maps.q);
       for (int j = 0; j < nch; ++j) {
         const int st = j % asm_::NS;
@@ -224,10 +243,34 @@ __global__ void __launch_bounds__(448)
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
+        if (j + 2 < nch) {
+          tma_prefetch_3d(&maps.q, 0, h, tok + 2 * C);
+          tma_prefetch_3d(&maps.q, 64, h, tok + 2 * C);
+        }
         mbar_expect_tx(&qfull[st], 16384);
         for (int x = 0; x < 2; ++x)
           tma_load_3d(sm + asm_::Q + st * 16384 + x * 8192, &maps.q, 64 * x, h, tok, &qfull[st]);
       }
+    } else if (lane == 2) {
+      // stores of full chunks (a ragged chunk is stored by its epilogue threads)
+      tma_prefetch_desc(&maps.dq);
+      tma_prefetch_desc(&maps.dgp);
+      for (int j = 0; j < nch; ++j) {
+        const int st = j % asm_::NS;
+        const int64_t tok0 = s0 + (int64_t)j * C;
+        if (!mbar_wait(&out_ready, j & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if (s1 - tok0 >= C) {
+          for (int x = 0; x < 2; ++x)
+            tma_store_3d(&maps.dq, sm + asm_::Q + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
+          for (int x = 0; x < 4; ++x)
+            tma_store_3d(&maps.dgp, sm + asm_::STG + x * 8192, 32 * x, h, (int)tok0);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&qempty[st]);
+        mbar_arrive(&stg_free);
+      }
+      bulk_wait_all();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -235,31 +278,31 @@ __global__ void __launch_bounds__(448)
       constexpr uint32_t idU = idesc_bf16(128, 128, true, true);
       constexpr uint32_t idQ1 = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idQ2 = idesc_bf16(128, 64, true, false);
-      uint32_t ph_prep = 0, ph_dpr = 0;
+      const uint32_t dpa = sbase + asm_::DP, Sa = sbase + asm_::S;
+      uint32_t ph_prep = 0, ph_dqf = 0;
       for (int j = 0; j < nch; ++j) {
         const int st = j % asm_::NS, b = j & 1;
-        const uint32_t qa = sbase + asm_::Q + st * 16384;
         const uint32_t ka = sbase + asm_::K + st * 16384, va = sbase + asm_::V + st * 16384;
-        const uint32_t doa = sbase + asm_::DO + st * 16384, dpa = sbase + asm_::DP + b * 8192;
-        const uint32_t Sa = sbase + asm_::S + (b ^ 1) * 32768;
-        (void)qa;
+        const uint32_t doa = sbase + asm_::DO + st * 16384;
         if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_prep ^= 1u << st;
         tc_fence_after();
-        // dP = dO V^T
+        // dP = dO V^T  (the mask of chunk j-1 has read tDP: dq^T(j-1) waited for it)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_bf16(tDP + 64 * b, kdesc(doa, ks, 64), kdesc(va, ks, 64), idDP, ks);
-        mma_commit(&dp_full[b]);
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDP, kdesc(doa, ks, 64), kdesc(va, ks, 64), idDP, ks);
+        mma_commit(&dp_full);
         // S (TMEM, = S_prev) += kt^T V
         if (!mbar_wait(&s_ready, j & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tS, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, 1);
         mma_commit(&u_full);
-        // dq^T = S_prev dO^T + kt^T dP^T
-        if (!mbar_wait(&dp_ready[b], (ph_dpr >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        ph_dpr ^= 1u << b;
+        // dq^T = S_prev dO^T + kt^T dP^T  (dq^T buffer b free once chunk j-2 is read)
+        if (!mbar_wait(&dp_ready, j & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if (j >= 2) {
+          if (!mbar_wait(&dq_free[b], (ph_dqf >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+          ph_dqf ^= 1u << b;
+        }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
@@ -272,70 +315,151 @@ __global__ void __launch_bounds__(448)
       }
     }
   } else if (warp < 10) {
-    // ---------------- prep: thread = key channel c, 32 tokens ----------------
+    // ---------- per-channel warps: key channel c, tokens 32 th .. +31 ----------
     const int qw = warp & 3, th = (warp - 2) >> 2;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    uint32_t ph_full = 0, ph_free = 0;
-    for (int j = 0; j < nch; ++j) {
-      const int st = j % asm_::NS, b = j & 1;
-      const int64_t tok0 = s0 + (int64_t)j * C;
-      const int L = (int)min((int64_t)C, s1 - tok0);
-      ChanGate cg;
-      load_gates(cg, a.g, tok0, H, h, c, th, L);
-      if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-      ph_full ^= 1u << st;
-      exchange_gates(cg, reinterpret_cast<float *>(sm + asm_::XCH) + b * 256, c, th, L);
-      // exp(G_t) -> TMEM (epilogue scales dq with it); column 63 = exp(Gam)
-      if (j >= 2) {
-        if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        ph_free ^= 1u << b;
-      }
-      tc_fence_after();
-      {
-        uint32_t r[32];
-        float pre = cg.before;
+    uint32_t ph_full = 0, ph_free = 0, ph_dqf = 0;
+    float xn[32];  // gates of the next chunk, loaded while this one is prepared
+    if (nch > 0) load_gates_to(xn, a.g, s0, H, h, c, th, (int)min((int64_t)C, s1 - s0));
+    // iteration j: gate work and kt of chunk j, then the epilogue of chunk j-1
+    for (int j = 0; j <= nch; ++j) {
+      if (j < nch) {
+        const int st = j % asm_::NS, b = j & 1;
+        const int64_t tok0 = s0 + (int64_t)j * C;
+        const int L = (int)min((int64_t)C, s1 - tok0);
+        ChanGate cg;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          pre *= cg.x[i];
-          r[i] = __float_as_uint(pre);
+        for (int i = 0; i < 32; ++i) cg.x[i] = xn[i];
+        if (j + 1 < nch)
+          load_gates_to(xn, a.g, tok0 + C, H, h, c, th, (int)min((int64_t)C, s1 - tok0 - C));
+        if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        ph_full ^= 1u << st;
+        exchange_gates(cg, reinterpret_cast<float *>(sm + asm_::XCH) + b * 256, c, th, L);
+        // exp(G_t) -> TMEM (dq scaling; column 63 = exp(Gam) for the state step)
+        if (j >= 2) {
+          if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+          ph_free ^= 1u << b;
         }
-        tmem_st32(tEG + 64 * b + lane_off + 32 * th, r);
-      }
-      // kt = k exp(-Gam) exp(Gam - G) in place
-      {
-        const float inv = __frcp_rn(cg.total);
-        uint8_t *kt = sm + asm_::K + st * 16384;
-        uint16_t kb[32];
+        tc_fence_after();
+        {
+          float pre = cg.before;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) kb[i] = ld_u16(kt + sw128_off(32 * th + i, c, 64));
-        float suf = cg.after;
+          for (int hb = 0; hb < 2; ++hb) {
+            uint32_t r[16];
 #pragma unroll
-        for (int i = 31; i >= 0; --i) {
-          const int t = 32 * th + i;
-          kb[i] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[i]) * suf * inv : 0.f);
-          suf *= cg.x[i];
+            for (int i = 0; i < 16; ++i) {
+              pre *= cg.x[16 * hb + i];
+              r[i] = __float_as_uint(pre);
+            }
+            tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
+          }
         }
+        // kt = k exp(-Gam) exp(Gam - G) in place
+        {
+          const ColBf16 kc(sbase + asm_::K + st * 16384, 32 * th, c);
+          float sc = cg.after * __frcp_rn(cg.total);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) st_u16(kt + sw128_off(32 * th + i, c, 64), kb[i]);
+          for (int hb = 1; hb >= 0; --hb) {
+            uint16_t kb[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) kb[i] = lds_u16(kc.at(16 * hb + i));
+#pragma unroll
+            for (int i = 15; i >= 0; --i) {
+              const int t = 32 * th + 16 * hb + i;
+              kb[i] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[i]) * sc : 0.f);
+              sc *= cg.x[16 * hb + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sts_u16(kc.at(16 * hb + i), kb[i]);
+          }
+        }
+        tmem_st_wait();
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&prep_done[st]);
+        mbar_arrive(&eg_ready[b]);
       }
-      tmem_st_wait();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&prep_done[st]);
-      mbar_arrive(&eg_ready[b]);
+      if (j >= 1) {
+        // dq epilogue of chunk jj for this thread's half:
+        //   dq_t = scale exp(G_t) acc_t,  dgp_t = sum_{r >= t in chunk} q_r dq_r
+        // Full chunks go to shared memory (dq over the raw q it was computed
+        // from) for the TMA stores; a ragged last chunk is stored directly.
+        const int jj = j - 1, bb = jj & 1, stt = jj % asm_::NS;
+        const int64_t tok0 = s0 + (int64_t)jj * C;
+        const int L = (int)min((int64_t)C, s1 - tok0);
+        if (!mbar_wait(&dq_full[bb], (ph_dqf >> bb) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        ph_dqf ^= 1u << bb;
+        if (!mbar_wait(&qfull[stt], (jj / asm_::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        tc_fence_after();
+        const ColBf16 qc(sbase + asm_::Q + stt * 16384, 32 * th, c);
+        float sv[32];
+        float suf = 0.f;
+#pragma unroll
+        for (int blk = 1; blk >= 0; --blk) {
+          const int tb = 32 * th + 16 * blk;  // first token of the block
+          uint32_t acc[16], eg[16];
+          tmem_ld16(tDQ + 64 * bb + lane_off + tb, acc);
+          tmem_ld16(tEG + 64 * bb + lane_off + tb, eg);
+          uint16_t qb[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) qb[i] = lds_u16(qc.at(16 * blk + i));
+          tmem_ld_wait(acc);
+          tmem_ld_wait(eg);
+          float dqv[16];
+#pragma unroll
+          for (int i = 15; i >= 0; --i) {
+            dqv[i] = a.scale * __uint_as_float(eg[i]) * __uint_as_float(acc[i]);
+            if (tb + i < L) suf += bf16_bits_to_f32(qb[i]) * dqv[i];
+            sv[16 * blk + i] = suf;
+          }
+          if (L == C) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sts_u16(qc.at(16 * blk + i), f32_to_bf16_bits(dqv[i]));
+          } else {
+            transpose_4x4_blocks(dqv, lane);
+            store_block_bf16(a.dq + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, dqv, lane, tb, L);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&dq_free[bb]);
+        // the low half adds the high half's total
+        float *xq = reinterpret_cast<float *>(sm + asm_::XQ) + bb * 128;
+        if (th == 1) xq[c] = suf;
+        // the staging buffer is free once the previous chunk's stores have read it
+        if (jj >= 1 && !mbar_wait(&stg_free, (jj - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        named_bar(2, 256);
+        const float add = th == 0 ? xq[c] : 0.f;
+        if (L == C) {
+          const ColF32 gc(sbase + asm_::STG, 32 * th, c);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sts_f32(gc.at(i), sv[i] + add);
+        } else {
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = sv[16 * blk + i] + add;
+            const int tb = 32 * th + 16 * blk;
+            transpose_4x4_blocks(v, lane);
+            store_block_f32(a.dgp + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
+          }
+        }
+        fence_async_smem();
+        mbar_arrive(&out_ready);
+      }
     }
   } else {
-    // ---------------- epilogue: thread = key channel c ----------------
+    // ---------------- state warpgroup: thread = key channel c ----------------
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    // S (TMEM) = h0, bf16 copy for chunk 0's readout
+    uint8_t *St = sm + asm_::S;
+    // S (TMEM) = state entering the unit, bf16 copy for chunk 0's readout
     {
       const float *h0 = un.piece == 0 ? (a.h0 ? a.h0 + (d * H + h) * KD * VD : nullptr)
                                       : a.sin + (u * H + h) * KD * VD;
       if (h0) h0 += (int64_t)c * VD;
-      uint8_t *St = sm + asm_::S + 32768;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t r[32];
@@ -355,66 +479,20 @@ __global__ void __launch_bounds__(448)
       tc_fence_before();
       mbar_arrive(&s_ready);
     }
-    uint32_t ph_dpf = 0, ph_dqf = 0, ph_egr = 0;
+    uint32_t ph_egr = 0, ph_dqf = 0;
     const int64_t gc0 = unit_chunk0(a.units, un), doc_c0 = a.units.docs.chunk_base(un.doc);
-    // dq epilogue of chunk jj (buffer bb): dq = scale exp(G) acc, suffix of q dq
-    auto dq_epilogue = [&](int jj) -> bool {
-      const int bb = jj & 1, stt = jj % asm_::NS;
-      const int64_t tok0 = s0 + (int64_t)jj * C;
-      const int L = (int)min((int64_t)C, s1 - tok0);
-      if (!mbar_wait(&dq_full[bb], (ph_dqf >> bb) & 1, WAIT_CYCLES)) return false;
-      ph_dqf ^= 1u << bb;
-      if (!mbar_wait(&qfull[stt], (jj / asm_::NS) & 1, WAIT_CYCLES)) return false;
-      tc_fence_after();
-      const uint8_t *qt = sm + asm_::Q + stt * 16384;
-      float suf = 0.f;
-#pragma unroll
-      for (int blk = 3; blk >= 0; --blk) {
-        uint32_t acc[16], eg[16];
-        tmem_ld16(tDQ + 64 * bb + lane_off + 16 * blk, acc);
-        tmem_ld16(tEG + 64 * bb + lane_off + 16 * blk, eg);
-        uint16_t qb[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) qb[i] = ld_u16(qt + sw128_off(16 * blk + i, c, 64));
-        tmem_ld_wait(acc);
-        tmem_ld_wait(eg);
-        float dqv[16], sv[16];
-#pragma unroll
-        for (int i = 15; i >= 0; --i) {
-          const int t = 16 * blk + i;
-          dqv[i] = a.scale * __uint_as_float(eg[i]) * __uint_as_float(acc[i]);
-          if (t < L) suf += bf16_bits_to_f32(qb[i]) * dqv[i];
-          sv[i] = suf;
-        }
-        __nv_bfloat16 *dq = a.dq + ((tok0 + 16 * blk) * H + h) * KD + c;
-        float *dgp = a.dgp + ((tok0 + 16 * blk) * H + h) * KD + c;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (16 * blk + i < L) {
-            dq[(int64_t)i * H * KD] = __float2bfloat16_rn(dqv[i]);
-            dgp[(int64_t)i * H * KD] = sv[i];
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&eg_free[bb]);
-      mbar_arrive(&qempty[stt]);
-      return true;
-    };
-    bool ok = true;
-    for (int j = 0; j < nch && ok; ++j) {
+    for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
-      // (1) masked dP -> bf16 operand
-      if (!mbar_wait(&dp_full[b], (ph_dpf >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-      ph_dpf ^= 1u << b;
+      // (1) masked dP -> bf16 operand (dq^T of chunk j-1, its last reader, is
+      //     complete: dp_full(j) is committed after it)
+      if (!mbar_wait(&dp_full, j & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
       tc_fence_after();
-      mask_tile_to_smem(tDP + 64 * b, lane_off, qw, lane, sm + asm_::DP + b * 8192);
+      mask_tile_to_smem(tDP, lane_off, qw, lane, sm + asm_::DP);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&dp_ready[b]);
-      // (2) dq of the previous chunk
-      if (j >= 1 && !dq_epilogue(j - 1)) BW_FAIL_AND_BREAK
-      // (3) S <- exp(Gam) (S_prev + kt^T V): TMEM in place, bf16 copy
+      mbar_arrive(&dp_ready);
+      // (2) S <- exp(Gam) (S_prev + kt^T V) in TMEM; its bf16 copy replaces
+      //     S_prev's once dq^T of chunk j has read that
       if (!mbar_wait(&u_full, j & 1, WAIT_CYCLES) ||
           !mbar_wait(&eg_ready[b], (ph_egr >> b) & 1, WAIT_CYCLES))
         BW_FAIL_AND_BREAK
@@ -425,23 +503,46 @@ __global__ void __launch_bounds__(448)
         tmem_ld16(tEG + 64 * b + lane_off + 48, e1);
         tmem_ld_wait(e1);
         const float eGam = __uint_as_float(e1[15]);
-        uint8_t *St = sm + asm_::S + b * 32768;
+        tc_fence_before();
+        mbar_arrive(&eg_free[b]);
+        bool waited = false;
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          uint32_t r[32];
+        for (int cb = 0; cb < 4; cb += 2) {
+          uint32_t r[32], r2[32];
           tmem_ld32(tS + lane_off + 32 * cb, r);
+          tmem_ld32(tS + lane_off + 32 * cb + 32, r2);
           tmem_ld_wait32(r);
+          tmem_ld_wait32(r2);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(eGam * __uint_as_float(r[i]));
+          for (int i = 0; i < 32; ++i) {
+            r[i] = __float_as_uint(eGam * __uint_as_float(r[i]));
+            r2[i] = __float_as_uint(eGam * __uint_as_float(r2[i]));
+          }
           tmem_st32(tS + lane_off + 32 * cb, r);
+          tmem_st32(tS + lane_off + 32 * cb + 32, r2);
+          if (!waited) {
+            if (!mbar_wait(&dq_full[b], (ph_dqf >> b) & 1, WAIT_CYCLES)) {
+              atomicExch(&abort_flag, 1);
+              break;
+            }
+            ph_dqf ^= 1u << b;
+            waited = true;
+          }
 #pragma unroll
-          for (int n = 0; n < 32; n += 8)
+          for (int n = 0; n < 32; n += 8) {
             st_shared_v4(smem_u32(St + sw128_off(c, 32 * cb + n, 128)),
                          pack_bf16(__uint_as_float(r[n]), __uint_as_float(r[n + 1])),
                          pack_bf16(__uint_as_float(r[n + 2]), __uint_as_float(r[n + 3])),
                          pack_bf16(__uint_as_float(r[n + 4]), __uint_as_float(r[n + 5])),
                          pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
+            st_shared_v4(smem_u32(St + sw128_off(c, 32 * cb + 32 + n, 128)),
+                         pack_bf16(__uint_as_float(r2[n]), __uint_as_float(r2[n + 1])),
+                         pack_bf16(__uint_as_float(r2[n + 2]), __uint_as_float(r2[n + 3])),
+                         pack_bf16(__uint_as_float(r2[n + 4]), __uint_as_float(r2[n + 5])),
+                         pack_bf16(__uint_as_float(r2[n + 6]), __uint_as_float(r2[n + 7])));
+          }
         }
+        if (*abortp) break;
         tmem_st_wait();
         const int64_t slot = ckpt_slot(gc0, doc_c0, j, nch);
         if (slot >= 0) {  // exact boundary state for pass B's gate-gradient carry
@@ -463,10 +564,7 @@ __global__ void __launch_bounds__(448)
       tc_fence_before();
       mbar_arrive(&s_ready);
     }
-    if (!*abortp && nch > 0) {
-      if (!dq_epilogue(nch - 1)) atomicExch(&abort_flag, 1);
-    }
-    // final-state term of the gate gradient: bvec = (S_T (.) dht) 1_V
+    // final-state term of the gate gradient: bvec = (S_end (.) dH_end) 1_V
     if (!*abortp && a.bvec) {
       float acc = 0.f;
       const float *dhe = dh_end_ptr(a, un, u, h);
@@ -483,7 +581,6 @@ __global__ void __launch_bounds__(448)
       }
       a.bvec[(u * H + h) * KD + c] = acc;
     }
-    (void)ok;
   }
   tc_fence_before();
   __syncthreads();
@@ -668,12 +765,19 @@ __global__ void __launch_bounds__(448)
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     uint32_t ph_full = 0, ph_free = 0;
+    float xn[32];  // gates of the next chunk (in visiting order)
+    if (nch > 0) {
+      const int64_t tl = s0 + (int64_t)(nch - 1) * C;
+      load_gates_to(xn, a.g, tl, H, h, c, th, (int)min((int64_t)C, s1 - tl));
+    }
     for (int i = 0; i < nch; ++i) {
       const int j = nch - 1 - i, st = i % bsm::NS, b = i & 1;
       const int64_t tok0 = s0 + (int64_t)j * C;
       const int L = (int)min((int64_t)C, s1 - tok0);
       ChanGate cg;
-      load_gates(cg, a.g, tok0, H, h, c, th, L);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) cg.x[u] = xn[u];
+      if (j >= 1) load_gates_to(xn, a.g, tok0 - C, H, h, c, th, C);
       if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES) ||
           (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)))
         BW_FAIL_AND_BREAK
@@ -683,18 +787,21 @@ __global__ void __launch_bounds__(448)
       // qt = scale q exp(G) in place
       {
         uint8_t *q = sm + bsm::Q + st * 16384;
-        uint16_t qb[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) qb[u] = ld_u16(q + sw128_off(32 * th + u, c, 64));
         float pre = cg.before;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int t = 32 * th + u;
-          pre *= cg.x[u];
-          qb[u] = f32_to_bf16_bits(t < L ? a.scale * bf16_bits_to_f32(qb[u]) * pre : 0.f);
-        }
+        for (int hb = 0; hb < 2; ++hb) {
+          uint16_t qb[16];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) st_u16(q + sw128_off(32 * th + u, c, 64), qb[u]);
+          for (int u = 0; u < 16; ++u) qb[u] = ld_u16(q + sw128_off(32 * th + 16 * hb + u, c, 64));
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int t = 32 * th + 16 * hb + u;
+            pre *= cg.x[16 * hb + u];
+            qb[u] = f32_to_bf16_bits(t < L ? a.scale * bf16_bits_to_f32(qb[u]) * pre : 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u) st_u16(q + sw128_off(32 * th + 16 * hb + u, c, 64), qb[u]);
+        }
       }
       // kt = k exp(-G) (separate tile; raw k is kept for k (.) dk); exp(-G) -> TMEM
       if (i >= 2) {
@@ -705,26 +812,29 @@ __global__ void __launch_bounds__(448)
       {
         const uint8_t *k = sm + bsm::K + st * 16384;
         uint8_t *kt = sm + bsm::KT + st * 16384;
-        uint32_t r[32];
-        uint16_t kb[32];
-        if (!DH_ONLY) {
-#pragma unroll
-          for (int w = 0; w < 32; ++w) kb[w] = ld_u16(k + sw128_off(32 * th + w, c, 64));
-        }
         float suf = cg.after;
 #pragma unroll
-        for (int w = 31; w >= 0; --w) {
-          const int t = 32 * th + w;
-          const float e = suf * inv;  // exp(-G_t)
-          r[w] = __float_as_uint(e);
-          if (!DH_ONLY) kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
-          suf *= cg.x[w];
-        }
-        if (!DH_ONLY) {
+        for (int hb = 1; hb >= 0; --hb) {
+          uint32_t r[16];
+          uint16_t kb[16];
+          if (!DH_ONLY) {
 #pragma unroll
-          for (int w = 0; w < 32; ++w) st_u16(kt + sw128_off(32 * th + w, c, 64), kb[w]);
+            for (int w = 0; w < 16; ++w) kb[w] = ld_u16(k + sw128_off(32 * th + 16 * hb + w, c, 64));
+          }
+#pragma unroll
+          for (int w = 15; w >= 0; --w) {
+            const int t = 32 * th + 16 * hb + w;
+            const float e = suf * inv;  // exp(-G_t)
+            r[w] = __float_as_uint(e);
+            if (!DH_ONLY) kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
+            suf *= cg.x[16 * hb + w];
+          }
+          if (!DH_ONLY) {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) st_u16(kt + sw128_off(32 * th + 16 * hb + w, c, 64), kb[w]);
+          }
+          tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
         }
-        tmem_st32(tEG + 64 * b + lane_off + 32 * th, r);
       }
       tmem_st_wait();
       fence_async_smem();
@@ -841,15 +951,11 @@ __global__ void __launch_bounds__(448)
             dgv[u] = qp[u] - sk + carry;
           }
           if (blk == 0) qtot = qp[0];
-          __nv_bfloat16 *dk = a.dk + ((tok0 + 16 * blk) * H + h) * KD + c;
-          float *dg = a.dg + ((tok0 + 16 * blk) * H + h) * KD + c;
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            if (16 * blk + u < L) {
-              dk[(int64_t)u * H * KD] = __float2bfloat16_rn(dkv[u]);
-              dg[(int64_t)u * H * KD] = dgv[u];
-            }
-          }
+          const int64_t row = ((tok0 + 16 * blk) * H + h) * KD + 32 * qw;
+          transpose_4x4_blocks(dkv, lane);
+          store_block_bf16(a.dk + row, H * KD, dkv, lane, 16 * blk, L);
+          transpose_4x4_blocks(dgv, lane);
+          store_block_f32(a.dg + row, H * KD, dgv, lane, 16 * blk, L);
         }
         carry += qtot - sk;
 #pragma unroll
@@ -857,10 +963,11 @@ __global__ void __launch_bounds__(448)
           uint32_t acc[16];
           tmem_ld16(tDV + lane_off + 16 * blk, acc);
           tmem_ld_wait(acc);
-          __nv_bfloat16 *dv = a.dv + ((tok0 + 16 * blk) * H + h) * VD + c;
+          float dvv[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            if (16 * blk + u < L) dv[(int64_t)u * H * VD] = __float2bfloat16_rn(__uint_as_float(acc[u]));
+          for (int u = 0; u < 16; ++u) dvv[u] = __uint_as_float(acc[u]);
+          transpose_4x4_blocks(dvv, lane);
+          store_block_bf16(a.dv + ((tok0 + 16 * blk) * H + h) * VD + 32 * qw, H * VD, dvv, lane, 16 * blk, L);
         }
       }
       tc_fence_before();
@@ -909,7 +1016,9 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
       !make_map(&maps.dO, dO, true, VD, pr.H, BT, 64) ||
-      !make_map(&maps.dgp, dgp, false, KD, pr.H, BT, 32))
+      !make_map(&maps.dgp, dgp, false, KD, pr.H, BT, 32) ||
+      !make_map(&maps.dq, dq, true, KD, pr.H, BT, 64) ||
+      !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32))
     return cudaErrorInvalidValue;
   BwdArgs a;
   memset(&a, 0, sizeof(a));

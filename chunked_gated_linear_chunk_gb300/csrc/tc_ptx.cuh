@@ -104,6 +104,22 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int x, int
                : "memory");
 }
 
+// Tile store shared -> global (bulk async group of the issuing thread).
+// Rows past the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   (uint64_t)m),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the issuing thread's committed stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... and their global writes are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA)
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
