@@ -35,7 +35,7 @@ namespace glacore {
 namespace tc {
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dO, dgp, dq, g;
+  CUtensorMap q, k, v, dO, dgp, dq, g, dk;
 };
 struct BwdArgs {
   Units units;
@@ -594,28 +594,37 @@ __global__ void __launch_bounds__(448)
 namespace bsm {  // shared-memory carve-up (bytes)
 constexpr int NS = 2;
 constexpr uint32_t Q = 0;          // 2 x 16 KB q, then qt in place
-constexpr uint32_t K = 32768;      // 2 x 16 KB raw k
+constexpr uint32_t K = 32768;      // 2 x 16 KB raw k, then dk in place (store source)
 constexpr uint32_t KT = 65536;     // 2 x 16 KB kt
 constexpr uint32_t V = 98304;      // 2 x 16 KB
 constexpr uint32_t DO = 131072;    // 2 x 16 KB
 constexpr uint32_t P = 163840;     // 8 KB masked P  (bf16 [t][s])
 constexpr uint32_t DP = 172032;    // 8 KB masked dP (bf16 [t][s])
 constexpr uint32_t DH = 180224;    // 32 KB dHh (bf16 [c][v])
-constexpr uint32_t XCH = 212992;   // 2 x 2 x 128 fp32
-constexpr uint32_t BYTES = 215040;
+constexpr uint32_t XCH = 212992;   // 2 x 2 x 128 fp32 gate products
+constexpr uint32_t XK = 215040;    // 2 x 2 x 128 fp32: token-half totals of k (.) dk
+constexpr uint32_t BND = 217088;   // 2 x 128 fp32: exact gate-gradient carry at checkpoints
+constexpr uint32_t BYTES = 218112;
 }  // namespace bsm
 
 // DH_ONLY: the reverse piece pass of the exact sequence split -- only the
 // state-gradient recurrence from zero at the piece end (needs q, g, do);
 // writes the gradient at the piece start and the piece's total decay.
 // First pieces have nothing to contribute and exit.
+//
+// Thread roles: warp 0 lane 0 TMA loads of q, v, do; lane 1 TMA loads of raw
+// k; lane 2 TMA stores of dk.  Warp 1 MMA + TMEM.  Warps 2..9 per-channel
+// warps (key channel / value column c, token half th): qt, kt and exp(-G)
+// of chunk i, then the dk / dg / dv epilogue of chunk i-1.  Warps 10..13
+// mask P and dP and scale the state gradient.
 template <bool DH_ONLY>
 __global__ void __launch_bounds__(448)
     gla_bwd_rev_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[bsm::NS], empty[bsm::NS], kfull[bsm::NS], kempty[bsm::NS],
-      prep_done[bsm::NS], pdp_full, pdp_ready, dh_ready, kv_full, eg_ready[2], eg_free[2];
+      prep_done[bsm::NS], pdp_full, pdp_ready, dh_ready, dh_full, kv_full, kv_free, eg_ready[2],
+      eg_free[2], bnd_ready[2], out_ready[bsm::NS];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -637,18 +646,22 @@ __global__ void __launch_bounds__(448)
     for (int i = 0; i < bsm::NS; ++i) {
       mbar_init(&full[i], 1);    // q, v, do (kt is written here too): MMA commit
       mbar_init(&empty[i], 1);
-      mbar_init(&kfull[i], 1);   // raw k: read by the prep and the epilogue
-      mbar_init(&kempty[i], 128);
+      mbar_init(&kfull[i], 1);   // raw k, then dk: released by the store thread
+      mbar_init(&kempty[i], 1);
       mbar_init(&prep_done[i], 256);
+      mbar_init(&out_ready[i], 256);  // dk written over raw k (per k stage)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&eg_ready[i], 256);
       mbar_init(&eg_free[i], 128);
+      mbar_init(&bnd_ready[i], 128);
     }
     mbar_init(&pdp_full, 1);
     mbar_init(&pdp_ready, 128);
     mbar_init(&dh_ready, 128);
+    mbar_init(&dh_full, 1);
     mbar_init(&kv_full, 1);
+    mbar_init(&kv_free, 256);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -659,6 +672,7 @@ __global__ void __launch_bounds__(448)
   volatile int *abortp = &abort_flag;
   const uint32_t tDH = tbase, tP = tbase + 128, tDP = tbase + 192, tDK = tbase + 256,
                  tDV = tbase + 320, tEG = tbase + 384;
+  const int64_t gc0 = unit_chunk0(a.units, un), doc_c0 = a.units.docs.chunk_base(un.doc);
 
   // chunks are visited in reverse: iteration i handles chunk j = nch - 1 - i
   if (warp == 0) {
@@ -668,24 +682,28 @@ __global__ void __launch_bounds__(448)
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.dO);
       tma_prefetch_desc(&maps.dgp);
+      tma_prefetch_desc(&maps.g);
       for (int i = 0; i < nch; ++i) {
         const int j = nch - 1 - i, st = i % bsm::NS;
         if (i >= bsm::NS && !mbar_wait(&empty[st], ((i / bsm::NS) - 1) & 1, WAIT_CYCLES))
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
-        if (i == 0)  // gate-gradient partials of the first chunk the epilogue reads
+        if (i == 0 && !DH_ONLY)  // gate-gradient partials of the first chunk the epilogue reads
           for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.dgp, x, h, tok);
         if (j - 2 >= 0) {
           const int tp = tok - 2 * C;
           for (int x = 0; x < 128; x += 64) {
             tma_prefetch_3d(&maps.q, x, h, tp);
-            tma_prefetch_3d(&maps.k, x, h, tp);
-            tma_prefetch_3d(&maps.v, x, h, tp);
+            if (!DH_ONLY) {
+              tma_prefetch_3d(&maps.k, x, h, tp);
+              tma_prefetch_3d(&maps.v, x, h, tp);
+            }
             tma_prefetch_3d(&maps.dO, x, h, tp);
           }
+          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
         }
-        if (j - 1 >= 0)
+        if (j - 1 >= 0 && !DH_ONLY)
           for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.dgp, x, h, tok - C);
         mbar_expect_tx(&full[st], (DH_ONLY ? 2 : 3) * 16384);
         for (int x = 0; x < 2; ++x) {
@@ -696,7 +714,7 @@ __global__ void __launch_bounds__(448)
         }
       }
     } else if (lane == 1 && !DH_ONLY) {
-      // ring of raw k: released by the epilogue after k (.) dk
+      // ring of raw k: released once dk (written over it) has been stored
       tma_prefetch_desc(&maps.k);
       for (int i = 0; i < nch; ++i) {
         const int j = nch - 1 - i, st = i % bsm::NS;
@@ -708,6 +726,22 @@ __global__ void __launch_bounds__(448)
         for (int x = 0; x < 2; ++x)
           tma_load_3d(sm + bsm::K + st * 16384 + x * 8192, &maps.k, 64 * x, h, tok, &kfull[st]);
       }
+    } else if (lane == 2 && !DH_ONLY) {
+      // dk stores of full chunks (a ragged chunk is stored by its epilogue threads)
+      tma_prefetch_desc(&maps.dk);
+      for (int i = 0; i < nch; ++i) {
+        const int j = nch - 1 - i, st = i % bsm::NS;
+        const int64_t tok0 = s0 + (int64_t)j * C;
+        if (!mbar_wait(&out_ready[st], (i / bsm::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if (s1 - tok0 >= C) {
+          for (int x = 0; x < 2; ++x)
+            tma_store_3d(&maps.dk, sm + bsm::K + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&kempty[st]);
+      }
+      bulk_wait_all();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -724,126 +758,212 @@ __global__ void __launch_bounds__(448)
         const uint32_t va = sbase + bsm::V + st * 16384, doa = sbase + bsm::DO + st * 16384;
         if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_prep ^= 1u << st;
-        if (DH_ONLY) {
-          if (!mbar_wait(&dh_ready, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-          tc_fence_after();
+        tc_fence_after();
+        if (!DH_ONLY) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDH, mdesc(qa, ks, 8192), mdesc(doa, ks, 8192), idH, 1);
-          mma_commit(&kv_full);
-          mma_commit(&empty[st]);
-          continue;
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(kta, ks, 64), idCC, ks);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tDP, kdesc(doa, ks, 64), kdesc(va, ks, 64), idCC, ks);
+          mma_commit(&pdp_full);
         }
+        // dH (TMEM, = dHh after the state step) += qt^T dO
+        if (!mbar_wait(&dh_ready, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(kta, ks, 64), idCC, ks);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDP, kdesc(doa, ks, 64), kdesc(va, ks, 64), idCC, ks);
-        mma_commit(&pdp_full);
-        if (!mbar_wait(&pdp_ready, i & 1, WAIT_CYCLES) || !mbar_wait(&dh_ready, i & 1, WAIT_CYCLES))
-          BW_FAIL_AND_BREAK
-        tc_fence_after();
-        // dk^T = qt^T dP + dHh V^T
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDK, mdesc(qa, ks, 8192), mdesc(dpa, ks, 8192), idMM, ks);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDK, kdesc(dha, ks, 128), kdesc(va, ks, 64), idKK, 1);
-        // dv^T = dO^T P + dHh^T kt^T
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDV, mdesc(doa, ks, 8192), mdesc(pa, ks, 8192), idMM, ks);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDV, mdesc(dha, ks, 16384), kdesc(kta, ks, 64), idMK, 1);
-        // dH (= dHh in TMEM) += qt^T dO
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tDH, mdesc(qa, ks, 8192), mdesc(doa, ks, 8192), idH, 1);
-        mma_commit(&kv_full);
+        mma_commit(&dh_full);
+        if (!DH_ONLY) {
+          // dk/dv accumulators are free once the epilogue of chunk i-1 has read them
+          if (!mbar_wait(&pdp_ready, i & 1, WAIT_CYCLES) ||
+              (i >= 1 && !mbar_wait(&kv_free, (i - 1) & 1, WAIT_CYCLES)))
+            BW_FAIL_AND_BREAK
+          tc_fence_after();
+          // dk^T = qt^T dP + dHh V^T
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDK, mdesc(qa, ks, 8192), mdesc(dpa, ks, 8192), idMM, ks);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tDK, kdesc(dha, ks, 128), kdesc(va, ks, 64), idKK, 1);
+          // dv^T = dO^T P + dHh^T kt^T
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDV, mdesc(doa, ks, 8192), mdesc(pa, ks, 8192), idMM, ks);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) mma_bf16(tDV, mdesc(dha, ks, 16384), kdesc(kta, ks, 64), idMK, 1);
+          mma_commit(&kv_full);
+        }
         mma_commit(&empty[st]);
       }
     }
   } else if (warp < 10) {
-    // ---------------- prep: thread = key channel c, 32 tokens ----------------
+    // ------- per-channel warps: key channel / value column c, tokens 32 th .. +31 -------
     const int qw = warp & 3, th = (warp - 2) >> 2;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     uint32_t ph_full = 0, ph_free = 0;
+    float carry = (!DH_ONLY && a.bvec) ? a.bvec[(u * H + h) * KD + c] : 0.f;
     float xn[32];  // gates of the next chunk (in visiting order)
     if (nch > 0) {
       const int64_t tl = s0 + (int64_t)(nch - 1) * C;
       load_gates_to(xn, a.g, tl, H, h, c, th, (int)min((int64_t)C, s1 - tl));
     }
-    for (int i = 0; i < nch; ++i) {
-      const int j = nch - 1 - i, st = i % bsm::NS, b = i & 1;
-      const int64_t tok0 = s0 + (int64_t)j * C;
-      const int L = (int)min((int64_t)C, s1 - tok0);
-      ChanGate cg;
+    // iteration i: qt, kt, exp(-G) of chunk nch-1-i, then the epilogue of the previous one
+    for (int i = 0; i <= nch; ++i) {
+      if (i < nch) {
+        const int j = nch - 1 - i, st = i % bsm::NS, b = i & 1;
+        const int64_t tok0 = s0 + (int64_t)j * C;
+        const int L = (int)min((int64_t)C, s1 - tok0);
+        ChanGate cg;
 #pragma unroll
-      for (int u = 0; u < 32; ++u) cg.x[u] = xn[u];
-      if (j >= 1) load_gates_to(xn, a.g, tok0 - C, H, h, c, th, C);
-      if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES) ||
-          (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)))
-        BW_FAIL_AND_BREAK
-      ph_full ^= 1u << st;
-      exchange_gates(cg, reinterpret_cast<float *>(sm + bsm::XCH) + b * 256, c, th, L);
-      const float inv = __frcp_rn(cg.total);
-      // qt = scale q exp(G) in place
-      {
-        uint8_t *q = sm + bsm::Q + st * 16384;
-        float pre = cg.before;
+        for (int w = 0; w < 32; ++w) cg.x[w] = xn[w];
+        if (j >= 1) load_gates_to(xn, a.g, tok0 - C, H, h, c, th, C);
+        if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES) ||
+            (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)))
+          BW_FAIL_AND_BREAK
+        ph_full ^= 1u << st;
+        exchange_gates(cg, reinterpret_cast<float *>(sm + bsm::XCH) + b * 256, c, th, L);
+        const float inv = __frcp_rn(cg.total);
+        // qt = scale q exp(G) in place
+        {
+          const ColBf16 qc(sbase + bsm::Q + st * 16384, 32 * th, c);
+          float pre = cg.before * a.scale;
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          uint16_t qb[16];
+          for (int hb = 0; hb < 2; ++hb) {
+            uint16_t qb[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) qb[u] = ld_u16(q + sw128_off(32 * th + 16 * hb + u, c, 64));
+            for (int w = 0; w < 16; ++w) qb[w] = lds_u16(qc.at(16 * hb + w));
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int t = 32 * th + 16 * hb + u;
-            pre *= cg.x[16 * hb + u];
-            qb[u] = f32_to_bf16_bits(t < L ? a.scale * bf16_bits_to_f32(qb[u]) * pre : 0.f);
+            for (int w = 0; w < 16; ++w) {
+              const int t = 32 * th + 16 * hb + w;
+              pre *= cg.x[16 * hb + w];
+              qb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(qb[w]) * pre : 0.f);
+            }
+#pragma unroll
+            for (int w = 0; w < 16; ++w) sts_u16(qc.at(16 * hb + w), qb[w]);
           }
-#pragma unroll
-          for (int u = 0; u < 16; ++u) st_u16(q + sw128_off(32 * th + 16 * hb + u, c, 64), qb[u]);
         }
-      }
-      // kt = k exp(-G) (separate tile; raw k is kept for k (.) dk); exp(-G) -> TMEM
-      if (i >= 2) {
-        if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        ph_free ^= 1u << b;
-      }
-      tc_fence_after();
-      {
-        const uint8_t *k = sm + bsm::K + st * 16384;
-        uint8_t *kt = sm + bsm::KT + st * 16384;
-        float suf = cg.after;
+        // kt = k exp(-G) (separate tile; raw k is kept for k (.) dk); exp(-G) -> TMEM
+        if (i >= 2) {
+          if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+          ph_free ^= 1u << b;
+        }
+        tc_fence_after();
+        {
+          const ColBf16 kc(sbase + bsm::K + st * 16384, 32 * th, c);
+          const ColBf16 ktc(sbase + bsm::KT + st * 16384, 32 * th, c);
+          float e = cg.after * inv;  // exp(-G_t), walking t downwards
 #pragma unroll
-        for (int hb = 1; hb >= 0; --hb) {
-          uint32_t r[16];
-          uint16_t kb[16];
-          if (!DH_ONLY) {
+          for (int hb = 1; hb >= 0; --hb) {
+            uint32_t r[16];
+            uint16_t kb[16];
+            if (!DH_ONLY) {
 #pragma unroll
-            for (int w = 0; w < 16; ++w) kb[w] = ld_u16(k + sw128_off(32 * th + 16 * hb + w, c, 64));
+              for (int w = 0; w < 16; ++w) kb[w] = lds_u16(kc.at(16 * hb + w));
+            }
+#pragma unroll
+            for (int w = 15; w >= 0; --w) {
+              const int t = 32 * th + 16 * hb + w;
+              r[w] = __float_as_uint(e);
+              if (!DH_ONLY) kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
+              e *= cg.x[16 * hb + w];
+            }
+            if (!DH_ONLY) {
+#pragma unroll
+              for (int w = 0; w < 16; ++w) sts_u16(ktc.at(16 * hb + w), kb[w]);
+            }
+            tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
           }
+        }
+        tmem_st_wait();
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&prep_done[st]);
+        mbar_arrive(&eg_ready[b]);
+      }
+      if (!DH_ONLY && i >= 1) {
+        // epilogue of chunk jj (visited at ii = i - 1), this thread's half:
+        //   dk_t = exp(-G_t) acc_t (channel c),  dv_t (value column c),
+        //   dg_t = dgp_t - sum_{r >= t in chunk} k_r dk_r + carry
+        const int ii = i - 1, jj = nch - 1 - ii, bb = ii & 1, stt = ii % bsm::NS;
+        const int64_t tok0 = s0 + (int64_t)jj * C;
+        const int L = (int)min((int64_t)C, s1 - tok0);
+        if (!mbar_wait(&kv_full, ii & 1, WAIT_CYCLES) ||
+            !mbar_wait(&bnd_ready[bb], (ii >> 1) & 1, WAIT_CYCLES))
+          BW_FAIL_AND_BREAK
+        tc_fence_after();
+        // the carry restarts from the exact boundary term at a checkpoint
+        const float cin = ckpt_slot(gc0, doc_c0, jj, nch) >= 0
+                              ? reinterpret_cast<const float *>(sm + bsm::BND)[bb * 128 + c]
+                              : carry;
+        const float *dgp = a.dgp + (tok0 * H + h) * KD + c;
+        const float qtot = __ldg(dgp);  // the chunk's q (.) dq total (suffix from its first token)
+        const ColBf16 kc(sbase + bsm::K + stt * 16384, 32 * th, c);
+        float dgv[32];
+        float sk = 0.f;
+#pragma unroll
+        for (int blk = 1; blk >= 0; --blk) {
+          const int tb = 32 * th + 16 * blk;
+          uint32_t acc[16], eg[16];
+          tmem_ld16(tDK + lane_off + tb, acc);
+          tmem_ld16(tEG + 64 * bb + lane_off + tb, eg);
+          float qp[16];
+          uint16_t kb[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            qp[w] = tb + w < L ? __ldg(dgp + (int64_t)(tb + w) * H * KD) : 0.f;
+            kb[w] = lds_u16(kc.at(16 * blk + w));
+          }
+          tmem_ld_wait(acc);
+          tmem_ld_wait(eg);
+          float dkv[16];
 #pragma unroll
           for (int w = 15; w >= 0; --w) {
-            const int t = 32 * th + 16 * hb + w;
-            const float e = suf * inv;  // exp(-G_t)
-            r[w] = __float_as_uint(e);
-            if (!DH_ONLY) kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
-            suf *= cg.x[16 * hb + w];
+            dkv[w] = __uint_as_float(eg[w]) * __uint_as_float(acc[w]);
+            if (tb + w < L) sk += bf16_bits_to_f32(kb[w]) * dkv[w];
+            dgv[16 * blk + w] = qp[w] - sk + cin;
           }
-          if (!DH_ONLY) {
+          if (L == C) {
 #pragma unroll
-            for (int w = 0; w < 16; ++w) st_u16(kt + sw128_off(32 * th + 16 * hb + w, c, 64), kb[w]);
+            for (int w = 0; w < 16; ++w) sts_u16(kc.at(16 * blk + w), f32_to_bf16_bits(dkv[w]));
+          } else {
+            transpose_4x4_blocks(dkv, lane);
+            store_block_bf16(a.dk + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, dkv, lane, tb, L);
           }
-          tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
         }
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const int tb = 32 * th + 16 * blk;
+          uint32_t acc[16];
+          tmem_ld16(tDV + lane_off + tb, acc);
+          tmem_ld_wait(acc);
+          float dvv[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) dvv[w] = __uint_as_float(acc[w]);
+          transpose_4x4_blocks(dvv, lane);
+          store_block_bf16(a.dv + ((tok0 + tb) * H + h) * VD + 32 * qw, H * VD, dvv, lane, tb, L);
+        }
+        tc_fence_before();
+        mbar_arrive(&kv_free);
+        // token-half totals of k (.) dk: the low half's suffixes include the high half's
+        float *xk = reinterpret_cast<float *>(sm + bsm::XK) + bb * 256;
+        xk[th * 128 + c] = sk;
+        named_bar(2, 256);
+        const float other = xk[(1 - th) * 128 + c];
+        const float off = th == 0 ? other : 0.f;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          float v[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) v[w] = dgv[16 * blk + w] - off;
+          const int tb = 32 * th + 16 * blk;
+          transpose_4x4_blocks(v, lane);
+          store_block_f32(a.dg + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
+        }
+        carry = cin + qtot - (sk + other);
+        fence_async_smem();
+        mbar_arrive(&out_ready[stt]);
       }
-      tmem_st_wait();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&prep_done[st]);
-      mbar_arrive(&eg_ready[b]);
     }
   } else {
-    // ---------------- epilogue: thread = key channel / value column c ----------------
+    // ------------- state-gradient warpgroup: thread = key channel c -------------
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
@@ -860,15 +980,12 @@ __global__ void __launch_bounds__(448)
       }
       tmem_st_wait();
     }
-    float carry = (!DH_ONLY && a.bvec) ? a.bvec[(u * H + h) * KD + c] : 0.f;
-    const int64_t gc0 = unit_chunk0(a.units, un), doc_c0 = a.units.docs.chunk_base(un.doc);
     float decay = 1.f;  // dH-only mode: exp(sum of g over the piece)
     uint32_t ph_egr = 0;
     for (int i = 0; i < nch; ++i) {
-      const int j = nch - 1 - i, st = i % bsm::NS, b = i & 1;
-      const int64_t tok0 = s0 + (int64_t)j * C;
-      const int L = (int)min((int64_t)C, s1 - tok0);
-      // (1) masked P and dP -> bf16 operands
+      const int j = nch - 1 - i, b = i & 1;
+      // (1) masked P and dP -> bf16 operands (dk/dv of chunk i-1, their last
+      //     readers, are complete: pdp_full(i) is committed after them)
       if (!DH_ONLY) {
         if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
@@ -878,8 +995,11 @@ __global__ void __launch_bounds__(448)
         tc_fence_before();
         mbar_arrive(&pdp_ready);
       }
-      // (2) dHh = exp(Gam) dH in TMEM, bf16 copy
-      if (!mbar_wait(&eg_ready[b], (ph_egr >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      // (2) dHh = exp(Gam) dH in TMEM; its bf16 copy replaces chunk i-1's
+      //     once dk/dv of chunk i-1 have read that
+      if (!mbar_wait(&eg_ready[b], (ph_egr >> b) & 1, WAIT_CYCLES) ||
+          (i >= 1 && !mbar_wait(&dh_full, (i - 1) & 1, WAIT_CYCLES)))
+        BW_FAIL_AND_BREAK
       ph_egr ^= 1u << b;
       tc_fence_after();
       {
@@ -887,11 +1007,14 @@ __global__ void __launch_bounds__(448)
         tmem_ld16(tEG + 64 * b + lane_off + 48, e1);
         tmem_ld_wait(e1);
         const float eGam = __frcp_rn(__uint_as_float(e1[15]));  // 1 / exp(-Gam)
+        tc_fence_before();
+        mbar_arrive(&eg_free[b]);
         decay *= eGam;
         uint8_t *Dt = sm + bsm::DH;
         const int64_t slot = DH_ONLY ? -1 : ckpt_slot(gc0, doc_c0, j, nch);
         const float *ck = slot >= 0 ? a.ckpt + ((slot * H + h) * KD + c) * VD : nullptr;
         float bnd = 0.f;
+        bool waited = DH_ONLY || i == 0;
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t r[32];
@@ -902,78 +1025,40 @@ __global__ void __launch_bounds__(448)
             for (int e = 0; e < 32; ++e) bnd += ck[32 * cb + e] * __uint_as_float(r[e]);
           }
 #pragma unroll
-          for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(eGam * __uint_as_float(r[u]));
+          for (int w = 0; w < 32; ++w) r[w] = __float_as_uint(eGam * __uint_as_float(r[w]));
           tmem_st32(tDH + lane_off + 32 * cb, r);
-          if (!DH_ONLY)
+          if (!DH_ONLY) {
+            if (!waited) {
+              if (!mbar_wait(&kv_full, (i - 1) & 1, WAIT_CYCLES)) {
+                atomicExch(&abort_flag, 1);
+                break;
+              }
+              waited = true;
+            }
 #pragma unroll
-          for (int n = 0; n < 32; n += 8)
-            st_shared_v4(smem_u32(Dt + sw128_off(c, 32 * cb + n, 128)),
-                         pack_bf16(__uint_as_float(r[n]), __uint_as_float(r[n + 1])),
-                         pack_bf16(__uint_as_float(r[n + 2]), __uint_as_float(r[n + 3])),
-                         pack_bf16(__uint_as_float(r[n + 4]), __uint_as_float(r[n + 5])),
-                         pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
+            for (int n = 0; n < 32; n += 8)
+              st_shared_v4(smem_u32(Dt + sw128_off(c, 32 * cb + n, 128)),
+                           pack_bf16(__uint_as_float(r[n]), __uint_as_float(r[n + 1])),
+                           pack_bf16(__uint_as_float(r[n + 2]), __uint_as_float(r[n + 3])),
+                           pack_bf16(__uint_as_float(r[n + 4]), __uint_as_float(r[n + 5])),
+                           pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
+          }
         }
+        if (*abortp) break;
         tmem_st_wait();
-        if (ck) carry = bnd;  // exact (S_end (.) dH_end) 1_V at this boundary
+        if (!DH_ONLY) {
+          // exact (S_end (.) dH_end) 1_V at this boundary, for the carry
+          reinterpret_cast<float *>(sm + bsm::BND)[b * 128 + c] = bnd;
+          mbar_arrive(&bnd_ready[b]);
+        }
       }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&dh_ready);
-      // (3) dk, dg (thread = channel c) and dv (thread = value column c)
-      if (!mbar_wait(&kv_full, i & 1, WAIT_CYCLES) ||
-          (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)))
-        BW_FAIL_AND_BREAK
-      tc_fence_after();
-      if (!DH_ONLY) {
-        const uint8_t *k = sm + bsm::K + st * 16384;
-        float sk = 0.f, qtot = 0.f;
-#pragma unroll
-        for (int blk = 3; blk >= 0; --blk) {
-          uint32_t acc[16], eg[16];
-          tmem_ld16(tDK + lane_off + 16 * blk, acc);
-          tmem_ld16(tEG + 64 * b + lane_off + 16 * blk, eg);
-          const float *src = a.dgp + ((tok0 + 16 * blk) * H + h) * KD + c;
-          float qp[16];
-          uint16_t kb[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            qp[u] = 16 * blk + u < L ? __ldg(src + (int64_t)u * H * KD) : 0.f;
-            kb[u] = ld_u16(k + sw128_off(16 * blk + u, c, 64));
-          }
-          tmem_ld_wait(acc);
-          tmem_ld_wait(eg);
-          float dkv[16], dgv[16];
-#pragma unroll
-          for (int u = 15; u >= 0; --u) {
-            const int t = 16 * blk + u;
-            dkv[u] = __uint_as_float(eg[u]) * __uint_as_float(acc[u]);
-            if (t < L) sk += bf16_bits_to_f32(kb[u]) * dkv[u];
-            dgv[u] = qp[u] - sk + carry;
-          }
-          if (blk == 0) qtot = qp[0];
-          const int64_t row = ((tok0 + 16 * blk) * H + h) * KD + 32 * qw;
-          transpose_4x4_blocks(dkv, lane);
-          store_block_bf16(a.dk + row, H * KD, dkv, lane, 16 * blk, L);
-          transpose_4x4_blocks(dgv, lane);
-          store_block_f32(a.dg + row, H * KD, dgv, lane, 16 * blk, L);
-        }
-        carry += qtot - sk;
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          uint32_t acc[16];
-          tmem_ld16(tDV + lane_off + 16 * blk, acc);
-          tmem_ld_wait(acc);
-          float dvv[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) dvv[u] = __uint_as_float(acc[u]);
-          transpose_4x4_blocks(dvv, lane);
-          store_block_bf16(a.dv + ((tok0 + 16 * blk) * H + h) * VD + 32 * qw, H * VD, dvv, lane, 16 * blk, L);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&eg_free[b]);
-      if (!DH_ONLY) mbar_arrive(&kempty[st]);
     }
+    // the last dH update
+    if (nch > 0 && !*abortp && !mbar_wait(&dh_full, (nch - 1) & 1, WAIT_CYCLES)) atomicExch(&abort_flag, 1);
+    tc_fence_after();
     float *dst = nullptr;
     if (DH_ONLY && nch > 0) {
       dst = a.lrout + ((u * H + h) * KD + c) * VD;
@@ -988,10 +1073,10 @@ __global__ void __launch_bounds__(448)
         tmem_ld32(tDH + lane_off + 32 * cb, r);
         tmem_ld_wait32(r);
 #pragma unroll
-        for (int u = 0; u < 32; u += 4)
-          *reinterpret_cast<float4 *>(dst + 32 * cb + u) =
-              make_float4(__uint_as_float(r[u]), __uint_as_float(r[u + 1]), __uint_as_float(r[u + 2]),
-                          __uint_as_float(r[u + 3]));
+        for (int w = 0; w < 32; w += 4)
+          *reinterpret_cast<float4 *>(dst + 32 * cb + w) =
+              make_float4(__uint_as_float(r[w]), __uint_as_float(r[w + 1]), __uint_as_float(r[w + 2]),
+                          __uint_as_float(r[w + 3]));
       }
     }
   }
@@ -1018,7 +1103,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       !make_map(&maps.dO, dO, true, VD, pr.H, BT, 64) ||
       !make_map(&maps.dgp, dgp, false, KD, pr.H, BT, 32) ||
       !make_map(&maps.dq, dq, true, KD, pr.H, BT, 64) ||
-      !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32))
+      !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32) ||
+      !make_map(&maps.dk, dk, true, KD, pr.H, BT, 64))
     return cudaErrorInvalidValue;
   BwdArgs a;
   memset(&a, 0, sizeof(a));
