@@ -35,7 +35,7 @@ namespace glacore {
 namespace tc {
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dO, dgp, dq, g, dk;
+  CUtensorMap q, k, v, dO, dgp, dq, g, dk, dv, dg;
 };
 struct BwdArgs {
   Units units;
@@ -594,13 +594,13 @@ __global__ void __launch_bounds__(448)
 namespace bsm {  // shared-memory carve-up (bytes)
 constexpr int NS = 2;
 constexpr uint32_t Q = 0;          // 2 x 16 KB q, then qt in place
-constexpr uint32_t K = 32768;      // 2 x 16 KB raw k, then dk in place (store source)
-constexpr uint32_t KT = 65536;     // 2 x 16 KB kt
-constexpr uint32_t V = 98304;      // 2 x 16 KB
-constexpr uint32_t DO = 131072;    // 2 x 16 KB
-constexpr uint32_t P = 163840;     // 8 KB masked P  (bf16 [t][s])
-constexpr uint32_t DP = 172032;    // 8 KB masked dP (bf16 [t][s])
-constexpr uint32_t DH = 180224;    // 32 KB dHh (bf16 [c][v])
+constexpr uint32_t K = 32768;      // 2 x 16 KB k, then kt in place, then dk (store source)
+constexpr uint32_t V = 65536;      // 2 x 16 KB v, then dv (store source)
+constexpr uint32_t DO = 98304;     // 2 x 16 KB
+constexpr uint32_t P = 131072;     // 8 KB masked P  (bf16 [t][s])
+constexpr uint32_t DP = 139264;    // 8 KB masked dP (bf16 [t][s])
+constexpr uint32_t DH = 147456;    // 32 KB dHh (bf16 [c][v])
+constexpr uint32_t DG = 180224;    // 32 KB gate-gradient partials from the dq pass, then dg
 constexpr uint32_t XCH = 212992;   // 2 x 2 x 128 fp32 gate products
 constexpr uint32_t XK = 215040;    // 2 x 2 x 128 fp32: token-half totals of k (.) dk
 constexpr uint32_t BND = 217088;   // 2 x 128 fp32: exact gate-gradient carry at checkpoints
@@ -612,19 +612,20 @@ constexpr uint32_t BYTES = 218112;
 // writes the gradient at the piece start and the piece's total decay.
 // First pieces have nothing to contribute and exit.
 //
-// Thread roles: warp 0 lane 0 TMA loads of q, v, do; lane 1 TMA loads of raw
-// k; lane 2 TMA stores of dk.  Warp 1 MMA + TMEM.  Warps 2..9 per-channel
-// warps (key channel / value column c, token half th): qt, kt and exp(-G)
-// of chunk i, then the dk / dg / dv epilogue of chunk i-1.  Warps 10..13
-// mask P and dP and scale the state gradient.
+// Thread roles: warp 0 lane 0 TMA loads of q, do; lane 1 TMA loads of k, v;
+// lane 2 TMA loads of the gate-gradient partials and TMA stores of dk, dv,
+// dg.  Warp 1 MMA + TMEM.  Warps 2..9 per-channel warps (key channel /
+// value column c, token half th): qt, kt and exp(-G) of chunk i, then the
+// dk / dg / dv epilogue of chunk i-1, written over kt, v and the partials.
+// Warps 10..13 mask P and dP and scale the state gradient.
 template <bool DH_ONLY>
 __global__ void __launch_bounds__(448)
     gla_bwd_rev_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[bsm::NS], empty[bsm::NS], kfull[bsm::NS], kempty[bsm::NS],
-      prep_done[bsm::NS], pdp_full, pdp_ready, dh_ready, dh_full, kv_full, kv_free, eg_ready[2],
-      eg_free[2], bnd_ready[2], out_ready[bsm::NS];
+      prep_done[bsm::NS], out_ready[bsm::NS], pdp_full, pdp_ready, dh_ready, dh_full, kv_full, kv_free,
+      eg_ready[2], eg_free[2], bnd_ready[2], dg_full;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -644,12 +645,12 @@ __global__ void __launch_bounds__(448)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < bsm::NS; ++i) {
-      mbar_init(&full[i], 1);    // q, v, do (kt is written here too): MMA commit
+      mbar_init(&full[i], 1);    // q, do: released by the MMA commit
       mbar_init(&empty[i], 1);
-      mbar_init(&kfull[i], 1);   // raw k, then dk: released by the store thread
+      mbar_init(&kfull[i], 1);   // k, v (then kt, dk, dv): released by the store thread
       mbar_init(&kempty[i], 1);
       mbar_init(&prep_done[i], 256);
-      mbar_init(&out_ready[i], 256);  // dk written over raw k (per k stage)
+      mbar_init(&out_ready[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&eg_ready[i], 256);
@@ -662,6 +663,7 @@ __global__ void __launch_bounds__(448)
     mbar_init(&dh_full, 1);
     mbar_init(&kv_full, 1);
     mbar_init(&kv_free, 256);
+    mbar_init(&dg_full, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -677,11 +679,9 @@ __global__ void __launch_bounds__(448)
   // chunks are visited in reverse: iteration i handles chunk j = nch - 1 - i
   if (warp == 0) {
     if (lane == 0) {
-      // ring of q, v, do (+ kt written by the prep): released by the MMA commit
+      // ring of q, do: released by the MMA commit
       tma_prefetch_desc(&maps.q);
-      tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.dO);
-      tma_prefetch_desc(&maps.dgp);
       tma_prefetch_desc(&maps.g);
       for (int i = 0; i < nch; ++i) {
         const int j = nch - 1 - i, st = i % bsm::NS;
@@ -689,57 +689,75 @@ __global__ void __launch_bounds__(448)
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
-        if (i == 0 && !DH_ONLY)  // gate-gradient partials of the first chunk the epilogue reads
-          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.dgp, x, h, tok);
         if (j - 2 >= 0) {
           const int tp = tok - 2 * C;
           for (int x = 0; x < 128; x += 64) {
             tma_prefetch_3d(&maps.q, x, h, tp);
+            tma_prefetch_3d(&maps.dO, x, h, tp);
             if (!DH_ONLY) {
               tma_prefetch_3d(&maps.k, x, h, tp);
               tma_prefetch_3d(&maps.v, x, h, tp);
             }
-            tma_prefetch_3d(&maps.dO, x, h, tp);
           }
-          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
+          for (int x = 0; x < 128; x += 32) {
+            tma_prefetch_3d(&maps.g, x, h, tp);
+            if (!DH_ONLY) tma_prefetch_3d(&maps.dgp, x, h, tp);
+          }
         }
-        if (j - 1 >= 0 && !DH_ONLY)
-          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.dgp, x, h, tok - C);
-        mbar_expect_tx(&full[st], (DH_ONLY ? 2 : 3) * 16384);
+        mbar_expect_tx(&full[st], 2 * 16384);
         for (int x = 0; x < 2; ++x) {
           tma_load_3d(sm + bsm::Q + st * 16384 + x * 8192, &maps.q, 64 * x, h, tok, &full[st]);
-          if (!DH_ONLY)
-            tma_load_3d(sm + bsm::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &full[st]);
           tma_load_3d(sm + bsm::DO + st * 16384 + x * 8192, &maps.dO, 64 * x, h, tok, &full[st]);
         }
       }
     } else if (lane == 1 && !DH_ONLY) {
-      // ring of raw k: released once dk (written over it) has been stored
+      // ring of k and v: released once dk and dv (written over them) are stored
       tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
       for (int i = 0; i < nch; ++i) {
         const int j = nch - 1 - i, st = i % bsm::NS;
         if (i >= bsm::NS && !mbar_wait(&kempty[st], ((i / bsm::NS) - 1) & 1, WAIT_CYCLES))
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
-        mbar_expect_tx(&kfull[st], 16384);
-        for (int x = 0; x < 2; ++x)
+        mbar_expect_tx(&kfull[st], 2 * 16384);
+        for (int x = 0; x < 2; ++x) {
           tma_load_3d(sm + bsm::K + st * 16384 + x * 8192, &maps.k, 64 * x, h, tok, &kfull[st]);
+          tma_load_3d(sm + bsm::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &kfull[st]);
+        }
       }
     } else if (lane == 2 && !DH_ONLY) {
-      // dk stores of full chunks (a ragged chunk is stored by its epilogue threads)
+      // gate-gradient partials in, dk / dv / dg of full chunks out (a ragged
+      // chunk is stored by its epilogue threads)
+      tma_prefetch_desc(&maps.dgp);
       tma_prefetch_desc(&maps.dk);
+      tma_prefetch_desc(&maps.dv);
+      tma_prefetch_desc(&maps.dg);
+      if (nch > 0) {
+        mbar_expect_tx(&dg_full, 32768);
+        for (int x = 0; x < 4; ++x)
+          tma_load_3d(sm + bsm::DG + x * 8192, &maps.dgp, 32 * x, h, (int)(s0 + (int64_t)(nch - 1) * C),
+                      &dg_full);
+      }
       for (int i = 0; i < nch; ++i) {
         const int j = nch - 1 - i, st = i % bsm::NS;
         const int64_t tok0 = s0 + (int64_t)j * C;
         if (!mbar_wait(&out_ready[st], (i / bsm::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         if (s1 - tok0 >= C) {
-          for (int x = 0; x < 2; ++x)
+          for (int x = 0; x < 2; ++x) {
             tma_store_3d(&maps.dk, sm + bsm::K + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
+            tma_store_3d(&maps.dv, sm + bsm::V + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
+          }
+          for (int x = 0; x < 4; ++x) tma_store_3d(&maps.dg, sm + bsm::DG + x * 8192, 32 * x, h, (int)tok0);
           bulk_commit();
           bulk_wait_read_all();
         }
         mbar_arrive(&kempty[st]);
+        if (i + 1 < nch) {
+          mbar_expect_tx(&dg_full, 32768);
+          for (int x = 0; x < 4; ++x)
+            tma_load_3d(sm + bsm::DG + x * 8192, &maps.dgp, 32 * x, h, (int)(tok0 - C), &dg_full);
+        }
       }
       bulk_wait_all();
     }
@@ -754,7 +772,7 @@ __global__ void __launch_bounds__(448)
       const uint32_t pa = sbase + bsm::P, dpa = sbase + bsm::DP, dha = sbase + bsm::DH;
       for (int i = 0; i < nch; ++i) {
         const int st = i % bsm::NS;
-        const uint32_t qa = sbase + bsm::Q + st * 16384, kta = sbase + bsm::KT + st * 16384;
+        const uint32_t qa = sbase + bsm::Q + st * 16384, kta = sbase + bsm::K + st * 16384;
         const uint32_t va = sbase + bsm::V + st * 16384, doa = sbase + bsm::DO + st * 16384;
         if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_prep ^= 1u << st;
@@ -840,7 +858,7 @@ __global__ void __launch_bounds__(448)
             for (int w = 0; w < 16; ++w) sts_u16(qc.at(16 * hb + w), qb[w]);
           }
         }
-        // kt = k exp(-G) (separate tile; raw k is kept for k (.) dk); exp(-G) -> TMEM
+        // kt = k exp(-G) in place; exp(-G) -> TMEM
         if (i >= 2) {
           if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
           ph_free ^= 1u << b;
@@ -848,7 +866,6 @@ __global__ void __launch_bounds__(448)
         tc_fence_after();
         {
           const ColBf16 kc(sbase + bsm::K + st * 16384, 32 * th, c);
-          const ColBf16 ktc(sbase + bsm::KT + st * 16384, 32 * th, c);
           float e = cg.after * inv;  // exp(-G_t), walking t downwards
 #pragma unroll
           for (int hb = 1; hb >= 0; --hb) {
@@ -867,7 +884,7 @@ __global__ void __launch_bounds__(448)
             }
             if (!DH_ONLY) {
 #pragma unroll
-              for (int w = 0; w < 16; ++w) sts_u16(ktc.at(16 * hb + w), kb[w]);
+              for (int w = 0; w < 16; ++w) sts_u16(kc.at(16 * hb + w), kb[w]);
             }
             tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
           }
@@ -881,21 +898,24 @@ __global__ void __launch_bounds__(448)
       if (!DH_ONLY && i >= 1) {
         // epilogue of chunk jj (visited at ii = i - 1), this thread's half:
         //   dk_t = exp(-G_t) acc_t (channel c),  dv_t (value column c),
-        //   dg_t = dgp_t - sum_{r >= t in chunk} k_r dk_r + carry
+        //   dg_t = dgp_t - sum_{r >= t in chunk} k_r dk_r + carry,  k dk = kt acc
         const int ii = i - 1, jj = nch - 1 - ii, bb = ii & 1, stt = ii % bsm::NS;
         const int64_t tok0 = s0 + (int64_t)jj * C;
         const int L = (int)min((int64_t)C, s1 - tok0);
         if (!mbar_wait(&kv_full, ii & 1, WAIT_CYCLES) ||
-            !mbar_wait(&bnd_ready[bb], (ii >> 1) & 1, WAIT_CYCLES))
+            !mbar_wait(&bnd_ready[bb], (ii >> 1) & 1, WAIT_CYCLES) ||
+            !mbar_wait(&dg_full, ii & 1, WAIT_CYCLES))
           BW_FAIL_AND_BREAK
         tc_fence_after();
         // the carry restarts from the exact boundary term at a checkpoint
         const float cin = ckpt_slot(gc0, doc_c0, jj, nch) >= 0
                               ? reinterpret_cast<const float *>(sm + bsm::BND)[bb * 128 + c]
                               : carry;
-        const float *dgp = a.dgp + (tok0 * H + h) * KD + c;
-        const float qtot = __ldg(dgp);  // the chunk's q (.) dq total (suffix from its first token)
         const ColBf16 kc(sbase + bsm::K + stt * 16384, 32 * th, c);
+        const ColBf16 vc(sbase + bsm::V + stt * 16384, 32 * th, c);
+        const ColF32 gc(sbase + bsm::DG, 32 * th, c);
+        // the chunk's q (.) dq total is the partial at its first token
+        const float qtot = lds_f32(sbase + bsm::DG + sw128_off_f32(0, c, 64));
         float dgv[32];
         float sk = 0.f;
 #pragma unroll
@@ -908,7 +928,7 @@ __global__ void __launch_bounds__(448)
           uint16_t kb[16];
 #pragma unroll
           for (int w = 0; w < 16; ++w) {
-            qp[w] = tb + w < L ? __ldg(dgp + (int64_t)(tb + w) * H * KD) : 0.f;
+            qp[w] = lds_f32(gc.at(16 * blk + w));
             kb[w] = lds_u16(kc.at(16 * blk + w));
           }
           tmem_ld_wait(acc);
@@ -917,7 +937,7 @@ __global__ void __launch_bounds__(448)
 #pragma unroll
           for (int w = 15; w >= 0; --w) {
             dkv[w] = __uint_as_float(eg[w]) * __uint_as_float(acc[w]);
-            if (tb + w < L) sk += bf16_bits_to_f32(kb[w]) * dkv[w];
+            sk += bf16_bits_to_f32(kb[w]) * __uint_as_float(acc[w]);  // kt is 0 past L
             dgv[16 * blk + w] = qp[w] - sk + cin;
           }
           if (L == C) {
@@ -937,8 +957,13 @@ __global__ void __launch_bounds__(448)
           float dvv[16];
 #pragma unroll
           for (int w = 0; w < 16; ++w) dvv[w] = __uint_as_float(acc[w]);
-          transpose_4x4_blocks(dvv, lane);
-          store_block_bf16(a.dv + ((tok0 + tb) * H + h) * VD + 32 * qw, H * VD, dvv, lane, tb, L);
+          if (L == C) {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) sts_u16(vc.at(16 * blk + w), f32_to_bf16_bits(dvv[w]));
+          } else {
+            transpose_4x4_blocks(dvv, lane);
+            store_block_bf16(a.dv + ((tok0 + tb) * H + h) * VD + 32 * qw, H * VD, dvv, lane, tb, L);
+          }
         }
         tc_fence_before();
         mbar_arrive(&kv_free);
@@ -948,14 +973,19 @@ __global__ void __launch_bounds__(448)
         named_bar(2, 256);
         const float other = xk[(1 - th) * 128 + c];
         const float off = th == 0 ? other : 0.f;
+        if (L == C) {
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          float v[16];
+          for (int w = 0; w < 32; ++w) sts_f32(gc.at(w), dgv[w] - off);
+        } else {
 #pragma unroll
-          for (int w = 0; w < 16; ++w) v[w] = dgv[16 * blk + w] - off;
-          const int tb = 32 * th + 16 * blk;
-          transpose_4x4_blocks(v, lane);
-          store_block_f32(a.dg + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
+          for (int blk = 0; blk < 2; ++blk) {
+            float v[16];
+#pragma unroll
+            for (int w = 0; w < 16; ++w) v[w] = dgv[16 * blk + w] - off;
+            const int tb = 32 * th + 16 * blk;
+            transpose_4x4_blocks(v, lane);
+            store_block_f32(a.dg + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
+          }
         }
         carry = cin + qtot - (sk + other);
         fence_async_smem();
@@ -1104,7 +1134,9 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       !make_map(&maps.dgp, dgp, false, KD, pr.H, BT, 32) ||
       !make_map(&maps.dq, dq, true, KD, pr.H, BT, 64) ||
       !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32) ||
-      !make_map(&maps.dk, dk, true, KD, pr.H, BT, 64))
+      !make_map(&maps.dk, dk, true, KD, pr.H, BT, 64) ||
+      !make_map(&maps.dv, dv, true, VD, pr.H, BT, 64) ||
+      !make_map(&maps.dg, dg, false, KD, pr.H, BT, 32))
     return cudaErrorInvalidValue;
   BwdArgs a;
   memset(&a, 0, sizeof(a));
