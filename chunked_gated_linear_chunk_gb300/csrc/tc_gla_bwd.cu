@@ -748,11 +748,15 @@ __global__ void __launch_bounds__(448)
             tma_store_3d(&maps.dk, sm + bsm::K + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
             tma_store_3d(&maps.dv, sm + bsm::V + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
           }
+          bulk_commit();
           for (int x = 0; x < 4; ++x) tma_store_3d(&maps.dg, sm + bsm::DG + x * 8192, 32 * x, h, (int)tok0);
           bulk_commit();
+          bulk_wait_read_all_but_one();  // the k / v stage can be refilled
+          mbar_arrive(&kempty[st]);
           bulk_wait_read_all();
+        } else {
+          mbar_arrive(&kempty[st]);
         }
-        mbar_arrive(&kempty[st]);
         if (i + 1 < nch) {
           mbar_expect_tx(&dg_full, 32768);
           for (int x = 0; x < 4; ++x)
@@ -833,9 +837,7 @@ __global__ void __launch_bounds__(448)
 #pragma unroll
         for (int w = 0; w < 32; ++w) cg.x[w] = xn[w];
         if (j >= 1) load_gates_to(xn, a.g, tok0 - C, H, h, c, th, C);
-        if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES) ||
-            (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)))
-          BW_FAIL_AND_BREAK
+        if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_full ^= 1u << st;
         exchange_gates(cg, reinterpret_cast<float *>(sm + bsm::XCH) + b * 256, c, th, L);
         const float inv = __frcp_rn(cg.total);
@@ -863,6 +865,7 @@ __global__ void __launch_bounds__(448)
           if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
           ph_free ^= 1u << b;
         }
+        if (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
         {
           const ColBf16 kc(sbase + bsm::K + st * 16384, 32 * th, c);
