@@ -51,19 +51,31 @@ struct Unit {
   int32_t doc, piece, npieces, pad;
 };
 
-// Units of a launch: an explicit table (pieces) or, when `table` is null,
-// one unit per document of `docs`.
+// Units of a launch: an explicit table (pieces of packed documents); with
+// `table` null and plen > 0, rows of docs.T tokens each cut into pieces of
+// plen tokens (unit u = piece u % n of row u / n); otherwise one unit per
+// document of `docs`.
 struct Units {
   const Unit *table;
   Docs docs;
+  int64_t plen;
   __device__ __forceinline__ Unit get(int64_t u) const {
     if (table) return table[u];
     Unit r;
+    r.pad = 0;
+    if (plen > 0) {
+      const int64_t np = (docs.T + plen - 1) / plen, d = u / np, p = u - d * np;
+      r.start = d * docs.T + p * plen;
+      r.end = min(r.start + plen, (d + 1) * docs.T);
+      r.doc = (int32_t)d;
+      r.piece = (int32_t)p;
+      r.npieces = (int32_t)np;
+      return r;
+    }
     docs.range(u, r.start, r.end);
     r.doc = (int32_t)u;
     r.piece = 0;
     r.npieces = 1;
-    r.pad = 0;
     return r;
   }
 };

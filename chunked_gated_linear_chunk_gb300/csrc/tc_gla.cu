@@ -55,11 +55,10 @@ struct FwdArgs {
   int64_t H;
   float scale;
   const float *g;
-  const float *h0;    // [n_docs,H,K,V] state entering piece 0, or null
-  const float *sin;   // [units,H,K,V] state entering pieces > 0 (scan output)
+  const float *h0;    // [n_docs,H,K,V] state entering the document, or null
   float *ht;          // [n_docs,H,K,V] final state (written by the last piece)
-  float *lout;        // state-only mode: [units,H,K,V] piece end state from zero
-  float *dout;        // state-only mode: [units,H,K] exp(sum of g over the piece)
+  float *lbuf;        // [units,H,K,V] piece end state from zero (state-only mode writes it)
+  float *dbuf;        // [units,H,K] exp(sum of g over the piece) (state-only mode writes it)
   __nv_bfloat16 *o;
   int *err;
 };
@@ -370,14 +369,13 @@ __global__ void __launch_bounds__(448)
     const int64_t H = a.H;
     const int v0 = vb * 64;
     float S[64];
-    {
-      const float *init = nullptr;
-      if (!STATE_ONLY)
-        init = un.piece == 0 ? (a.h0 ? a.h0 + (d * H + h) * KD * VD : nullptr)
-                             : a.sin + (u * H + h) * KD * VD;
-      if (init) init += (int64_t)c * VD + v0;
+    if (STATE_ONLY) {
 #pragma unroll
-      for (int n = 0; n < 64; ++n) S[n] = init ? init[n] : 0.f;
+      for (int n = 0; n < 64; ++n) S[n] = 0.f;
+    } else {
+      // state entering the unit: h0 folded over the document's earlier pieces
+      const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
+      piece_state_in<64>(S, h0row, a.lbuf, a.dbuf, u - un.piece, un.piece, H, h, c, v0);
     }
     float decay = 1.f;  // state-only mode: exp(sum of g over the piece)
     if (!STATE_ONLY) {
@@ -473,8 +471,8 @@ __global__ void __launch_bounds__(448)
     }
     float *dst = nullptr;
     if (STATE_ONLY && nch > 0) {
-      dst = a.lout + ((u * H + h) * KD + c) * VD + v0;
-      if (vb == 0) a.dout[(u * H + h) * KD + c] = decay;
+      dst = a.lbuf + ((u * H + h) * KD + c) * VD + v0;
+      if (vb == 0) a.dbuf[(u * H + h) * KD + c] = decay;
     } else if (!STATE_ONLY && a.ht && last_piece) {
       dst = a.ht + ((d * H + h) * KD + c) * VD + v0;
     }
@@ -517,8 +515,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
     return cudaErrorInvalidValue;
   FwdArgs a;
   memset(&a, 0, sizeof(a));
-  a.units.table = nullptr;
-  a.units.docs = docs;
+  a.units = units_of(docs, Lo, ws);
   a.H = pr.H;
   a.scale = pr.scale;
   a.g = pr.g;
@@ -533,20 +530,16 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
     return e;
   const dim3 grid((unsigned)(2 * Lo.max_units), (unsigned)pr.H);
   if (Lo.pieces) {
-    Unit *ut = (Unit *)(ws + Lo.off_units);
-    int64_t *ub = (int64_t *)(ws + Lo.off_ubase);
-    float *Lb = (float *)(ws + Lo.off_L), *Db = (float *)(ws + Lo.off_D), *Sin = (float *)(ws + Lo.off_sin);
-    if ((e = launch_build_units(docs, Lo.plen, ut, ub, Lo.max_units, st)) != cudaSuccess) return e;
-    a.units.table = ut;
+    if (Lo.table &&
+        (e = launch_build_units(docs, Lo.plen, (Unit *)(ws + Lo.off_units), Lo.max_units, st)) != cudaSuccess)
+      return e;
+    a.lbuf = (float *)(ws + Lo.off_L);
+    a.dbuf = (float *)(ws + Lo.off_D);
     FwdArgs as = a;
-    as.lout = Lb;
-    as.dout = Db;
     as.ht = nullptr;
     gla_fwd_kernel<true><<<grid, 448, smem, st>>>(maps, as);
     mark_launch("gla_fwd_piece_state_kernel", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_fwd_scan(docs, ub, pr.H, pr.h0, Lb, Db, Sin, st)) != cudaSuccess) return e;
-    a.sin = Sin;
   }
   gla_fwd_kernel<false><<<grid, 448, smem, st>>>(maps, a);
   mark_launch("gla_fwd_kernel", st);
@@ -569,8 +562,8 @@ cudaError_t fwd_piece_states(const Prob &pr, const Units &units, int64_t max_uni
   a.H = pr.H;
   a.scale = pr.scale;
   a.g = pr.g;
-  a.lout = Lb;
-  a.dout = Db;
+  a.lbuf = Lb;
+  a.dbuf = Db;
   a.err = pr.err;
   const int smem = fsm::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(gla_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

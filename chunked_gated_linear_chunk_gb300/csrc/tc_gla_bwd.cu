@@ -44,14 +44,13 @@ struct BwdArgs {
   const float *g;
   const float *h0;     // [n_docs,H,K,V] or null
   const float *dht;    // [n_docs,H,K,V] or null
-  const float *sin;    // [units,H,K,V] state entering pieces > 0
-  const float *dhend;  // [units,H,K,V] state gradient leaving pieces but the last
   __nv_bfloat16 *dq, *dk, *dv;
   float *dg, *dh0;
   float *dgp;    // scratch [BT, H, K] fp32
   float *bvec;   // scratch [units, H, K] fp32
-  float *lrout;  // dH-only mode: [units,H,K,V] state gradient at the piece start
-  float *dout;   // dH-only mode: [units,H,K] exp(sum of g over the piece)
+  const float *lf, *df;  // forward piece hand-off: [units,H,K,V] end states from zero, [units,H,K] decays
+  float *lr, *dr;        // reverse piece hand-off (dH-only mode writes them): state gradients
+                         // at the piece starts from zero, decays
   float *ckpt;   // [slots,H,K,V] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
   int *err;
 };
@@ -71,14 +70,6 @@ __device__ __forceinline__ int64_t ckpt_slot(int64_t gc0, int64_t doc_c0, int j,
   const int64_t jd = gc0 - doc_c0 + j;  // chunk index inside the document
   if ((jd + 1) % CKPT_CHUNKS) return -1;
   return (gc0 + j) / CKPT_CHUNKS;
-}
-
-// State gradient leaving unit u (its end): dht for the document's last
-// piece, the reverse scan's value otherwise.
-__device__ __forceinline__ const float *dh_end_ptr(const BwdArgs &a, const Unit &un, int64_t u,
-                                                   int64_t h) {
-  if (un.piece == un.npieces - 1) return a.dht ? a.dht + ((int64_t)un.doc * a.H + h) * KD * VD : nullptr;
-  return a.dhend + (u * a.H + h) * KD * VD;
 }
 
 #define BW_FAIL_AND_BREAK         \
@@ -455,16 +446,17 @@ __global__ void __launch_bounds__(448)
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     uint8_t *St = sm + asm_::S;
-    // S (TMEM) = state entering the unit, bf16 copy for chunk 0's readout
+    // S (TMEM) = state entering the unit (h0 folded over the document's
+    // earlier pieces), bf16 copy for chunk 0's readout
     {
-      const float *h0 = un.piece == 0 ? (a.h0 ? a.h0 + (d * H + h) * KD * VD : nullptr)
-                                      : a.sin + (u * H + h) * KD * VD;
-      if (h0) h0 += (int64_t)c * VD;
-#pragma unroll
+      const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
+#pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
+        float sv[32];
+        piece_state_in<32>(sv, h0row, a.lf, a.df, u - un.piece, un.piece, H, h, c, 32 * cb);
         uint32_t r[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(h0 ? h0[32 * cb + i] : 0.f);
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sv[i]);
         tmem_st32(tS + lane_off + 32 * cb, r);
 #pragma unroll
         for (int n = 0; n < 32; n += 8)
@@ -565,18 +557,20 @@ __global__ void __launch_bounds__(448)
       mbar_arrive(&s_ready);
     }
     // final-state term of the gate gradient: bvec = (S_end (.) dH_end) 1_V
+    // (dH_end: dht folded over the document's later pieces)
     if (!*abortp && a.bvec) {
       float acc = 0.f;
-      const float *dhe = dh_end_ptr(a, un, u, h);
-      if (dhe) {
-        const float *dh = dhe + (int64_t)c * VD;
-#pragma unroll
+      const float *dhtrow = a.dht ? a.dht + ((d * H + h) * KD + c) * VD : nullptr;
+      if (dhtrow || un.piece + 1 < un.npieces) {
+#pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
+          float dh[32];
+          piece_grad_out<32>(dh, dhtrow, a.lr, a.dr, u - un.piece, un.piece, un.npieces, H, h, c, 32 * cb);
           uint32_t r[32];
           tmem_ld32(tS + lane_off + 32 * cb, r);
           tmem_ld_wait32(r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc += __uint_as_float(r[i]) * dh[32 * cb + i];
+          for (int i = 0; i < 32; ++i) acc += __uint_as_float(r[i]) * dh[i];
         }
       }
       a.bvec[(u * H + h) * KD + c] = acc;
@@ -1000,15 +994,22 @@ __global__ void __launch_bounds__(448)
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    // dH = dht (or 0)
+    // dH = state gradient leaving the unit: dht folded over the document's
+    // later pieces (0 in dH-only mode)
     {
-      const float *dh = DH_ONLY ? nullptr : dh_end_ptr(a, un, u, h);
-      if (dh) dh += (int64_t)c * VD;
-#pragma unroll
+      const float *dhtrow = (!DH_ONLY && a.dht) ? a.dht + ((d * H + h) * KD + c) * VD : nullptr;
+#pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
+        float dh[32];
+        if (DH_ONLY) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dh[e] = 0.f;
+        } else {
+          piece_grad_out<32>(dh, dhtrow, a.lr, a.dr, u - un.piece, un.piece, un.npieces, H, h, c, 32 * cb);
+        }
         uint32_t r[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(dh ? dh[32 * cb + e] : 0.f);
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(dh[e]);
         tmem_st32(tDH + lane_off + 32 * cb, r);
       }
       tmem_st_wait();
@@ -1094,8 +1095,8 @@ __global__ void __launch_bounds__(448)
     tc_fence_after();
     float *dst = nullptr;
     if (DH_ONLY && nch > 0) {
-      dst = a.lrout + ((u * H + h) * KD + c) * VD;
-      a.dout[(u * H + h) * KD + c] = decay;
+      dst = a.lr + ((u * H + h) * KD + c) * VD;
+      a.dr[(u * H + h) * KD + c] = decay;
     } else if (!DH_ONLY && a.dh0 && un.piece == 0) {
       dst = a.dh0 + ((d * H + h) * KD + c) * VD;
     }
@@ -1143,8 +1144,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     return cudaErrorInvalidValue;
   BwdArgs a;
   memset(&a, 0, sizeof(a));
-  a.units.table = nullptr;
-  a.units.docs = docs;
+  a.units = units_of(docs, Lo, ws);
   a.H = pr.H;
   a.scale = pr.scale;
   a.g = pr.g;
@@ -1167,25 +1167,21 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       (e = cudaFuncSetAttribute(gla_bwd_rev_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
     return e;
   if (Lo.pieces) {
-    Unit *ut = (Unit *)(ws + Lo.off_units);
-    int64_t *ub = (int64_t *)(ws + Lo.off_ubase);
-    float *Lb = (float *)(ws + Lo.off_L), *Db = (float *)(ws + Lo.off_D);
-    float *Sin = (float *)(ws + Lo.off_sin), *Dhe = (float *)(ws + Lo.off_dhend);
-    if ((e = launch_build_units(docs, Lo.plen, ut, ub, Lo.max_units, st)) != cudaSuccess) return e;
-    a.units.table = ut;
-    // states entering every piece (forward piece pass + scan)
-    if ((e = fwd_piece_states(pr, a.units, Lo.max_units, Lb, Db, st)) != cudaSuccess) return e;
-    if ((e = launch_fwd_scan(docs, ub, pr.H, pr.h0, Lb, Db, Sin, st)) != cudaSuccess) return e;
-    // state gradients leaving every piece (reverse piece pass + scan)
-    BwdArgs ar = a;
-    ar.lrout = Lb;
-    ar.dout = Db;
-    gla_bwd_rev_kernel<true><<<grid, 448, smB, st>>>(maps, ar);
+    if (Lo.table &&
+        (e = launch_build_units(docs, Lo.plen, (Unit *)(ws + Lo.off_units), Lo.max_units, st)) != cudaSuccess)
+      return e;
+    a.lf = (const float *)(ws + Lo.off_L);
+    a.df = (const float *)(ws + Lo.off_D);
+    a.lr = (float *)(ws + Lo.off_Lr);
+    a.dr = (float *)(ws + Lo.off_Dr);
+    // local end states of the pieces (forward) and local state gradients at
+    // their starts (reverse); the consumers fold them
+    if ((e = fwd_piece_states(pr, a.units, Lo.max_units, (float *)(ws + Lo.off_L), (float *)(ws + Lo.off_D),
+                              st)) != cudaSuccess)
+      return e;
+    gla_bwd_rev_kernel<true><<<grid, 448, smB, st>>>(maps, a);
     mark_launch("gla_bwd_piece_dh_kernel", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_rev_scan(docs, ub, pr.H, dht, Lb, Db, Dhe, st)) != cudaSuccess) return e;
-    a.sin = Sin;
-    a.dhend = Dhe;
   }
   gla_bwd_dq_kernel<<<grid, 448, smA, st>>>(maps, a);
   mark_launch("gla_bwd_dq_kernel", st);

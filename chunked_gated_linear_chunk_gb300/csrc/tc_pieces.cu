@@ -11,40 +11,35 @@
 // and in reverse time, with Lr_p the state gradient at the start of piece p
 // from its own outputs started from zero at its end,
 //   dH_end[last] = dht,   dH_end[p] = diag(D_{p+1}) dH_end[p+1] + Lr_{p+1}.
-// This file builds the unit (piece) table and runs the two scans; the local
-// states come from state-only modes of the forward and reverse kernels.
+// The consumers fold these recurrences over the earlier (later) pieces of
+// their document when they start (piece_state_in / piece_grad_out in
+// tc.cuh); the local states come from state-only modes of the forward and
+// reverse kernels.  This file builds the unit table of packed documents and
+// sizes the workspace.
 #include "tc.cuh"
 
 namespace glacore {
 namespace tc {
 
-// One CTA: documents -> pieces of `plen` tokens.  ubase[d] = first unit of
-// document d, ubase[n] = number of units; units past it are empty.
+// One CTA: packed documents -> pieces of `plen` tokens, in document order
+// (the pieces of one document are consecutive units); units past the last
+// piece are empty.
 __global__ void __launch_bounds__(1024)
-    build_units_kernel(Docs docs, int64_t plen, Unit *units, int64_t *ubase, int64_t max_units) {
+    build_units_kernel(Docs docs, int64_t plen, Unit *units, int64_t max_units) {
   __shared__ int64_t wbuf[32];
+  __shared__ int64_t base_of_chunk;
   int64_t off = 0;
   for (int64_t base = 0; base < docs.n; base += blockDim.x) {
     const int64_t d = base + threadIdx.x;
-    int64_t np = 0;
+    int64_t np = 0, s = 0, e = 0;
     if (d < docs.n) {
-      int64_t s, e;
       docs.range(d, s, e);
       np = (e - s + plen - 1) / plen;
     }
     int64_t tot;
     const int64_t ex = block_excl_scan(np, wbuf, tot);
-    if (d < docs.n) ubase[d] = off + ex;
-    off += tot;
-  }
-  if (threadIdx.x == 0) ubase[docs.n] = off;
-  __syncthreads();
-  for (int64_t d = threadIdx.x; d < docs.n; d += blockDim.x) {
-    int64_t s, e;
-    docs.range(d, s, e);
-    const int64_t np = (e - s + plen - 1) / plen;
     for (int64_t p = 0; p < np; ++p) {
-      const int64_t u = ubase[d] + p;
+      const int64_t u = off + ex + p;
       if (u >= max_units) break;
       Unit r;
       r.start = s + p * plen;
@@ -55,8 +50,11 @@ __global__ void __launch_bounds__(1024)
       r.pad = 0;
       units[u] = r;
     }
+    off += tot;
   }
-  for (int64_t u = off + threadIdx.x; u < max_units; u += blockDim.x) {
+  if (threadIdx.x == 0) base_of_chunk = off;
+  __syncthreads();
+  for (int64_t u = base_of_chunk + threadIdx.x; u < max_units; u += blockDim.x) {
     Unit r;
     r.start = r.end = 0;
     r.doc = r.piece = r.pad = 0;
@@ -65,58 +63,10 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// grid (n_docs, H, K*V/256): states entering every piece after the first.
-__global__ void fwd_scan_kernel(const int64_t *ubase, int64_t H, const float *h0, const float *L,
-                                const float *D, float *sin) {
-  const int64_t d = blockIdx.x, h = blockIdx.y;
-  const int64_t e = (int64_t)blockIdx.z * blockDim.x + threadIdx.x;  // element of K x V
-  const int64_t KV = (int64_t)KD * VD;
-  const int64_t u0 = ubase[d], np = ubase[d + 1] - u0;
-  if (np <= 1 || e >= KV) return;
-  const int64_t c = e / VD;
-  float S = h0 ? h0[(d * H + h) * KV + e] : 0.f;
-  for (int64_t p = 1; p < np; ++p) {
-    const int64_t up = u0 + p - 1;
-    S = D[(up * H + h) * KD + c] * S + L[(up * H + h) * KV + e];
-    sin[((u0 + p) * H + h) * KV + e] = S;
-  }
-}
-
-// grid (n_docs, H, K*V/256): state gradients leaving every piece but the last.
-__global__ void rev_scan_kernel(const int64_t *ubase, int64_t H, const float *dht, const float *Lr,
-                                const float *D, float *dhend) {
-  const int64_t d = blockIdx.x, h = blockIdx.y;
-  const int64_t e = (int64_t)blockIdx.z * blockDim.x + threadIdx.x;
-  const int64_t KV = (int64_t)KD * VD;
-  const int64_t u0 = ubase[d], np = ubase[d + 1] - u0;
-  if (np <= 1 || e >= KV) return;
-  const int64_t c = e / VD;
-  float G = dht ? dht[(d * H + h) * KV + e] : 0.f;
-  for (int64_t p = np - 2; p >= 0; --p) {
-    const int64_t un = u0 + p + 1;
-    G = D[(un * H + h) * KD + c] * G + Lr[(un * H + h) * KV + e];
-    dhend[((u0 + p) * H + h) * KV + e] = G;
-  }
-}
-
-cudaError_t launch_build_units(const Docs &docs, int64_t plen, Unit *units, int64_t *ubase,
-                               int64_t max_units, cudaStream_t st) {
-  build_units_kernel<<<1, 1024, 0, st>>>(docs, plen, units, ubase, max_units);
+cudaError_t launch_build_units(const Docs &docs, int64_t plen, Unit *units, int64_t max_units,
+                               cudaStream_t st) {
+  build_units_kernel<<<1, 1024, 0, st>>>(docs, plen, units, max_units);
   mark_launch("build_units", st);
-  return cudaGetLastError();
-}
-cudaError_t launch_fwd_scan(const Docs &docs, const int64_t *ubase, int64_t H, const float *h0,
-                            const float *L, const float *D, float *sin, cudaStream_t st) {
-  dim3 grid((unsigned)docs.n, (unsigned)H, (unsigned)((KD * VD + 255) / 256));
-  fwd_scan_kernel<<<grid, 256, 0, st>>>(ubase, H, h0, L, D, sin);
-  mark_launch("piece_fwd_scan", st);
-  return cudaGetLastError();
-}
-cudaError_t launch_rev_scan(const Docs &docs, const int64_t *ubase, int64_t H, const float *dht,
-                            const float *Lr, const float *D, float *dhend, cudaStream_t st) {
-  dim3 grid((unsigned)docs.n, (unsigned)H, (unsigned)((KD * VD + 255) / 256));
-  rev_scan_kernel<<<grid, 256, 0, st>>>(ubase, H, dht, Lr, D, dhend);
-  mark_launch("piece_rev_scan", st);
   return cudaGetLastError();
 }
 
@@ -150,30 +100,30 @@ TcLayout tc_layout(const glacore_problem *p, bool backward) {
   TcLayout L;
   L.plen = piece_len(p, backward);
   L.pieces = L.plen < ((int64_t)1 << 40);
+  L.table = L.pieces && p->segment_ids != nullptr;
   L.max_units = max_units_of(p, L.plen);
-  const size_t mu = (size_t)L.max_units, H = (size_t)p->H, n = (size_t)p->n_seqs;
+  const size_t mu = (size_t)L.max_units, H = (size_t)p->H;
   const size_t state = (size_t)KD * VD * sizeof(float);
   size_t off = 0;
-  L.off_units = L.off_ubase = L.off_L = L.off_D = L.off_sin = L.off_dhend = L.off_dgp = L.off_bvec = 0;
-  L.off_ckpt = 0;
+  L.off_units = L.off_L = L.off_D = L.off_Lr = L.off_Dr = L.off_dgp = L.off_bvec = L.off_ckpt = 0;
   // chunks of all documents (upper bound) -> checkpoint slots
   const int64_t chunks = p->segment_ids ? (p->B * p->T + C - 1) / C + p->n_seqs
                                         : p->B * ((p->T + C - 1) / C);
   L.ckpt_slots = chunks / CKPT_CHUNKS + 1;
   if (L.pieces) {
-    L.off_units = off;
-    off = al256(off + mu * sizeof(Unit));
-    L.off_ubase = off;
-    off = al256(off + (n + 1) * sizeof(int64_t));
+    if (L.table) {
+      L.off_units = off;
+      off = al256(off + mu * sizeof(Unit));
+    }
     L.off_L = off;
     off = al256(off + mu * H * state);
     L.off_D = off;
     off = al256(off + mu * H * KD * sizeof(float));
-    L.off_sin = off;
-    off = al256(off + mu * H * state);
     if (backward) {
-      L.off_dhend = off;
+      L.off_Lr = off;
       off = al256(off + mu * H * state);
+      L.off_Dr = off;
+      off = al256(off + mu * H * KD * sizeof(float));
     }
   }
   if (backward) {
