@@ -105,6 +105,17 @@ __device__ __forceinline__ void load_gates_to(float (&x)[32], const float *g, in
     x[i] = t < L ? __ldg(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
   }
 }
+// Tokens 32 th + I0 .. 32 th + I0 + N - 1 of load_gates_to: the loads of one
+// chunk are issued in parts so that fewer misses are in flight at once.
+template <int I0, int N>
+__device__ __forceinline__ void load_gates_part(float (&x)[32], const float *g, int64_t tok0, int64_t H,
+                                                int h, int c, int th, int L) {
+#pragma unroll
+  for (int i = I0; i < I0 + N; ++i) {
+    const int t = 32 * th + i;
+    x[i] = t < L ? __ldg(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
+  }
+}
 __device__ __forceinline__ void exchange_gates(ChanGate &cg, float *xch, int c, int th, int L) {
   float p = 1.f;
 #pragma unroll
@@ -130,7 +141,7 @@ constexpr uint32_t K = 32768;      // 2 x 16 KB k, then kt in place
 constexpr uint32_t V = 65536;      // 2 x 16 KB
 constexpr uint32_t DO = 98304;     // 2 x 16 KB
 constexpr uint32_t DP = 131072;    // 8 KB masked dP (bf16 [t][s])
-constexpr uint32_t S = 139264;     // 32 KB S (bf16 [c][v], K-major A)
+constexpr uint32_t GT = 139264;    // 32 KB gate tile g [t][c] (fp32, TMA box 32 x 64)
 constexpr uint32_t STG = 172032;   // 32 KB gate-gradient partials (fp32, store source)
 constexpr uint32_t XCH = 204800;   // 2 x 2 x 128 fp32 gate products
 constexpr uint32_t XQ = 206848;    // 2 x 128 fp32: token-half totals of q (.) dq
@@ -138,7 +149,8 @@ constexpr uint32_t BYTES = 207872;
 }  // namespace asm_
 
 // Thread roles: warp 0 lane 0 TMA loads of k, v, do; lane 1 TMA loads of
-// raw q; lane 2 TMA stores of dq and the gate-gradient partials.  Warp 1
+// raw q; lane 2 TMA stores of dq and the gate-gradient partials; lane 3 TMA
+// loads of the gate tile.  Warp 1
 // MMA + TMEM.  Warps 2..9 per-channel warps (key channel c = lane of the
 // warp's TMEM quarter, token half th): gate work and kt for chunk j, then
 // the dq / q (.) dq epilogue of chunk j-1 for their half, written to shared
@@ -149,7 +161,7 @@ __global__ void __launch_bounds__(448)
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[asm_::NS], empty[asm_::NS], qfull[asm_::NS], qempty[asm_::NS],
       prep_done[asm_::NS], dp_full, dp_ready, dq_full[2], dq_free[2], u_full, s_ready, eg_ready[2],
-      eg_free[2], out_ready, stg_free;
+      eg_free[2], out_ready, stg_free, g_full, g_free;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -187,6 +199,8 @@ __global__ void __launch_bounds__(448)
     mbar_init(&s_ready, 128);
     mbar_init(&out_ready, 256);
     mbar_init(&stg_free, 1);
+    mbar_init(&g_full, 1);
+    mbar_init(&g_free, 256);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -195,8 +209,8 @@ __global__ void __launch_bounds__(448)
   const uint32_t tbase = tmem_base;
   const uint32_t sbase = smem_u32(sm);
   volatile int *abortp = &abort_flag;
-  // TMEM columns: dP, dq^T[2], S, exp(G)[2]
-  const uint32_t tDP = tbase, tDQ = tbase + 128, tS = tbase + 256, tEG = tbase + 384;
+  // TMEM columns: dP, S_prev (bf16 A operand), dq^T[2], S, exp(G)[2]
+  const uint32_t tDP = tbase, tSb = tbase + 64, tDQ = tbase + 128, tS = tbase + 256, tEG = tbase + 384;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -262,6 +276,15 @@ __global__ void __launch_bounds__(448)
         mbar_arrive(&stg_free);
       }
       bulk_wait_all();
+    } else if (lane == 3) {
+      // gate tile of each chunk (single buffer: refilled once the prep has read it)
+      for (int j = 0; j < nch; ++j) {
+        if (j >= 1 && !mbar_wait(&g_free, (j - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if (*abortp) break;
+        const int tok = (int)(s0 + (int64_t)j * C);
+        mbar_expect_tx(&g_full, 32768);
+        for (int x = 0; x < 4; ++x) tma_load_3d(sm + asm_::GT + x * 8192, &maps.g, 32 * x, h, tok, &g_full);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -269,7 +292,7 @@ __global__ void __launch_bounds__(448)
       constexpr uint32_t idU = idesc_bf16(128, 128, true, true);
       constexpr uint32_t idQ1 = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idQ2 = idesc_bf16(128, 64, true, false);
-      const uint32_t dpa = sbase + asm_::DP, Sa = sbase + asm_::S;
+      const uint32_t dpa = sbase + asm_::DP;
       uint32_t ph_prep = 0, ph_dqf = 0;
       for (int j = 0; j < nch; ++j) {
         const int st = j % asm_::NS, b = j & 1;
@@ -296,8 +319,7 @@ __global__ void __launch_bounds__(448)
         }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_bf16(tDQ + 64 * b, kdesc(Sa, ks, 128), kdesc(doa, ks, 64), idQ1, ks);
+        for (int ks = 0; ks < 8; ++ks) mma_bf16_ta(tDQ + 64 * b, tSb + 8 * ks, kdesc(doa, ks, 64), idQ1, ks);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tDQ + 64 * b, mdesc(ka, ks, 8192), kdesc(dpa, ks, 64), idQ2, 1);
@@ -311,8 +333,7 @@ __global__ void __launch_bounds__(448)
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     uint32_t ph_full = 0, ph_free = 0, ph_dqf = 0;
-    float xn[32];  // gates of the next chunk, loaded while this one is prepared
-    if (nch > 0) load_gates_to(xn, a.g, s0, H, h, c, th, (int)min((int64_t)C, s1 - s0));
+    const ColF32 gcol(sbase + asm_::GT, 32 * th, c);
     // iteration j: gate work and kt of chunk j, then the epilogue of chunk j-1
     for (int j = 0; j <= nch; ++j) {
       if (j < nch) {
@@ -320,10 +341,10 @@ __global__ void __launch_bounds__(448)
         const int64_t tok0 = s0 + (int64_t)j * C;
         const int L = (int)min((int64_t)C, s1 - tok0);
         ChanGate cg;
+        if (!mbar_wait(&g_full, j & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
 #pragma unroll
-        for (int i = 0; i < 32; ++i) cg.x[i] = xn[i];
-        if (j + 1 < nch)
-          load_gates_to(xn, a.g, tok0 + C, H, h, c, th, (int)min((int64_t)C, s1 - tok0 - C));
+        for (int i = 0; i < 32; ++i) cg.x[i] = 32 * th + i < L ? lds_f32(gcol.at(i)) : 0.f;
+        mbar_arrive(&g_free);
         if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_full ^= 1u << st;
         exchange_gates(cg, reinterpret_cast<float *>(sm + asm_::XCH) + b * 256, c, th, L);
@@ -445,9 +466,8 @@ __global__ void __launch_bounds__(448)
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    uint8_t *St = sm + asm_::S;
     // S (TMEM) = state entering the unit (h0 folded over the document's
-    // earlier pieces), bf16 copy for chunk 0's readout
+    // earlier pieces), bf16 copy (TMEM A operand) for chunk 0's readout
     {
       const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
 #pragma unroll 1
@@ -458,16 +478,12 @@ __global__ void __launch_bounds__(448)
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sv[i]);
         tmem_st32(tS + lane_off + 32 * cb, r);
+        uint32_t pk[16];
 #pragma unroll
-        for (int n = 0; n < 32; n += 8)
-          st_shared_v4(smem_u32(St + sw128_off(c, 32 * cb + n, 128)),
-                       pack_bf16(__uint_as_float(r[n]), __uint_as_float(r[n + 1])),
-                       pack_bf16(__uint_as_float(r[n + 2]), __uint_as_float(r[n + 3])),
-                       pack_bf16(__uint_as_float(r[n + 4]), __uint_as_float(r[n + 5])),
-                       pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
+        for (int n = 0; n < 16; ++n) pk[n] = pack_bf16(sv[2 * n], sv[2 * n + 1]);
+        tmem_st16(tSb + lane_off + 16 * cb, pk);
       }
       tmem_st_wait();
-      fence_async_smem();
       tc_fence_before();
       mbar_arrive(&s_ready);
     }
@@ -520,19 +536,14 @@ __global__ void __launch_bounds__(448)
             ph_dqf ^= 1u << b;
             waited = true;
           }
+          uint32_t pk[16], pk2[16];
 #pragma unroll
-          for (int n = 0; n < 32; n += 8) {
-            st_shared_v4(smem_u32(St + sw128_off(c, 32 * cb + n, 128)),
-                         pack_bf16(__uint_as_float(r[n]), __uint_as_float(r[n + 1])),
-                         pack_bf16(__uint_as_float(r[n + 2]), __uint_as_float(r[n + 3])),
-                         pack_bf16(__uint_as_float(r[n + 4]), __uint_as_float(r[n + 5])),
-                         pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
-            st_shared_v4(smem_u32(St + sw128_off(c, 32 * cb + 32 + n, 128)),
-                         pack_bf16(__uint_as_float(r2[n]), __uint_as_float(r2[n + 1])),
-                         pack_bf16(__uint_as_float(r2[n + 2]), __uint_as_float(r2[n + 3])),
-                         pack_bf16(__uint_as_float(r2[n + 4]), __uint_as_float(r2[n + 5])),
-                         pack_bf16(__uint_as_float(r2[n + 6]), __uint_as_float(r2[n + 7])));
+          for (int n = 0; n < 16; ++n) {
+            pk[n] = pack_bf16(__uint_as_float(r[2 * n]), __uint_as_float(r[2 * n + 1]));
+            pk2[n] = pack_bf16(__uint_as_float(r2[2 * n]), __uint_as_float(r2[2 * n + 1]));
           }
+          tmem_st16(tSb + lane_off + 16 * cb, pk);
+          tmem_st16(tSb + lane_off + 16 * cb + 16, pk2);
         }
         if (*abortp) break;
         tmem_st_wait();
@@ -552,7 +563,6 @@ __global__ void __launch_bounds__(448)
           }
         }
       }
-      fence_async_smem();
       tc_fence_before();
       mbar_arrive(&s_ready);
     }
