@@ -60,11 +60,18 @@ def shape_of(w, n_docs=None):
                     initial_state=w.initial_state, final_state=w.final_state, dht=w.final_state, chunk=w.chunk)
 
 
-def aggregate(step_ms_per_rank, tokens_per_rank_step, steps):
-    """Whole-job throughput: the slowest rank's time, the tokens of all ranks."""
-    t = max(step_ms_per_rank)
-    n = len(step_ms_per_rank)
-    return t, n * tokens_per_rank_step / (t / 1e3), steps
+def job_throughput(ms_local, tokens_per_rank_step, world, device=None):
+    """Whole-job throughput: the slowest rank's step time (max over the
+    ranks of the current process group) and the tokens of all ranks."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_per_rank_step / (ms / 1e3)
 
 
 # ---------------------------------------------------------------- clocks ----
@@ -262,14 +269,7 @@ def run_glacore(args, w):
         bwd_ms.append(fprev.elapsed_time(prev))
         launches += len(tfs[i].labels) + len(tbs[i].labels)
 
-    if world > 1:
-        t = torch.tensor([ms_local], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    else:
-        ms = ms_local
-    tokens = w.B * w.T
-    value = world * tokens / (ms / 1e3)
+    ms, value = job_throughput(ms_local, w.B * w.T, world, dev)
 
     peaks, peak_kind = load_peaks()
     shp = shape_of(w)
@@ -364,15 +364,12 @@ def run_e2e(args, w, d, x, scale, outs, fws, bws, dev, world):
     for i in range(K):
         one(i)
     torch.cuda.synchronize()
-    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, value = job_throughput(statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)), w.B * w.T,
+                               world, dev)
     h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in names_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    return {"value": world * w.B * w.T / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K}
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": K}
 
 
 def kernel_source_sha():
