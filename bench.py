@@ -383,6 +383,44 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
+# ncu kernel names -> the library's launch labels (template argument: mode)
+NCU_LABELS = (("gla_fwd_kernel<0>", "gla_fwd_kernel"), ("gla_fwd_kernel<1>", "gla_fwd_piece_state_kernel"),
+              ("gla_bwd_rev_kernel<0>", "gla_bwd_rev_kernel"), ("gla_bwd_rev_kernel<1>", "gla_bwd_piece_dh_kernel"),
+              ("gla_bwd_dq_kernel", "gla_bwd_dq_kernel"))
+
+
+def ingest_traffic(csv_path):
+    """Writes profiles/traffic.json (DRAM bytes per launch, per kernel label)
+    from an ncu --csv capture with dram__bytes_read.sum / dram__bytes_write.sum,
+    stamped with the hash of the kernel sources it was taken on."""
+    import csv
+
+    rows = list(csv.reader(l for l in open(csv_path) if l.startswith('"')))
+    hdr, data = rows[0], rows[1:]
+    ix = {k: hdr.index(k) for k in ("Kernel Name", "Metric Name", "Metric Value", "ID", "Metric Unit")}
+    scale_of = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1024.0, "MB": 1024.0 ** 2,
+                "GB": 1024.0 ** 3}
+    per = {}
+    for r in data:
+        name = r[ix["Kernel Name"]].replace("(bool)", "").replace(" ", "")
+        lab = next((l for key, l in NCU_LABELS if key in name), None)
+        if lab is None or r[ix["Metric Name"]] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        val = float(r[ix["Metric Value"]].replace(",", "")) * scale_of.get(r[ix["Metric Unit"]], 1.0)
+        per.setdefault(lab, {}).setdefault(r[ix["ID"]], 0.0)
+        per[lab][r[ix["ID"]]] += val
+    out = {}
+    for lab, launches in per.items():
+        vals = list(launches.values())
+        out[lab] = {"dram_bytes_per_launch": statistics.mean(vals), "launches": len(vals),
+                    "source_sha": kernel_source_sha()}
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1, sort_keys=True)
+    print(json.dumps(out))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -391,7 +429,11 @@ def main(argv=None):
     ap.add_argument("--impl", default="glacore", choices=["glacore", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ingest-traffic", metavar="NCU_CSV",
+                    help="write profiles/traffic.json from an ncu DRAM-bytes capture and exit")
     args = ap.parse_args(argv)
+    if args.ingest_traffic:
+        return ingest_traffic(args.ingest_traffic)
     if args.warmup < 3:
         args.warmup = 3
     from chunked_gated_linear_chunk_gb300 import inputs
