@@ -385,7 +385,7 @@ def kernel_source_sha():
 
 # ncu kernel names -> the library's launch labels (template argument: mode)
 NCU_LABELS = (("gla_fwd_kernel<0>", "gla_fwd_kernel"), ("gla_fwd_kernel<1>", "gla_fwd_piece_state_kernel"),
-              ("gla_bwd_rev_kernel<0>", "gla_bwd_rev_kernel"), ("gla_bwd_rev_kernel<1>", "gla_bwd_piece_dh_kernel"),
+              ("gla_bwd_rev_kernel<0>", "gla_bwd_rev_kernel"), ("gla_piece_pass_kernel", "gla_piece_pass_kernel"),
               ("gla_bwd_dq_kernel", "gla_bwd_dq_kernel"))
 
 

@@ -29,7 +29,7 @@
 // TMEM lane), warps 10..13 epilogue.
 #include <string.h>
 
-#include "tc_common.cuh"
+#include "tc_gla_fwd.cuh"
 
 namespace glacore {
 namespace tc {
@@ -623,8 +623,7 @@ constexpr uint32_t BYTES = 218112;
 // dk / dg / dv epilogue of chunk i-1, written over kt, v and the partials.
 // Warps 10..13 mask P and dP and scale the state gradient.
 template <bool DH_ONLY>
-__global__ void __launch_bounds__(448)
-    gla_bwd_rev_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+__device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdArgs &a, unsigned bx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[bsm::NS], empty[bsm::NS], kfull[bsm::NS], kempty[bsm::NS],
@@ -635,7 +634,7 @@ __global__ void __launch_bounds__(448)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int64_t u = blockIdx.x;
+  const int64_t u = bx;
   const int64_t H = a.H;
   const Unit un = a.units.get(u);
   const int64_t d = un.doc;
@@ -1130,8 +1129,25 @@ __global__ void __launch_bounds__(448)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-cudaError_t fwd_piece_states(const Prob &pr, const Units &units, int64_t max_units, float *Lb,
-                             float *Db, cudaStream_t st);
+template <bool DH_ONLY>
+__global__ void __launch_bounds__(448)
+    gla_bwd_rev_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  gla_bwd_rev_body<DH_ONLY>(maps, a, blockIdx.x);
+}
+
+// The two piece passes of the exact sequence split in one launch (they are
+// independent): CTAs x < nrev run the reverse dH-only pass (local state
+// gradient at the start of every piece but the first; the longer CTAs, so
+// they are dispatched first), the rest the forward's state-only pass (local
+// end state and decay of every piece but the last of a document).
+__global__ void __launch_bounds__(448)
+    gla_piece_pass_kernel(const __grid_constant__ FwdMaps fm, const FwdArgs fa,
+                          const __grid_constant__ BwdMaps bm, const BwdArgs ba, unsigned nrev) {
+  if (blockIdx.x < nrev)
+    gla_bwd_rev_body<true>(bm, ba, blockIdx.x);
+  else
+    gla_fwd_body<true>(fm, fa, blockIdx.x - nrev);
+}
 
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,
                 const float *dht, void *dq, void *dk, void *dv, float *dg, float *dh0, char *ws,
@@ -1173,8 +1189,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   const int smA = asm_::BYTES + 1024, smB = bsm::BYTES + 1024;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gla_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smA)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gla_bwd_rev_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gla_bwd_rev_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
+      (e = cudaFuncSetAttribute(gla_bwd_rev_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
     return e;
   if (Lo.pieces) {
     if (Lo.table &&
@@ -1185,12 +1200,28 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     a.lr = (float *)(ws + Lo.off_Lr);
     a.dr = (float *)(ws + Lo.off_Dr);
     // local end states of the pieces (forward) and local state gradients at
-    // their starts (reverse); the consumers fold them
-    if ((e = fwd_piece_states(pr, a.units, Lo.max_units, (float *)(ws + Lo.off_L), (float *)(ws + Lo.off_D),
-                              st)) != cudaSuccess)
+    // their starts (reverse), in one launch; the consumers fold them
+    FwdMaps fm;
+    if (!make_map(&fm.q, pr.q, true, KD, pr.Hqk, BT, 64) || !make_map(&fm.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
+        !make_map(&fm.v, pr.v, true, VD, pr.H, BT, 64) || !make_map(&fm.g, pr.g, false, KD, pr.H, BT, 32))
+      return cudaErrorInvalidValue;
+    FwdArgs fa;
+    memset(&fa, 0, sizeof(fa));
+    fa.units = a.units;
+    fa.H = pr.H;
+    fa.scale = pr.scale;
+    fa.g = pr.g;
+    fa.lbuf = (float *)(ws + Lo.off_L);
+    fa.dbuf = (float *)(ws + Lo.off_D);
+    fa.err = pr.err;
+    const int smP = (fsm::BYTES > bsm::BYTES ? fsm::BYTES : bsm::BYTES) + 1024;
+    if ((e = cudaFuncSetAttribute(gla_piece_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smP)) !=
+        cudaSuccess)
       return e;
-    gla_bwd_rev_kernel<true><<<grid, 448, smB, st>>>(maps, a);
-    mark_launch("gla_bwd_piece_dh_kernel", st);
+    const unsigned nrev = (unsigned)Lo.max_units;
+    gla_piece_pass_kernel<<<dim3(nrev + (unsigned)(2 * Lo.max_units), (unsigned)pr.H), 448, smP, st>>>(fm, fa, maps,
+                                                                                                        a, nrev);
+    mark_launch("gla_piece_pass_kernel", st);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   gla_bwd_dq_kernel<<<grid, 448, smA, st>>>(maps, a);

@@ -1,0 +1,492 @@
+// tc_gla_fwd.cuh -- the forward kernel body of the tcgen05 path for GLA with bf16 inputs,
+// K = V = 128, chunk C = 64.
+//
+// Chunk formulas (FLAT blog, trainstation-project.github.io/blog/flat:
+// "Linear Attention / Forward Recurrence" for the chunkwise form, "Gated
+// Linear Attention" for the decay ratios as exponentiated chunk-local
+// prefix sums of the log gate, "Backward Recurrence" / "Backward Kernels"
+// for the reverse chunk walk and the gate gradient as a suffix sum):
+//
+//   G   = inclusive prefix sum of g over the chunk (per key channel, fp32)
+//   qt  = scale q exp(G)      kt = k exp(-G)       Gam = G at the chunk end
+//   P   = (qt kt^T) masked to s <= t
+//   O   = qt S + P V          S <- diag(exp(Gam)) (S + kt^T V)
+//
+// The fp32 state S never leaves the SM between chunks (FLAT's "keep the
+// state on-chip"; FLA instead writes every chunk state to HBM).  All
+// matrix products run on tcgen05 (bf16 operands from shared memory,
+// fp32 accumulators in TMEM); q/k/v/g tiles arrive by TMA.
+//
+// Thread roles in every kernel: warp 0 issues TMA loads (one lane), warp 1
+// owns TMEM and issues tcgen05.mma (one lane), warps 2..5 are the compute
+// warpgroup.  Compute thread i of the warpgroup owns key channel (or value
+// column) c = 32 * (warp % 4) + lane, which is also the TMEM lane it may
+// read: M = 128 accumulators are laid out one row per lane, so products
+// whose rows are channels (state update, transposed gradients) land in the
+// thread that owns that channel.  M = 64 accumulators (the C x C matrices,
+// the output tile) put row r in lane 32 * (r / 16) + r % 16.
+#pragma once
+
+#include "tc_common.cuh"
+
+namespace glacore {
+namespace tc {
+
+// =========================================================================
+// Forward: grid (2 * n_docs, H), 448 threads (x = 2 * doc + value half).
+// One CTA owns one document, one head and 64 value columns and walks the
+// document's chunks in order.
+//   warp 0      TMA producer (3-stage ring of q, k, v tiles; L2 prefetch of
+//               gates and of the tiles two chunks ahead)
+//   warp 1      TMEM owner and MMA issuer
+//   warps 2..9  prep: gates straight from L2, prefix/suffix products,
+//               scaled q / k in place
+//   warps 10..13 epilogue: causal mask of P, state update S (fp32, in
+//               registers, thread c holds row c), output stores
+// TMEM (512 columns): P[2] at 0/64, U[2] at 128/192, O[2] at 256/320.
+// =========================================================================
+struct FwdMaps {
+  CUtensorMap q, k, v, g;
+};
+struct FwdArgs {
+  Units units;
+  int64_t H;
+  float scale;
+  const float *g;
+  const float *h0;    // [n_docs,H,K,V] state entering the document, or null
+  float *ht;          // [n_docs,H,K,V] final state (written by the last piece)
+  float *lbuf;        // [units,H,K,V] piece end state from zero (state-only mode writes it)
+  float *dbuf;        // [units,H,K] exp(sum of g over the piece) (state-only mode writes it)
+  __nv_bfloat16 *o;
+  int *err;
+};
+
+namespace fsm {  // shared-memory carve-up of the forward kernel (bytes)
+constexpr int NS = 3;             // q/k/v pipeline stages
+constexpr uint32_t Q = 0;         // 3 x 16 KB: q, then qt in place
+constexpr uint32_t K = 49152;     // 3 x 16 KB: k, then kt in place
+constexpr uint32_t V = 98304;     // 3 x 8 KB (64 value columns)
+constexpr uint32_t P = 122880;    // 2 x 8 KB: masked P (bf16, K-major A)
+constexpr uint32_t S = 139264;    // 2 x 16 KB: S (bf16, rows = key channel)
+constexpr uint32_t GAM = 172032;  // 4 x 128 fp32: exp(chunk gate total)
+constexpr uint32_t XCH = 174080;  // 2 x 4 x 128 fp32: quarter-chunk gate products
+constexpr uint32_t BYTES = 178176;
+}  // namespace fsm
+
+// Shared-memory addresses of the 16 rows t0 .. t0+15 (t0 % 8 == 0) of one
+// 4-byte column pair (c, c+1) of a bf16 128-byte-swizzled tile with 64-row
+// column blocks: the XOR pattern depends only on (row % 8), so eight bases
+// cover all rows and the row offset folds into the instruction immediate.
+struct Rows16 {
+  uint32_t a[8];
+  __device__ __forceinline__ Rows16(const uint8_t *tile, int t0, int c) {
+    const uint32_t base = smem_u32(tile) + (uint32_t)(c >> 6) * 8192u + (uint32_t)t0 * 128u +
+                          (uint32_t)(c & 7) * 2u;
+    const uint32_t cch = (uint32_t)(c & 63) >> 3;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = base + ((cch ^ (uint32_t)k) << 4);
+  }
+};
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Prep of one chunk by the 256 prep threads: thread (warp pw in 0..7, lane)
+// owns key channels c0, c0+1 (c0 = 64 * (pw & 1) + 2 * lane) and tokens
+// t0 = 16 * (pw >> 1) .. +15.  `gv` holds its gate values (already loaded).
+// exp(G_t) is the prefix product of exp(g) and exp(Gam - G_t) the suffix
+// product, so each element costs one exponential:
+//   qt = scale q exp(G),  kt = k exp(-Gam) exp(Gam - G).
+// The four token quarters exchange their partial products through `xch`.
+// Rows t >= L (past the document end) are zeroed.  Writes exp(Gam) of its
+// channels to gam (quarter-0 warps).
+__device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[16], float *gam,
+                                           float *xch, int pw, int lane, int L, float scale,
+                                           bool with_q) {
+  const int tq = pw >> 1;
+  const int c0 = 64 * (pw & 1) + 2 * lane;
+  const int t0 = 16 * tq;
+  float p0 = 1.f, p1 = 1.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const bool ok = t0 + i < L;
+    x[i].x = ok ? __expf(x[i].x) : 1.f;
+    x[i].y = ok ? __expf(x[i].y) : 1.f;
+    p0 *= x[i].x;
+    p1 *= x[i].y;
+  }
+  xch[tq * 128 + c0] = p0;
+  xch[tq * 128 + c0 + 1] = p1;
+  named_bar(1, 256);
+  float pre0 = 1.f, pre1 = 1.f, suf0 = 1.f, suf1 = 1.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float e0 = xch[u * 128 + c0], e1 = xch[u * 128 + c0 + 1];
+    if (u < tq) {
+      pre0 *= e0;
+      pre1 *= e1;
+    } else if (u > tq) {
+      suf0 *= e0;
+      suf1 *= e1;
+    }
+  }
+  const float T0 = pre0 * p0 * suf0, T1 = pre1 * p1 * suf1;  // exp(Gam)
+  const float i0 = __frcp_rn(T0), i1 = __frcp_rn(T1);
+  const Rows16 rq(q, t0, c0), rk(k, t0, c0);
+  uint32_t v[16];
+  if (with_q) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = lds_u32(rq.a[i & 7] + i * 128);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      pre0 *= x[i].x;
+      pre1 *= x[i].y;
+      const __nv_bfloat162 qq = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
+      v[i] = (t0 + i < L) ? pack_bf16(scale * __low2float(qq) * pre0, scale * __high2float(qq) * pre1) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sts_u32(rq.a[i & 7] + i * 128, v[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = lds_u32(rk.a[i & 7] + i * 128);
+#pragma unroll
+  for (int i = 15; i >= 0; --i) {
+    const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
+    v[i] = (t0 + i < L) ? pack_bf16(__low2float(kk) * suf0 * i0, __high2float(kk) * suf1 * i1) : 0u;
+    suf0 *= x[i].x;
+    suf1 *= x[i].y;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) sts_u32(rk.a[i & 7] + i * 128, v[i]);
+  if (tq == 0) {
+    gam[c0] = T0;
+    gam[c0 + 1] = T1;
+  }
+}
+
+__device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float (&S)[64]) {
+#pragma unroll
+  for (int n = 0; n < 64; n += 8)
+    st_shared_v4(smem_u32(St + sw128_off(c, n, 128)), pack_bf16(S[n], S[n + 1]),
+                 pack_bf16(S[n + 2], S[n + 3]), pack_bf16(S[n + 4], S[n + 5]),
+                 pack_bf16(S[n + 6], S[n + 7]));
+}
+
+// STATE_ONLY: the piece pass of the exact sequence split -- only the state
+// recurrence from a zero state (no q, no output); writes the piece's end
+// state and its total decay.  Pieces that end their document have nothing
+// to contribute and exit.
+template <bool STATE_ONLY>
+__device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs &a, unsigned bx) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[fsm::NS], empty[fsm::NS], prep_done[fsm::NS], p_full[2], u_full[2],
+      o_full[2], p_ready[2], s_ready[2], gam_ready[4];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int vb = bx & 1, h = blockIdx.y;
+  const int64_t u = bx >> 1;
+  const Unit un = a.units.get(u);
+  const int64_t d = un.doc;
+  const int64_t s0 = un.start, s1 = un.end;
+  const bool last_piece = un.piece == un.npieces - 1;
+  const int nch = (STATE_ONLY && last_piece) ? 0 : (int)((s1 - s0 + C - 1) / C);
+
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < fsm::NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&prep_done[i], 256);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&u_full[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&p_ready[i], 128);
+      mbar_init(&s_ready[i], 128);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 256);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  const uint32_t sbase = smem_u32(sm);
+  volatile int *abortp = &abort_flag;
+#define FAIL_AND_BREAK        \
+  {                           \
+    atomicExch(&abort_flag, 1); \
+    break;                    \
+  }
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.g);
+      for (int j = 0; j < nch; ++j) {
+        const int s = j % fsm::NS;
+        if (j >= fsm::NS && !mbar_wait(&empty[s], ((j / fsm::NS) - 1) & 1, WAIT_CYCLES))
+          FAIL_AND_BREAK
+        if (*abortp) break;
+        const int tok = (int)(s0 + (int64_t)j * C);
+        for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
+          // gates for the prep warps (read from L2); q/k/v ahead of the ring
+          const int tp = (int)(s0 + (int64_t)jp * C);
+          for (int x = 0; x < KD; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
+          if (jp >= fsm::NS) {
+            if (!STATE_ONLY) {
+              tma_prefetch_3d(&maps.q, 0, h, tp);
+              tma_prefetch_3d(&maps.q, 64, h, tp);
+            }
+            tma_prefetch_3d(&maps.k, 0, h, tp);
+            tma_prefetch_3d(&maps.k, 64, h, tp);
+            tma_prefetch_3d(&maps.v, vb * 64, h, tp);
+          }
+        }
+        mbar_expect_tx(&full[s], (STATE_ONLY ? 16384 : 2 * 16384) + 8192);
+        uint8_t *q = sm + fsm::Q + s * 16384, *k = sm + fsm::K + s * 16384;
+        if (!STATE_ONLY) {
+          tma_load_3d(q, &maps.q, 0, h, tok, &full[s]);
+          tma_load_3d(q + 8192, &maps.q, 64, h, tok, &full[s]);
+        }
+        tma_load_3d(k, &maps.k, 0, h, tok, &full[s]);
+        tma_load_3d(k + 8192, &maps.k, 64, h, tok, &full[s]);
+        tma_load_3d(sm + fsm::V + s * 8192, &maps.v, vb * 64, h, tok, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idP = idesc_bf16(64, 64, false, false);
+      constexpr uint32_t idO = idesc_bf16(64, 64, false, true);
+      constexpr uint32_t idU = idesc_bf16(128, 64, true, true);
+      uint32_t ph_prep = 0, ph_pr = 0, ph_sr = 0;  // one parity bit per buffer
+      for (int j = 0; j < nch; ++j) {
+        const int b = j & 1, st = j % fsm::NS;
+        const uint32_t qa = sbase + fsm::Q + st * 16384, ka = sbase + fsm::K + st * 16384;
+        const uint32_t va = sbase + fsm::V + st * 8192;
+        const uint32_t Pa = sbase + fsm::P + b * 8192, Sa = sbase + fsm::S + (b ^ 1) * 16384;
+        const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
+        if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) {
+          FAIL_AND_BREAK
+        }
+        ph_prep ^= 1u << st;
+        if (STATE_ONLY) {
+          // U[b] is free once the epilogue has folded chunk j-2 into S
+          if (j >= 2) {
+            if (!mbar_wait(&s_ready[b], (ph_sr >> b) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
+            ph_sr ^= 1u << b;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) mma_bf16(tU, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, ks);
+          mma_commit(&u_full[b]);
+          mma_commit(&empty[st]);
+          continue;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(ka, ks, 64), idP, ks);
+        mma_commit(&p_full[b]);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tU, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, ks);
+        mma_commit(&u_full[b]);
+        if (!mbar_wait(&p_ready[b], (ph_pr >> b) & 1, WAIT_CYCLES) ||
+            !mbar_wait(&s_ready[b ^ 1], (ph_sr >> (b ^ 1)) & 1, WAIT_CYCLES)) {
+          FAIL_AND_BREAK
+        }
+        ph_pr ^= 1u << b;
+        ph_sr ^= 1u << (b ^ 1);
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(qa, ks, 64), mdesc(Sa, ks, 16384), idO, ks);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tO, kdesc(Pa, ks, 64), mdesc(va, ks, 8192), idO, 1);
+        mma_commit(&o_full[b]);
+        mma_commit(&empty[st]);
+      }
+    }
+  } else if (warp < 10) {
+    // ---------------- prep warps (8) ----------------
+    const int pw = warp - 2;
+    const int c0 = 64 * (pw & 1) + 2 * lane, t0 = 16 * (pw >> 1);
+    uint32_t ph_full = 0;
+    // gates of chunk j+1 are loaded into registers while chunk j is prepared
+    float2 xn[16];
+    auto load_x = [&](int jj, float2 (&x)[16]) {
+      const int64_t tk = s0 + (int64_t)jj * C;
+      const int LL = (int)min((int64_t)C, s1 - tk);
+      const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        x[i] = (t0 + i < LL) ? __ldg(reinterpret_cast<const float2 *>(gp + (int64_t)i * a.H * KD))
+                             : make_float2(0.f, 0.f);
+    };
+    if (nch > 0) load_x(0, xn);
+    for (int j = 0; j < nch; ++j) {
+      const int s = j % fsm::NS;
+      const int64_t tok0 = s0 + (int64_t)j * C;
+      const int L = (int)min((int64_t)C, s1 - tok0);
+      float2 x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = xn[i];
+      if (j + 1 < nch) load_x(j + 1, xn);
+      if (!mbar_wait(&full[s], (ph_full >> s) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
+      ph_full ^= 1u << s;
+      prep_chunk(sm + fsm::Q + s * 16384, sm + fsm::K + s * 16384, x,
+                 reinterpret_cast<float *>(sm + fsm::GAM) + (j & 3) * 128,
+                 reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 512, pw, lane, L, a.scale,
+                 !STATE_ONLY);
+      fence_async_smem();
+      mbar_arrive(&prep_done[s]);
+      mbar_arrive(&gam_ready[j & 3]);
+    }
+  } else {
+    // ---------------- epilogue warpgroup ----------------
+    const int qw = warp & 3;
+    const int c = qw * 32 + lane;       // key channel = TMEM lane of M = 128 tiles
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const int prow = qw * 16 + lane;    // row of M = 64 tiles (lanes < 16)
+    const int64_t H = a.H;
+    const int v0 = vb * 64;
+    float S[64];
+    if (STATE_ONLY) {
+#pragma unroll
+      for (int n = 0; n < 64; ++n) S[n] = 0.f;
+    } else {
+      // state entering the unit: h0 folded over the document's earlier pieces
+      const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
+      piece_state_in<64>(S, h0row, a.lbuf, a.dbuf, u - un.piece, un.piece, H, h, c, v0);
+    }
+    float decay = 1.f;  // state-only mode: exp(sum of g over the piece)
+    if (!STATE_ONLY) {
+      store_state_bf16(sm + fsm::S + 16384, c, S);
+      fence_async_smem();
+      mbar_arrive(&s_ready[1]);
+    }
+    uint32_t ph_p = 0, ph_u = 0, ph_o = 0;
+    for (int j = 0; j < nch; ++j) {
+      const int b = j & 1;
+      const int64_t tok0 = s0 + (int64_t)j * C;
+      const int L = (int)min((int64_t)C, s1 - tok0);
+      const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
+      // S2: P -> causal mask -> bf16 A operand of the intra-chunk product
+      if (!STATE_ONLY) {
+      if (!mbar_wait(&p_full[b], (ph_p >> b) & 1, WAIT_CYCLES)) {
+        FAIL_AND_BREAK
+      }
+      ph_p ^= 1u << b;
+      tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[16];
+        tmem_ld16(tP + lane_off + cb * 16, r);
+        tmem_ld_wait(r);
+        if (lane < 16) {
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = (cb * 16 + i <= prow) ? __uint_as_float(r[i]) : 0.f;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+            st_shared_v4(smem_u32(sm + fsm::P + b * 8192 + sw128_off(prow, cb * 16 + hb * 8, 64)),
+                         pack_bf16(x[hb * 8 + 0], x[hb * 8 + 1]),
+                         pack_bf16(x[hb * 8 + 2], x[hb * 8 + 3]),
+                         pack_bf16(x[hb * 8 + 4], x[hb * 8 + 5]),
+                         pack_bf16(x[hb * 8 + 6], x[hb * 8 + 7]));
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_ready[b]);
+      }
+      // S3a: state update S <- exp(Gam) (S + kt^T V), bf16 copy for the next readout
+      if (!mbar_wait(&u_full[b], (ph_u >> b) & 1, WAIT_CYCLES) ||
+          !mbar_wait(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
+        FAIL_AND_BREAK
+      }
+      ph_u ^= 1u << b;
+      tc_fence_after();
+      const float eG = reinterpret_cast<const float *>(sm + fsm::GAM)[(j & 3) * 128 + c];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[16];
+        tmem_ld16(tU + lane_off + cb * 16, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) S[cb * 16 + i] = eG * (S[cb * 16 + i] + __uint_as_float(r[i]));
+      }
+      if (STATE_ONLY) {
+        decay *= eG;
+        tc_fence_before();
+        mbar_arrive(&s_ready[b]);
+        continue;
+      }
+      store_state_bf16(sm + fsm::S + b * 16384, c, S);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s_ready[b]);
+      // S3b: output tile O = qt S_prev + P V
+      if (!mbar_wait(&o_full[b], (ph_o >> b) & 1, WAIT_CYCLES)) {
+        FAIL_AND_BREAK
+      }
+      ph_o ^= 1u << b;
+      tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[16];
+        tmem_ld16(tO + lane_off + cb * 16, r);
+        tmem_ld_wait(r);
+        if (lane < 16 && prow < L) {
+          __nv_bfloat16 *dst = a.o + ((tok0 + prow) * H + h) * VD + v0 + cb * 16;
+          st_global_v4(dst, pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                       pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                       pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                       pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7])));
+          st_global_v4(dst + 8, pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                       pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                       pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                       pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15])));
+        }
+      }
+      tc_fence_before();
+    }
+    float *dst = nullptr;
+    if (STATE_ONLY && nch > 0) {
+      dst = a.lbuf + ((u * H + h) * KD + c) * VD + v0;
+      if (vb == 0) a.dbuf[(u * H + h) * KD + c] = decay;
+    } else if (!STATE_ONLY && a.ht && last_piece) {
+      dst = a.ht + ((d * H + h) * KD + c) * VD + v0;
+    }
+    if (dst && !*abortp) {
+#pragma unroll
+      for (int n = 0; n < 64; n += 4)
+        *reinterpret_cast<float4 *>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abortp && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_TIMEOUT);
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// STATE_ONLY body is also launched by the backward's combined piece pass
+// (tc_gla_bwd.cu), so the kernel body lives in this header.
+
+}  // namespace tc
+}  // namespace glacore
