@@ -145,14 +145,17 @@ class ClockSampler:
 
 # ----------------------------------------------------------- CPU oracle ----
 def oracle_sample(d, rows, threads=None):
-    """Times the oracle fwd+bwd on batch rows `rows` (all heads); returns seconds."""
+    """Times the oracle fwd+bwd on batch rows `rows` (all heads); returns
+    seconds.  Workloads with documents or states run whole (rows = all)."""
     import oracle
 
-    sl = lambda t: None if t is None else t[rows[0]:rows[-1] + 1]
+    whole = d["segment_ids"] is not None or d["h0"] is not None or d["dht"] is not None
+    sl = (lambda t: t) if whole else (lambda t: None if t is None else t[rows[0]:rows[-1] + 1])
     t0 = time.perf_counter()
-    oracle.fwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), d["scale"], None, None, threads=threads)
-    oracle.bwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), sl(d["do"]), d["scale"], None, None, None,
+    oracle.fwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), d["scale"], sl(d["segment_ids"]), d["h0"],
                threads=threads)
+    oracle.bwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), sl(d["do"]), d["scale"], sl(d["segment_ids"]),
+               d["h0"], d["dht"], threads=threads)
     return time.perf_counter() - t0
 
 
@@ -204,21 +207,35 @@ def run_glacore(args, w):
     glc.load()
     d = inputs.make(w)
     x = inputs.to_device(d, dev)
-    scale = d["scale"]
+    scale, n_seqs = d["scale"], d["n_seqs"]
+    fwd_fn = glc.gla_fwd if w.kind == "gla" else glc.ssd_fwd
+    bwd_fn = glc.gla_bwd if w.kind == "gla" else glc.ssd_bwd
     o = torch.empty_like(x["v"])
     dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
     dg = torch.empty_like(x["g"])
+    st_shape = (n_seqs, w.H, w.K, w.V)
+    ht = torch.empty(st_shape, dtype=torch.float32, device=dev) if w.final_state else None
+    dh0 = torch.empty(st_shape, dtype=torch.float32, device=dev) if x["h0"] is not None else None
     # size the workspaces through the ABI
-    p, _ = glc._problem(x["q"], x["k"], x["v"], x["g"], scale, None, None, 64, None, False)
-    nf, nb = glc.workspace_size(p, "gla_fwd"), glc.workspace_size(p, "gla_bwd")
+    p, _ = glc._problem(x["q"], x["k"], x["v"], x["g"], scale, x["segment_ids"], x["h0"], w.chunk, n_seqs,
+                        w.kind == "ssd")
+    nf, nb = glc.workspace_size(p, w.kind + "_fwd"), glc.workspace_size(p, w.kind + "_bwd")
     fws = torch.empty(max(nf, 256), dtype=torch.uint8, device=dev)
     bws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
 
+    def fwd_call():
+        fwd_fn(x["q"], x["k"], x["v"], x["g"], scale, x["segment_ids"], x["h0"], w.final_state, w.chunk, n_seqs,
+               out=o, final_out=ht, workspace=fws)
+
+    def bwd_call():
+        bwd_fn(x["q"], x["k"], x["v"], x["g"], x["do"], scale, x["segment_ids"], x["h0"], x["dht"], w.chunk,
+               n_seqs, outs=(dq, dk, dv, dg, dh0), workspace=bws)
+
     def step():
-        glc.gla_fwd(x["q"], x["k"], x["v"], x["g"], scale, out=o, workspace=fws)
-        glc.gla_bwd(x["q"], x["k"], x["v"], x["g"], x["do"], scale, outs=(dq, dk, dv, dg, None), workspace=bws)
+        fwd_call()
+        bwd_call()
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -229,8 +246,8 @@ def run_glacore(args, w):
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    tfs = [glc.LaunchTimer(8) for _ in range(K)]
-    tbs = [glc.LaunchTimer(12) for _ in range(K)]
+    tfs = [glc.LaunchTimer(16) for _ in range(K)]
+    tbs = [glc.LaunchTimer(16) for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -239,10 +256,9 @@ def run_glacore(args, w):
             flush.fill_(i & 0xFF)
             starts[i].record()
             with tfs[i]:
-                glc.gla_fwd(x["q"], x["k"], x["v"], x["g"], scale, out=o, workspace=fws)
+                fwd_call()
             with tbs[i]:
-                glc.gla_bwd(x["q"], x["k"], x["v"], x["g"], x["do"], scale, outs=(dq, dk, dv, dg, None),
-                            workspace=bws)
+                bwd_call()
             ends[i].record()
         torch.cuda.synchronize()
     if world > 1:
@@ -272,7 +288,7 @@ def run_glacore(args, w):
     ms, value = job_throughput(ms_local, w.B * w.T, world, dev)
 
     peaks, peak_kind = load_peaks()
-    shp = shape_of(w)
+    shp = shape_of(w, n_seqs)
     flops = rf.fwd_flops(shp) + rf.bwd_flops(shp)
     nbytes = rf.fwd_bytes(shp) + rf.bwd_bytes(shp)
     t_roof = rf.roofline_time_s(flops, nbytes, peaks["bf16_tflops"], peaks["hbm_gbs"])
@@ -293,7 +309,8 @@ def run_glacore(args, w):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, d, x, scale, (o, dq, dk, dv, dg), fws, bws, dev, world)
+        e2e = run_e2e(args, w, d, x, [t for t in (o, ht, dq, dk, dv, dg, dh0) if t is not None], fwd_call,
+                      bwd_call, dev, world)
 
     if rank != 0:
         if world > 1:
@@ -306,11 +323,12 @@ def run_glacore(args, w):
         secs = oracle_sample(d, rows, threads)
         cpu = {"value": len(rows) * w.T / secs, "unit": UNIT, "cores": min(threads, len(rows) * w.H),
                "kind": "oracle",
-               "sample": f"fp64 token-by-token oracle fwd+bwd over the whole batch ({w.B}x{w.T} tokens, "
+               "sample": f"fp64 token-by-token oracle fwd+bwd over the whole workload ({w.B}x{w.T} tokens, "
                          f"{w.H} heads), {secs:.1f} s"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": w.chunk,
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}"},
@@ -333,15 +351,12 @@ def run_glacore(args, w):
     return 0
 
 
-def run_e2e(args, w, d, x, scale, outs, fws, bws, dev, world):
+def run_e2e(args, w, d, x, outs, fwd_call, bwd_call, dev, world):
     import torch
 
-    import chunked_gated_linear_chunk_gb300 as glc
-
-    names_in = ("q", "k", "v", "g", "do")
+    names_in = [n for n in ("q", "k", "v", "g", "do", "segment_ids", "h0", "dht") if d.get(n) is not None]
     host_in = {n: d[n].pin_memory() for n in names_in}
     host_out = [t.detach().to("cpu").pin_memory() for t in outs]
-    o, dq, dk, dv, dg = outs
     K = max(3, min(args.steps, 50))
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -351,8 +366,8 @@ def run_e2e(args, w, d, x, scale, outs, fws, bws, dev, world):
             starts[i].record()
         for n in names_in:
             x[n].copy_(host_in[n], non_blocking=True)
-        glc.gla_fwd(x["q"], x["k"], x["v"], x["g"], scale, out=o, workspace=fws)
-        glc.gla_bwd(x["q"], x["k"], x["v"], x["g"], x["do"], scale, outs=(dq, dk, dv, dg, None), workspace=bws)
+        fwd_call()
+        bwd_call()
         for hdst, dsrc in zip(host_out, outs):
             hdst.copy_(dsrc, non_blocking=True)
         if i is not None:
@@ -429,6 +444,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="glacore", choices=["glacore", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX, choices=[1, 2, 3, 4, 5],
+                    help="synthetic workload (default 2: GLA B4 H16 T2048 d128 bf16, the headline)")
     ap.add_argument("--ingest-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.json from an ncu DRAM-bytes capture and exit")
     args = ap.parse_args(argv)
@@ -438,7 +455,7 @@ def main(argv=None):
         args.warmup = 3
     from chunked_gated_linear_chunk_gb300 import inputs
 
-    w = inputs.WORKLOADS[WORKLOAD_INDEX]
+    w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
     return run_glacore(args, w)

@@ -104,9 +104,13 @@ namespace {
 
 struct Layout {
   bool tc;             // tensor-core path
+  bool ssdx;           // SSD through the GLA tensor-core kernels (expanded problem in the workspace)
   int chunk;           // chunk length of the state workspace / doc table
   size_t off_start, off_cbase;  // doc tables (segments only)
   size_t off_states, off_final, off_acc_q, off_acc_k, off_tc;
+  // ssdx: the GLA problem's tensors ([B*T, H, 128]) and states ([n, H, 128, 128])
+  size_t off_xq, off_xk, off_xv, off_xg, off_xh0, off_xo, off_xht, off_xdo, off_xdht, off_xdq, off_xdk,
+      off_xdv, off_xdg, off_xdh0;
   size_t total;
 };
 
@@ -140,11 +144,27 @@ glacore_status check_problem(const glacore_problem *p, bool head_gate) {
 
 bool simt_supported(const glacore_problem *p) { return p->K <= 128 && p->V <= 128; }
 
+// The GLA problem an SSD problem is run as (ssd_gla.cu): every head its own
+// q / k, the gate on every key channel, V padded to 128.
+glacore_problem ssd_as_gla(const glacore_problem *p) {
+  glacore_problem e = *p;
+  e.Hqk = p->H;
+  e.K = 128;
+  e.V = 128;
+  return e;
+}
+bool ssdx_supported(const glacore_problem *p, bool head_gate, bool backward) {
+  if (!head_gate || p->dtype != GLACORE_BF16 || p->K != 128 || p->V > 128 || p->V % 8) return false;
+  const glacore_problem e = ssd_as_gla(p);
+  return tc::supported(&e, false, backward);
+}
+
 Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
   Layout L;
   memset(&L, 0, sizeof(L));
   L.tc = tc::supported(p, head_gate, backward);
-  L.chunk = L.tc ? tc::chunk_of(p) : simt::SC;
+  L.ssdx = !L.tc && ssdx_supported(p, head_gate, backward);
+  L.chunk = (L.tc || L.ssdx) ? tc::C : simt::SC;
   const int64_t BT = p->B * p->T, n = p->n_seqs;
   size_t off = 0;
   if (p->segment_ids) {
@@ -153,7 +173,34 @@ Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
     L.off_cbase = off;
     off = align256(off + sizeof(int64_t) * (n + 1));
   }
-  if (L.tc) {
+  if (L.ssdx) {
+    const size_t rows = (size_t)BT * p->H, bf = rows * 128 * 2, f32 = rows * 128 * 4;
+    const size_t st = (size_t)n * p->H * 128 * 128 * 4;
+    auto take = [&](size_t &o, size_t bytes) {
+      o = off;
+      off = align256(off + bytes);
+    };
+    take(L.off_xq, bf);
+    take(L.off_xk, bf);
+    take(L.off_xv, bf);
+    take(L.off_xg, f32);
+    if (p->initial_state) take(L.off_xh0, st);
+    if (!backward) {
+      take(L.off_xo, bf);
+      take(L.off_xht, st);
+    } else {
+      take(L.off_xdo, bf);
+      take(L.off_xdht, st);
+      take(L.off_xdq, bf);
+      take(L.off_xdk, bf);
+      take(L.off_xdv, bf);
+      take(L.off_xdg, f32);
+      if (p->initial_state) take(L.off_xdh0, st);
+    }
+    const glacore_problem e = ssd_as_gla(p);
+    L.off_tc = off;
+    off = align256(off + tc::workspace_bytes(&e, false, backward));
+  } else if (L.tc) {
     L.off_tc = off;
     off = align256(off + tc::workspace_bytes(p, head_gate, backward));
   } else if (backward) {
@@ -220,9 +267,9 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
   const int64_t BT = p->B * p->T;
   if (BT > 0 && !o) return GLACORE_ERR_INVALID_ARG;
   const Layout L = layout(p, head_gate, false);
-  if (!L.tc && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
+  if (!L.tc && !L.ssdx && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
   if ((s = check_ws(p, L))) return s;
-  if (L.tc && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
+  if ((L.tc || L.ssdx) && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
                 aligned16(o) && aligned16(ht) && aligned16(p->initial_state)))
     return GLACORE_ERR_INVALID_ARG;
   if (BT == 0) return GLACORE_OK;
@@ -234,6 +281,25 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
     if (e != cudaSuccess) return GLACORE_ERR_CUDA;
   }
   const Docs docs = make_docs(p, L, ws);
+  if (L.ssdx) {
+    const int64_t rows = BT * p->H, mats = p->n_seqs * p->H;
+    glacore_problem e = ssd_as_gla(p);
+    e.q = ws + L.off_xq;
+    e.k = ws + L.off_xk;
+    e.v = ws + L.off_xv;
+    e.g = (const float *)(ws + L.off_xg);
+    e.initial_state = p->initial_state ? (const float *)(ws + L.off_xh0) : nullptr;
+    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, nullptr, ws + L.off_xq,
+                                 ws + L.off_xk, ws + L.off_xv, (float *)(ws + L.off_xg), nullptr, st);
+    if (c == cudaSuccess && p->initial_state)
+      c = ssdx::pad_states(mats, p->V, p->initial_state, (float *)(ws + L.off_xh0), st);
+    if (c == cudaSuccess)
+      c = tc::fwd(make_prob(&e, false), docs, &e, ws + L.off_xo, ht ? (float *)(ws + L.off_xht) : nullptr,
+                  ws + L.off_tc, st);
+    if (c == cudaSuccess) c = ssdx::cut_rows(rows, p->V, ws + L.off_xo, o, st);
+    if (c == cudaSuccess && ht) c = ssdx::cut_states(mats, p->V, (const float *)(ws + L.off_xht), ht, st);
+    return cuda_status(c);
+  }
   const Prob pr = make_prob(p, head_gate);
   if (L.tc) return cuda_status(tc::fwd(pr, docs, p, o, ht, ws + L.off_tc, st));
   return cuda_status(simt::launch_fwd(pr, docs, p->dtype, o, ht, nullptr, st));
@@ -247,9 +313,9 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
   const int64_t BT = p->B * p->T;
   if (BT > 0 && (!dO || !dq || !dk || !dv || !dg)) return GLACORE_ERR_INVALID_ARG;
   const Layout L = layout(p, head_gate, true);
-  if (!L.tc && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
+  if (!L.tc && !L.ssdx && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
   if ((s = check_ws(p, L))) return s;
-  if (L.tc && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
+  if ((L.tc || L.ssdx) && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
                 aligned16(dO) && aligned16(dht) && aligned16(dq) && aligned16(dk) &&
                 aligned16(dv) && aligned16(dg) && aligned16(dh0) &&
                 aligned16(p->initial_state)))
@@ -263,6 +329,30 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
     if (e != cudaSuccess) return GLACORE_ERR_CUDA;
   }
   const Docs docs = make_docs(p, L, ws);
+  if (L.ssdx) {
+    const int64_t rows = BT * p->H, mats = p->n_seqs * p->H;
+    glacore_problem e = ssd_as_gla(p);
+    e.q = ws + L.off_xq;
+    e.k = ws + L.off_xk;
+    e.v = ws + L.off_xv;
+    e.g = (const float *)(ws + L.off_xg);
+    e.initial_state = p->initial_state ? (const float *)(ws + L.off_xh0) : nullptr;
+    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, dO, ws + L.off_xq, ws + L.off_xk,
+                                 ws + L.off_xv, (float *)(ws + L.off_xg), ws + L.off_xdo, st);
+    if (c == cudaSuccess && p->initial_state)
+      c = ssdx::pad_states(mats, p->V, p->initial_state, (float *)(ws + L.off_xh0), st);
+    if (c == cudaSuccess && dht) c = ssdx::pad_states(mats, p->V, dht, (float *)(ws + L.off_xdht), st);
+    if (c == cudaSuccess)
+      c = tc::bwd(make_prob(&e, false), docs, &e, ws + L.off_xdo, dht ? (const float *)(ws + L.off_xdht) : nullptr,
+                  ws + L.off_xdq, ws + L.off_xdk, ws + L.off_xdv, (float *)(ws + L.off_xdg),
+                  dh0 ? (float *)(ws + L.off_xdh0) : nullptr, ws + L.off_tc, st);
+    if (c == cudaSuccess) c = ssdx::reduce_heads(BT, p->H, p->Hqk, ws + L.off_xdq, dq, st);
+    if (c == cudaSuccess) c = ssdx::reduce_heads(BT, p->H, p->Hqk, ws + L.off_xdk, dk, st);
+    if (c == cudaSuccess) c = ssdx::cut_rows(rows, p->V, ws + L.off_xdv, dv, st);
+    if (c == cudaSuccess) c = ssdx::sum_channels(rows, (const float *)(ws + L.off_xdg), dg, st);
+    if (c == cudaSuccess && dh0) c = ssdx::cut_states(mats, p->V, (const float *)(ws + L.off_xdh0), dh0, st);
+    return cuda_status(c);
+  }
   const Prob pr = make_prob(p, head_gate);
   if (L.tc)
     return cuda_status(tc::bwd(pr, docs, p, dO, dht, dq, dk, dv, dg, dh0, ws + L.off_tc, st));
