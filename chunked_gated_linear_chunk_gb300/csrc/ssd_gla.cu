@@ -19,27 +19,29 @@ namespace ssdx {
 
 constexpr int KX = 128, VX = 128;
 
-// One warp per (token, head): 16-byte chunks.  Writes xq, xk (q, k of the
-// head's group), xv (v padded), xg (gate broadcast), xdo (do padded, or
-// skipped when null).
+// One warp per (token, head), 16-byte chunks (V % 8 == 0).  Writes xq, xk
+// (q, k of the head's group), xv (v padded), xg (gate broadcast) and xdo
+// (do padded; skipped when null).
 __global__ void expand_kernel(int64_t rows, int64_t H, int64_t Hqk, int64_t V, const uint4 *q, const uint4 *k,
-                              const uint16_t *v, const float *g, const uint16_t *dO, uint4 *xq, uint4 *xk,
-                              uint16_t *xv, float4 *xg, uint16_t *xdo) {
+                              const uint4 *v, const float *g, const uint4 *dO, uint4 *xq, uint4 *xk, uint4 *xv,
+                              float4 *xg, uint4 *xdo) {
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;  // = t * H + h
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int64_t t = row / H, h = row - t * H, hq = h / (H / Hqk);
   const int64_t src = (t * Hqk + hq) * (KX / 8);  // 16 chunks of 8 bf16 per row
-  if (lane < 16)
+  const int64_t nv = V / 8;                       // chunks of a v / do row
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  if (lane < 16) {
     xq[row * (KX / 8) + lane] = q[src + lane];
-  else
-    xk[row * (KX / 8) + lane - 16] = k[src + lane - 16];
+    xv[row * (VX / 8) + lane] = lane < nv ? v[row * nv + lane] : zero;
+  } else {
+    const int l = lane - 16;
+    xk[row * (KX / 8) + l] = k[src + l];
+    if (xdo) xdo[row * (VX / 8) + l] = l < nv ? dO[row * nv + l] : zero;
+  }
   const float gv = g[row];
   xg[row * (KX / 4) + lane] = make_float4(gv, gv, gv, gv);
-  for (int c = lane; c < VX; c += 32) {
-    xv[row * VX + c] = c < V ? v[row * V + c] : (uint16_t)0;
-    if (xdo) xdo[row * VX + c] = c < V ? dO[row * V + c] : (uint16_t)0;
-  }
 }
 
 // states [n*H, K, V] <-> [n*H, K, 128] (pad with zeros / cut)
@@ -55,12 +57,13 @@ __global__ void cut_state_kernel(int64_t mats, int64_t V, const float *src, floa
   const int64_t c = i % V, rowk = i / V;
   dst[i] = src[rowk * VX + c];
 }
-// [rows, 128] bf16 -> [rows, V] bf16
-__global__ void cut_rows_kernel(int64_t rows, int64_t V, const uint16_t *src, uint16_t *dst) {
+// [rows, 128] bf16 -> [rows, V] bf16, 16-byte chunks
+__global__ void cut_rows_kernel(int64_t rows, int64_t V, const uint4 *src, uint4 *dst) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= rows * V) return;
-  const int64_t r = i / V, c = i - r * V;
-  dst[i] = src[r * VX + c];
+  const int64_t nv = V / 8;
+  if (i >= rows * nv) return;
+  const int64_t r = i / nv, c = i - r * nv;
+  dst[i] = src[r * (VX / 8) + c];
 }
 // dq / dk: sum over the G = H / Hqk heads of a group, fp32, rounded once.
 // One thread per (token, group, 8 channels).
@@ -106,8 +109,8 @@ cudaError_t expand(int64_t BT, int64_t H, int64_t Hqk, int64_t V, const void *q,
                    cudaStream_t st) {
   const int64_t rows = BT * H;
   expand_kernel<<<blocks_of(rows, 8), 256, 0, st>>>(rows, H, Hqk, V, (const uint4 *)q, (const uint4 *)k,
-                                                   (const uint16_t *)v, g, (const uint16_t *)dO, (uint4 *)xq,
-                                                   (uint4 *)xk, (uint16_t *)xv, (float4 *)xg, (uint16_t *)xdo);
+                                                   (const uint4 *)v, g, (const uint4 *)dO, (uint4 *)xq,
+                                                   (uint4 *)xk, (uint4 *)xv, (float4 *)xg, (uint4 *)xdo);
   mark_launch("ssd_expand", st);
   return cudaGetLastError();
 }
@@ -122,7 +125,7 @@ cudaError_t cut_states(int64_t mats, int64_t V, const float *src, float *dst, cu
   return cudaGetLastError();
 }
 cudaError_t cut_rows(int64_t rows, int64_t V, const void *src, void *dst, cudaStream_t st) {
-  cut_rows_kernel<<<blocks_of(rows * V, 256), 256, 0, st>>>(rows, V, (const uint16_t *)src, (uint16_t *)dst);
+  cut_rows_kernel<<<blocks_of(rows * (V / 8), 256), 256, 0, st>>>(rows, V, (const uint4 *)src, (uint4 *)dst);
   mark_launch("ssd_cut_rows", st);
   return cudaGetLastError();
 }
