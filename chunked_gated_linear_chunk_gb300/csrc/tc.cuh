@@ -97,6 +97,24 @@ __device__ __forceinline__ void piece_grad_out(float (&G)[N], const float *dhtro
   }
 }
 
+// Launch of a kernel whose CTAs pair up along x in clusters of two.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pairs(void (*kernel)(Params...), dim3 grid, int smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(448, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void *o, float *ht,
                 char *ws, cudaStream_t st);
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,

@@ -63,13 +63,12 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
     a.dbuf = (float *)(ws + Lo.off_D);
     FwdArgs as = a;
     as.ht = nullptr;
-    gla_fwd_kernel<true><<<grid, 448, smem, st>>>(maps, as);
+    if ((e = launch_pairs(gla_fwd_kernel<true>, grid, smem, st, maps, as)) != cudaSuccess) return e;
     mark_launch("gla_fwd_piece_state_kernel", st);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  gla_fwd_kernel<false><<<grid, 448, smem, st>>>(maps, a);
+  if ((e = launch_pairs(gla_fwd_kernel<false>, grid, smem, st, maps, a)) != cudaSuccess) return e;
   mark_launch("gla_fwd_kernel", st);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace tc

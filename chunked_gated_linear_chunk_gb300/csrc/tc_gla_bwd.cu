@@ -1140,13 +1140,18 @@ __global__ void __launch_bounds__(448)
 // gradient at the start of every piece but the first; the longer CTAs, so
 // they are dispatched first), the rest the forward's state-only pass (local
 // end state and decay of every piece but the last of a document).
+// Launched in clusters of two along x (the forward body pairs its value
+// halves); nrev is even so that the forward CTAs pair among themselves, and
+// CTAs x in [nunits, nrev) have nothing to do.
 __global__ void __launch_bounds__(448)
     gla_piece_pass_kernel(const __grid_constant__ FwdMaps fm, const FwdArgs fa,
-                          const __grid_constant__ BwdMaps bm, const BwdArgs ba, unsigned nrev) {
-  if (blockIdx.x < nrev)
-    gla_bwd_rev_body<true>(bm, ba, blockIdx.x);
-  else
+                          const __grid_constant__ BwdMaps bm, const BwdArgs ba, unsigned nrev,
+                          unsigned nunits) {
+  if (blockIdx.x < nrev) {
+    if (blockIdx.x < nunits) gla_bwd_rev_body<true>(bm, ba, blockIdx.x);
+  } else {
     gla_fwd_body<true>(fm, fa, blockIdx.x - nrev);
+  }
 }
 
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,
@@ -1218,11 +1223,11 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     if ((e = cudaFuncSetAttribute(gla_piece_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smP)) !=
         cudaSuccess)
       return e;
-    const unsigned nrev = (unsigned)Lo.max_units;
-    gla_piece_pass_kernel<<<dim3(nrev + (unsigned)(2 * Lo.max_units), (unsigned)pr.H), 448, smP, st>>>(fm, fa, maps,
-                                                                                                        a, nrev);
+    const unsigned nunits = (unsigned)Lo.max_units, nrev = (nunits + 1) & ~1u;
+    if ((e = launch_pairs(gla_piece_pass_kernel, dim3(nrev + 2 * nunits, (unsigned)pr.H), smP, st, fm, fa, maps, a,
+                          nrev, nunits)) != cudaSuccess)
+      return e;
     mark_launch("gla_piece_pass_kernel", st);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   gla_bwd_dq_kernel<<<grid, 448, smA, st>>>(maps, a);
   mark_launch("gla_bwd_dq_kernel", st);

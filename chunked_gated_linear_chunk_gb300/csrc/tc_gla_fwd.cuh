@@ -33,9 +33,11 @@ namespace glacore {
 namespace tc {
 
 // =========================================================================
-// Forward: grid (2 * n_docs, H), 448 threads (x = 2 * doc + value half).
-// One CTA owns one document, one head and 64 value columns and walks the
-// document's chunks in order.
+// Forward: grid (2 * n_docs, H), 448 threads (x = 2 * doc + value half),
+// clusters of two CTAs along x.  One CTA owns one document, one head and
+// 64 value columns and walks the document's chunks in order; the two CTAs
+// of a cluster (the value halves) split the gate / q / k prep by key channel
+// and exchange the prepared tiles through distributed shared memory.
 //   warp 0      TMA producer (3-stage ring of q, k, v tiles; L2 prefetch of
 //               gates and of the tiles two chunks ahead)
 //   warp 1      TMEM owner and MMA issuer
@@ -69,8 +71,8 @@ constexpr uint32_t V = 98304;     // 3 x 8 KB (64 value columns)
 constexpr uint32_t P = 122880;    // 2 x 8 KB: masked P (bf16, K-major A)
 constexpr uint32_t S = 139264;    // 2 x 16 KB: S (bf16, rows = key channel)
 constexpr uint32_t GAM = 172032;  // 4 x 128 fp32: exp(chunk gate total)
-constexpr uint32_t XCH = 174080;  // 2 x 4 x 128 fp32: quarter-chunk gate products
-constexpr uint32_t BYTES = 178176;
+constexpr uint32_t XCH = 174080;  // 2 x 8 x 128 fp32: eighth-chunk gate products
+constexpr uint32_t BYTES = 182272;
 }  // namespace fsm
 
 // Shared-memory addresses of the 16 rows t0 .. t0+15 (t0 % 8 == 0) of one
@@ -169,6 +171,88 @@ __device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[1
   }
 }
 
+// Prep of one chunk by the 256 prep threads of one CTA of a pair.  The two
+// CTAs (value halves) of a (unit, head) share the q / k tiles: CTA `rank`
+// prepares key channels 64 rank .. 64 rank + 63 (one 64-column block of
+// each tile) in place; the block is then copied to the peer.
+// Thread (warp pw in 0..7, lane) owns channels c0, c0+1 (c0 = 64 rank +
+// 2 lane) and tokens t0 = 8 pw .. t0 + 7; x holds their gates.  As in
+// prep_chunk: exp(G_t) by prefix products, exp(Gam - G_t) by suffix
+// products, one exponential per element; the eight token groups exchange
+// their products through xch.
+__device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (&x)[8], float *gam, float *xch,
+                                                int pw, int lane, int rank, int L, float scale, bool with_q) {
+  const int c0 = 64 * rank + 2 * lane;
+  const int t0 = 8 * pw;
+  float p0 = 1.f, p1 = 1.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool ok = t0 + i < L;
+    x[i].x = ok ? __expf(x[i].x) : 1.f;
+    x[i].y = ok ? __expf(x[i].y) : 1.f;
+    p0 *= x[i].x;
+    p1 *= x[i].y;
+  }
+  xch[pw * 128 + c0] = p0;
+  xch[pw * 128 + c0 + 1] = p1;
+  named_bar(1, 256);
+  float pre0 = 1.f, pre1 = 1.f, suf0 = 1.f, suf1 = 1.f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float e0 = xch[u * 128 + c0], e1 = xch[u * 128 + c0 + 1];
+    if (u < pw) {
+      pre0 *= e0;
+      pre1 *= e1;
+    } else if (u > pw) {
+      suf0 *= e0;
+      suf1 *= e1;
+    }
+  }
+  const float T0 = pre0 * p0 * suf0, T1 = pre1 * p1 * suf1;  // exp(Gam)
+  // byte offsets of rows t0 .. t0+7 of the column pair (c0, c0+1) in a tile
+  uint32_t off[8];
+  {
+    const uint32_t b = (uint32_t)(c0 >> 6) * 8192u + (uint32_t)t0 * 128u + (uint32_t)(c0 & 7) * 2u;
+    const uint32_t cch = (uint32_t)(c0 & 63) >> 3;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) off[i] = b + ((cch ^ (uint32_t)i) << 4) + (uint32_t)i * 128u;
+  }
+  uint32_t v[8];
+  if (with_q) {
+    const float sp0 = scale * pre0, sp1 = scale * pre1;
+    float a0 = sp0, a1 = sp1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = lds_u32(q + off[i]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a0 *= x[i].x;
+      a1 *= x[i].y;
+      const __nv_bfloat162 qq = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
+      v[i] = (t0 + i < L) ? pack_bf16(__low2float(qq) * a0, __high2float(qq) * a1) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sts_u32(q + off[i], v[i]);
+  }
+  {
+    float a0 = suf0 * __frcp_rn(T0), a1 = suf1 * __frcp_rn(T1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
+#pragma unroll
+    for (int i = 7; i >= 0; --i) {
+      const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
+      v[i] = (t0 + i < L) ? pack_bf16(__low2float(kk) * a0, __high2float(kk) * a1) : 0u;
+      a0 *= x[i].x;
+      a1 *= x[i].y;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
+  }
+  if (pw == 0) {
+    gam[c0] = T0;
+    gam[c0 + 1] = T1;
+  }
+}
+
 __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float (&S)[64]) {
 #pragma unroll
   for (int n = 0; n < 64; n += 8)
@@ -191,7 +275,10 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the two value halves of a (unit, head) are a cluster of two CTAs that
+  // share the q / k prep (rank = value half)
   const int vb = bx & 1, h = blockIdx.y;
+  const uint32_t peer = (uint32_t)(vb ^ 1);
   const int64_t u = bx >> 1;
   const Unit un = a.units.get(u);
   const int64_t d = un.doc;
@@ -207,8 +294,8 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     abort_flag = 0;
     for (int i = 0; i < fsm::NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-      mbar_init(&prep_done[i], 256);
+      mbar_init(&empty[i], 2);        // the MMA commits of both CTAs (multicast)
+      mbar_init(&prep_done[i], 257);  // 256 local prep threads + the peer's
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
@@ -217,11 +304,12 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       mbar_init(&p_ready[i], 128);
       mbar_init(&s_ready[i], 128);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 256);
+    for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 257);
     fence_mbar_init();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tbase = tmem_base;
   const uint32_t sbase = smem_u32(sm);
@@ -259,14 +347,12 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
             tma_prefetch_3d(&maps.v, vb * 64, h, tp);
           }
         }
-        mbar_expect_tx(&full[s], (STATE_ONLY ? 16384 : 2 * 16384) + 8192);
+        // this CTA's half of the q / k channels (the peer writes the other
+        // half of the prepared tiles) and its value half of v
+        mbar_expect_tx(&full[s], (STATE_ONLY ? 8192 : 2 * 8192) + 8192);
         uint8_t *q = sm + fsm::Q + s * 16384, *k = sm + fsm::K + s * 16384;
-        if (!STATE_ONLY) {
-          tma_load_3d(q, &maps.q, 0, h, tok, &full[s]);
-          tma_load_3d(q + 8192, &maps.q, 64, h, tok, &full[s]);
-        }
-        tma_load_3d(k, &maps.k, 0, h, tok, &full[s]);
-        tma_load_3d(k + 8192, &maps.k, 64, h, tok, &full[s]);
+        if (!STATE_ONLY) tma_load_3d(q + vb * 8192, &maps.q, 64 * vb, h, tok, &full[s]);
+        tma_load_3d(k + vb * 8192, &maps.k, 64 * vb, h, tok, &full[s]);
         tma_load_3d(sm + fsm::V + s * 8192, &maps.v, vb * 64, h, tok, &full[s]);
       }
     }
@@ -283,21 +369,23 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         const uint32_t va = sbase + fsm::V + st * 8192;
         const uint32_t Pa = sbase + fsm::P + b * 8192, Sa = sbase + fsm::S + (b ^ 1) * 16384;
         const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
-        if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) {
+        if (!mbar_wait_cluster(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) {
           FAIL_AND_BREAK
         }
         ph_prep ^= 1u << st;
         if (STATE_ONLY) {
-          // U[b] is free once the epilogue has folded chunk j-2 into S
-          if (j >= 2) {
-            if (!mbar_wait(&s_ready[b], (ph_sr >> b) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
-            ph_sr ^= 1u << b;
+          // the epilogue has folded chunk j-1 into S (so U[b] is free, and the
+          // gate products of chunk j-1 are read before the prep, which runs
+          // at most NS chunks ahead of this commit, reuses their buffer)
+          if (j >= 1) {
+            if (!mbar_wait(&s_ready[b ^ 1], (ph_sr >> (b ^ 1)) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
+            ph_sr ^= 1u << (b ^ 1);
           }
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) mma_bf16(tU, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, ks);
           mma_commit(&u_full[b]);
-          mma_commit(&empty[st]);
+          mma_commit_multicast(&empty[st], 3);
           continue;
         }
         tc_fence_after();
@@ -319,22 +407,29 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tO, kdesc(Pa, ks, 64), mdesc(va, ks, 8192), idO, 1);
         mma_commit(&o_full[b]);
-        mma_commit(&empty[st]);
+        mma_commit_multicast(&empty[st], 3);
       }
+      // every commit that targets this CTA's stage barriers has landed
+      // before the CTAs leave (the peer's arrive on our barriers and ours on
+      // its): wait for the last phase of each stage
+      for (int j = max(0, nch - fsm::NS); j < nch && !*abortp; ++j)
+        if (!mbar_wait(&empty[j % fsm::NS], (j / fsm::NS) & 1, WAIT_CYCLES)) atomicExch(&abort_flag, 1);
     }
   } else if (warp < 10) {
     // ---------------- prep warps (8) ----------------
+    // this CTA's 64 key channels (c0, c0+1 per lane), tokens 8 pw .. 8 pw + 7
     const int pw = warp - 2;
-    const int c0 = 64 * (pw & 1) + 2 * lane, t0 = 16 * (pw >> 1);
+    const int c0 = 64 * vb + 2 * lane, t0 = 8 * pw;
+    const uint32_t rem = mapa_shared(sbase, peer);  // the peer's tiles
     uint32_t ph_full = 0;
     // gates of chunk j+1 are loaded into registers while chunk j is prepared
-    float2 xn[16];
-    auto load_x = [&](int jj, float2 (&x)[16]) {
+    float2 xn[8];
+    auto load_x = [&](int jj, float2 (&x)[8]) {
       const int64_t tk = s0 + (int64_t)jj * C;
       const int LL = (int)min((int64_t)C, s1 - tk);
       const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
+      for (int i = 0; i < 8; ++i)
         x[i] = (t0 + i < LL) ? __ldg(reinterpret_cast<const float2 *>(gp + (int64_t)i * a.H * KD))
                              : make_float2(0.f, 0.f);
     };
@@ -343,17 +438,33 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       const int s = j % fsm::NS;
       const int64_t tok0 = s0 + (int64_t)j * C;
       const int L = (int)min((int64_t)C, s1 - tok0);
-      float2 x[16];
+      float2 x[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = xn[i];
+      for (int i = 0; i < 8; ++i) x[i] = xn[i];
       if (j + 1 < nch) load_x(j + 1, xn);
       if (!mbar_wait(&full[s], (ph_full >> s) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
       ph_full ^= 1u << s;
-      prep_chunk(sm + fsm::Q + s * 16384, sm + fsm::K + s * 16384, x,
-                 reinterpret_cast<float *>(sm + fsm::GAM) + (j & 3) * 128,
-                 reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 512, pw, lane, L, a.scale,
-                 !STATE_ONLY);
+      // this CTA's 64-column block of q, k and its gate totals (byte offsets)
+      const uint32_t qo = fsm::Q + s * 16384 + vb * 8192, ko = fsm::K + s * 16384 + vb * 8192,
+                     go = fsm::GAM + (j & 3) * 512 + vb * 256;
+      prep_chunk_pair(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
+                      reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
+                      reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 1024, pw, lane, vb, L, a.scale,
+                      !STATE_ONLY);
       fence_async_smem();
+      // copy the prepared blocks into the peer's tiles (bulk copies that
+      // complete on the peer's barriers; one arrive there stands for the
+      // 256 threads here)
+      named_bar(1, 256);
+      if (pw == 0 && lane == 0) {
+        const uint32_t pbar = mapa_shared(smem_u32(&prep_done[s]), peer);
+        const uint32_t gbar = mapa_shared(smem_u32(&gam_ready[j & 3]), peer);
+        mbar_arrive_expect_tx_cluster(pbar, STATE_ONLY ? 8192u : 16384u);
+        if (!STATE_ONLY) bulk_copy_to_cluster(rem + qo, sbase + qo, 8192, pbar);
+        bulk_copy_to_cluster(rem + ko, sbase + ko, 8192, pbar);
+        mbar_arrive_expect_tx_cluster(gbar, 256u);
+        bulk_copy_to_cluster(rem + go, sbase + go, 256, gbar);
+      }
       mbar_arrive(&prep_done[s]);
       mbar_arrive(&gam_ready[j & 3]);
     }
@@ -417,7 +528,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       }
       // S3a: state update S <- exp(Gam) (S + kt^T V), bf16 copy for the next readout
       if (!mbar_wait(&u_full[b], (ph_u >> b) & 1, WAIT_CYCLES) ||
-          !mbar_wait(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
+          !mbar_wait_cluster(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
         FAIL_AND_BREAK
       }
       ph_u ^= 1u << b;
@@ -480,7 +591,8 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     }
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // no remote access to this CTA's shared memory after this point
   if (*abortp && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_TIMEOUT);
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
