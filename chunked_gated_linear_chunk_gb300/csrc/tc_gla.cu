@@ -8,10 +8,10 @@
 namespace glacore {
 namespace tc {
 
-template <bool STATE_ONLY>
+template <int MODE>
 __global__ void __launch_bounds__(448)
     gla_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
-  gla_fwd_body<STATE_ONLY>(maps, a, blockIdx.x);
+  gla_fwd_body<MODE>(maps, a, blockIdx.x);
 }
 
 // =========================================================================
@@ -51,8 +51,8 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   a.err = pr.err;
   const int smem = fsm::BYTES + 1024;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gla_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gla_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(gla_fwd_kernel<FWD_MAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(gla_fwd_kernel<FWD_STATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const dim3 grid((unsigned)(2 * Lo.max_units), (unsigned)pr.H);
   if (Lo.pieces) {
@@ -63,10 +63,10 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
     a.dbuf = (float *)(ws + Lo.off_D);
     FwdArgs as = a;
     as.ht = nullptr;
-    if ((e = launch_pairs(gla_fwd_kernel<true>, grid, smem, st, maps, as)) != cudaSuccess) return e;
+    if ((e = launch_pairs(gla_fwd_kernel<FWD_STATE>, grid, smem, st, maps, as)) != cudaSuccess) return e;
     mark_launch("gla_fwd_piece_state_kernel", st);
   }
-  if ((e = launch_pairs(gla_fwd_kernel<false>, grid, smem, st, maps, a)) != cudaSuccess) return e;
+  if ((e = launch_pairs(gla_fwd_kernel<FWD_MAIN>, grid, smem, st, maps, a)) != cudaSuccess) return e;
   mark_launch("gla_fwd_kernel", st);
   return cudaSuccess;
 }

@@ -1136,22 +1136,17 @@ __global__ void __launch_bounds__(448)
 }
 
 // The two piece passes of the exact sequence split in one launch (they are
-// independent): CTAs x < nrev run the reverse dH-only pass (local state
-// gradient at the start of every piece but the first; the longer CTAs, so
-// they are dispatched first), the rest the forward's state-only pass (local
-// end state and decay of every piece but the last of a document).
-// Launched in clusters of two along x (the forward body pairs its value
-// halves); nrev is even so that the forward CTAs pair among themselves, and
-// CTAs x in [nunits, nrev) have nothing to do.
+// independent), both modes of the forward kernel body in clusters of two
+// value halves: CTAs x < nfwd the forward state pass (end state and decay of
+// every piece but the last of a document), the rest the reverse pass (state
+// gradient at the start of every piece but the first, from zero at its end).
 __global__ void __launch_bounds__(448)
     gla_piece_pass_kernel(const __grid_constant__ FwdMaps fm, const FwdArgs fa,
-                          const __grid_constant__ BwdMaps bm, const BwdArgs ba, unsigned nrev,
-                          unsigned nunits) {
-  if (blockIdx.x < nrev) {
-    if (blockIdx.x < nunits) gla_bwd_rev_body<true>(bm, ba, blockIdx.x);
-  } else {
-    gla_fwd_body<true>(fm, fa, blockIdx.x - nrev);
-  }
+                          const __grid_constant__ FwdMaps rm, const FwdArgs ra, unsigned nfwd) {
+  if (blockIdx.x < nfwd)
+    gla_fwd_body<FWD_STATE>(fm, fa, blockIdx.x);
+  else
+    gla_fwd_body<REV_STATE>(rm, ra, blockIdx.x - nfwd);
 }
 
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,
@@ -1206,26 +1201,32 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     a.dr = (float *)(ws + Lo.off_Dr);
     // local end states of the pieces (forward) and local state gradients at
     // their starts (reverse), in one launch; the consumers fold them
-    FwdMaps fm;
+    FwdMaps fm, rm;
     if (!make_map(&fm.q, pr.q, true, KD, pr.Hqk, BT, 64) || !make_map(&fm.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
         !make_map(&fm.v, pr.v, true, VD, pr.H, BT, 64) || !make_map(&fm.g, pr.g, false, KD, pr.H, BT, 32))
       return cudaErrorInvalidValue;
+    rm = fm;
+    rm.k = fm.q;   // the reverse pass runs q through the k slot ...
+    rm.v = maps.dO;  // ... and do through the v slot
     FwdArgs fa;
     memset(&fa, 0, sizeof(fa));
     fa.units = a.units;
     fa.H = pr.H;
     fa.scale = pr.scale;
     fa.g = pr.g;
+    fa.err = pr.err;
+    FwdArgs ra = fa;
     fa.lbuf = (float *)(ws + Lo.off_L);
     fa.dbuf = (float *)(ws + Lo.off_D);
-    fa.err = pr.err;
-    const int smP = (fsm::BYTES > bsm::BYTES ? fsm::BYTES : bsm::BYTES) + 1024;
+    ra.lbuf = a.lr;
+    ra.dbuf = a.dr;
+    const int smP = fsm::BYTES + 1024;
     if ((e = cudaFuncSetAttribute(gla_piece_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smP)) !=
         cudaSuccess)
       return e;
-    const unsigned nunits = (unsigned)Lo.max_units, nrev = (nunits + 1) & ~1u;
-    if ((e = launch_pairs(gla_piece_pass_kernel, dim3(nrev + 2 * nunits, (unsigned)pr.H), smP, st, fm, fa, maps, a,
-                          nrev, nunits)) != cudaSuccess)
+    const unsigned nfwd = (unsigned)(2 * Lo.max_units);
+    if ((e = launch_pairs(gla_piece_pass_kernel, dim3(2 * nfwd, (unsigned)pr.H), smP, st, fm, fa, rm, ra, nfwd)) !=
+        cudaSuccess)
       return e;
     mark_launch("gla_piece_pass_kernel", st);
   }

@@ -47,6 +47,13 @@ namespace tc {
 //               registers, thread c holds row c), output stores
 // TMEM (512 columns): P[2] at 0/64, U[2] at 128/192, O[2] at 256/320.
 // =========================================================================
+// Modes of the forward kernel body: the forward itself, and the two
+// state-only passes of the exact sequence split (forward: each piece's end
+// state from zero; reverse: each piece's state gradient at its start from
+// zero at its end -- maps.k / maps.v then hold q / do, chunks run backwards,
+// and the k-slot factor is scale exp(G - Gam)).
+constexpr int FWD_MAIN = 0, FWD_STATE = 1, REV_STATE = 2;
+
 struct FwdMaps {
   CUtensorMap q, k, v, g;
 };
@@ -180,8 +187,11 @@ __device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[1
 // prep_chunk: exp(G_t) by prefix products, exp(Gam - G_t) by suffix
 // products, one exponential per element; the eight token groups exchange
 // their products through xch.
+// rev (reverse state-gradient pass): the tile in the k slot holds q and
+// becomes scale q exp(G - Gam) (prefix products) instead of k exp(-G).
 __device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (&x)[8], float *gam, float *xch,
-                                                int pw, int lane, int rank, int L, float scale, bool with_q) {
+                                                int pw, int lane, int rank, int L, float scale, bool with_q,
+                                                bool rev) {
   const int c0 = 64 * rank + 2 * lane;
   const int t0 = 8 * pw;
   float p0 = 1.f, p1 = 1.f;
@@ -233,7 +243,7 @@ __device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (
 #pragma unroll
     for (int i = 0; i < 8; ++i) sts_u32(q + off[i], v[i]);
   }
-  {
+  if (!rev) {
     float a0 = suf0 * __frcp_rn(T0), a1 = suf1 * __frcp_rn(T1);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
@@ -243,6 +253,19 @@ __device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (
       v[i] = (t0 + i < L) ? pack_bf16(__low2float(kk) * a0, __high2float(kk) * a1) : 0u;
       a0 *= x[i].x;
       a1 *= x[i].y;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
+  } else {
+    float a0 = scale * pre0 * __frcp_rn(T0), a1 = scale * pre1 * __frcp_rn(T1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a0 *= x[i].x;
+      a1 *= x[i].y;
+      const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
+      v[i] = (t0 + i < L) ? pack_bf16(__low2float(kk) * a0, __high2float(kk) * a1) : 0u;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
@@ -261,12 +284,14 @@ __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float
                  pack_bf16(S[n + 6], S[n + 7]));
 }
 
-// STATE_ONLY: the piece pass of the exact sequence split -- only the state
+// STATE_ONLY (MODE != FWD_MAIN): the piece passes of the exact sequence split -- only the state
 // recurrence from a zero state (no q, no output); writes the piece's end
 // state and its total decay.  Pieces that end their document have nothing
 // to contribute and exit.
-template <bool STATE_ONLY>
+template <int MODE>
 __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs &a, unsigned bx) {
+  constexpr bool STATE_ONLY = MODE != FWD_MAIN;
+  constexpr bool REV = MODE == REV_STATE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[fsm::NS], empty[fsm::NS], prep_done[fsm::NS], p_full[2], u_full[2],
@@ -284,7 +309,12 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   const int64_t d = un.doc;
   const int64_t s0 = un.start, s1 = un.end;
   const bool last_piece = un.piece == un.npieces - 1;
-  const int nch = (STATE_ONLY && last_piece) ? 0 : (int)((s1 - s0 + C - 1) / C);
+  // the forward state pass has nothing to hand on from a document's last
+  // piece, the reverse pass nothing from its first
+  const bool idle = STATE_ONLY && (REV ? un.piece == 0 : last_piece);
+  const int nch = idle ? 0 : (int)((s1 - s0 + C - 1) / C);
+  // chunk visited at iteration j (the reverse pass walks backwards)
+  auto chunk_tok = [&](int j) -> int64_t { return s0 + (int64_t)(REV ? nch - 1 - j : j) * C; };
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -332,10 +362,10 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         if (j >= fsm::NS && !mbar_wait(&empty[s], ((j / fsm::NS) - 1) & 1, WAIT_CYCLES))
           FAIL_AND_BREAK
         if (*abortp) break;
-        const int tok = (int)(s0 + (int64_t)j * C);
+        const int tok = (int)chunk_tok(j);
         for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
           // gates for the prep warps (read from L2); q/k/v ahead of the ring
-          const int tp = (int)(s0 + (int64_t)jp * C);
+          const int tp = (int)chunk_tok(jp);
           for (int x = 0; x < KD; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
           if (jp >= fsm::NS) {
             if (!STATE_ONLY) {
@@ -425,7 +455,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     // gates of chunk j+1 are loaded into registers while chunk j is prepared
     float2 xn[8];
     auto load_x = [&](int jj, float2 (&x)[8]) {
-      const int64_t tk = s0 + (int64_t)jj * C;
+      const int64_t tk = chunk_tok(jj);
       const int LL = (int)min((int64_t)C, s1 - tk);
       const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
 #pragma unroll
@@ -436,7 +466,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     if (nch > 0) load_x(0, xn);
     for (int j = 0; j < nch; ++j) {
       const int s = j % fsm::NS;
-      const int64_t tok0 = s0 + (int64_t)j * C;
+      const int64_t tok0 = chunk_tok(j);
       const int L = (int)min((int64_t)C, s1 - tok0);
       float2 x[8];
 #pragma unroll
@@ -450,7 +480,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       prep_chunk_pair(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
                       reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
                       reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 1024, pw, lane, vb, L, a.scale,
-                      !STATE_ONLY);
+                      !STATE_ONLY, REV);
       fence_async_smem();
       // copy the prepared blocks into the peer's tiles (bulk copies that
       // complete on the peer's barriers; one arrive there stands for the
@@ -494,7 +524,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     uint32_t ph_p = 0, ph_u = 0, ph_o = 0;
     for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
-      const int64_t tok0 = s0 + (int64_t)j * C;
+      const int64_t tok0 = chunk_tok(j);
       const int L = (int)min((int64_t)C, s1 - tok0);
       const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
       // S2: P -> causal mask -> bf16 A operand of the intra-chunk product
