@@ -49,8 +49,8 @@ struct BwdArgs {
   float *dgp;    // scratch [BT, H, K] fp32
   float *bvec;   // scratch [units, H, K] fp32
   const float *lf, *df;  // forward piece hand-off: [units,H,K,V] end states from zero, [units,H,K] decays
-  float *lr, *dr;        // reverse piece hand-off (dH-only mode writes them): state gradients
-                         // at the piece starts from zero, decays
+  const float *lr, *dr;  // reverse piece hand-off: [units,H,K,V] state gradients at the piece
+                         // starts from zero at their ends, [units,H,K] decays
   float *ckpt;   // [slots,H,K,V] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
   int *err;
 };
@@ -611,18 +611,12 @@ constexpr uint32_t BND = 217088;   // 2 x 128 fp32: exact gate-gradient carry at
 constexpr uint32_t BYTES = 218112;
 }  // namespace bsm
 
-// DH_ONLY: the reverse piece pass of the exact sequence split -- only the
-// state-gradient recurrence from zero at the piece end (needs q, g, do);
-// writes the gradient at the piece start and the piece's total decay.
-// First pieces have nothing to contribute and exit.
-//
 // Thread roles: warp 0 lane 0 TMA loads of q, do; lane 1 TMA loads of k, v;
 // lane 2 TMA loads of the gate-gradient partials and TMA stores of dk, dv,
 // dg.  Warp 1 MMA + TMEM.  Warps 2..9 per-channel warps (key channel /
 // value column c, token half th): qt, kt and exp(-G) of chunk i, then the
 // dk / dg / dv epilogue of chunk i-1, written over kt, v and the partials.
 // Warps 10..13 mask P and dP and scale the state gradient.
-template <bool DH_ONLY>
 __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdArgs &a, unsigned bx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -639,7 +633,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
   const Unit un = a.units.get(u);
   const int64_t d = un.doc;
   const int64_t s0 = un.start, s1 = un.end;
-  const int nch = (DH_ONLY && un.piece == 0) ? 0 : (int)((s1 - s0 + C - 1) / C);
+  const int nch = (int)((s1 - s0 + C - 1) / C);
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -697,14 +691,12 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           for (int x = 0; x < 128; x += 64) {
             tma_prefetch_3d(&maps.q, x, h, tp);
             tma_prefetch_3d(&maps.dO, x, h, tp);
-            if (!DH_ONLY) {
-              tma_prefetch_3d(&maps.k, x, h, tp);
-              tma_prefetch_3d(&maps.v, x, h, tp);
-            }
+            tma_prefetch_3d(&maps.k, x, h, tp);
+            tma_prefetch_3d(&maps.v, x, h, tp);
           }
           for (int x = 0; x < 128; x += 32) {
             tma_prefetch_3d(&maps.g, x, h, tp);
-            if (!DH_ONLY) tma_prefetch_3d(&maps.dgp, x, h, tp);
+            tma_prefetch_3d(&maps.dgp, x, h, tp);
           }
         }
         mbar_expect_tx(&full[st], 2 * 16384);
@@ -713,7 +705,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           tma_load_3d(sm + bsm::DO + st * 16384 + x * 8192, &maps.dO, 64 * x, h, tok, &full[st]);
         }
       }
-    } else if (lane == 1 && !DH_ONLY) {
+    } else if (lane == 1) {
       // ring of k and v: released once dk and dv (written over them) are stored
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
@@ -729,7 +721,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           tma_load_3d(sm + bsm::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &kfull[st]);
         }
       }
-    } else if (lane == 2 && !DH_ONLY) {
+    } else if (lane == 2) {
       // gate-gradient partials in, dk / dv / dg of full chunks out (a ragged
       // chunk is stored by its epilogue threads)
       tma_prefetch_desc(&maps.dgp);
@@ -784,37 +776,33 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_prep ^= 1u << st;
         tc_fence_after();
-        if (!DH_ONLY) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(kta, ks, 64), idCC, ks);
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(kta, ks, 64), idCC, ks);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tDP, kdesc(doa, ks, 64), kdesc(va, ks, 64), idCC, ks);
-          mma_commit(&pdp_full);
-        }
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDP, kdesc(doa, ks, 64), kdesc(va, ks, 64), idCC, ks);
+        mma_commit(&pdp_full);
         // dH (TMEM, = dHh after the state step) += qt^T dO
         if (!mbar_wait(&dh_ready, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tDH, mdesc(qa, ks, 8192), mdesc(doa, ks, 8192), idH, 1);
         mma_commit(&dh_full);
-        if (!DH_ONLY) {
-          // dk/dv accumulators are free once the epilogue of chunk i-1 has read them
-          if (!mbar_wait(&pdp_ready, i & 1, WAIT_CYCLES) ||
-              (i >= 1 && !mbar_wait(&kv_free, (i - 1) & 1, WAIT_CYCLES)))
-            BW_FAIL_AND_BREAK
-          tc_fence_after();
-          // dk^T = qt^T dP + dHh V^T
+        // dk/dv accumulators are free once the epilogue of chunk i-1 has read them
+        if (!mbar_wait(&pdp_ready, i & 1, WAIT_CYCLES) ||
+            (i >= 1 && !mbar_wait(&kv_free, (i - 1) & 1, WAIT_CYCLES)))
+          BW_FAIL_AND_BREAK
+        tc_fence_after();
+        // dk^T = qt^T dP + dHh V^T
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDK, mdesc(qa, ks, 8192), mdesc(dpa, ks, 8192), idMM, ks);
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDK, mdesc(qa, ks, 8192), mdesc(dpa, ks, 8192), idMM, ks);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tDK, kdesc(dha, ks, 128), kdesc(va, ks, 64), idKK, 1);
-          // dv^T = dO^T P + dHh^T kt^T
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDK, kdesc(dha, ks, 128), kdesc(va, ks, 64), idKK, 1);
+        // dv^T = dO^T P + dHh^T kt^T
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) mma_bf16(tDV, mdesc(doa, ks, 8192), mdesc(pa, ks, 8192), idMM, ks);
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDV, mdesc(doa, ks, 8192), mdesc(pa, ks, 8192), idMM, ks);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) mma_bf16(tDV, mdesc(dha, ks, 16384), kdesc(kta, ks, 64), idMK, 1);
-          mma_commit(&kv_full);
-        }
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDV, mdesc(dha, ks, 16384), kdesc(kta, ks, 64), idMK, 1);
+        mma_commit(&kv_full);
         mma_commit(&empty[st]);
       }
     }
@@ -824,7 +812,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     uint32_t ph_full = 0, ph_free = 0;
-    float carry = (!DH_ONLY && a.bvec) ? a.bvec[(u * H + h) * KD + c] : 0.f;
+    float carry = a.bvec ? a.bvec[(u * H + h) * KD + c] : 0.f;
     float xn[32];  // gates of the next chunk (in visiting order)
     if (nch > 0) {
       const int64_t tl = s0 + (int64_t)(nch - 1) * C;
@@ -868,7 +856,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
           ph_free ^= 1u << b;
         }
-        if (!DH_ONLY && !mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if (!mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
         {
           const ColBf16 kc(sbase + bsm::K + st * 16384, 32 * th, c);
@@ -877,21 +865,17 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           for (int hb = 1; hb >= 0; --hb) {
             uint32_t r[16];
             uint16_t kb[16];
-            if (!DH_ONLY) {
 #pragma unroll
-              for (int w = 0; w < 16; ++w) kb[w] = lds_u16(kc.at(16 * hb + w));
-            }
+            for (int w = 0; w < 16; ++w) kb[w] = lds_u16(kc.at(16 * hb + w));
 #pragma unroll
             for (int w = 15; w >= 0; --w) {
               const int t = 32 * th + 16 * hb + w;
               r[w] = __float_as_uint(e);
-              if (!DH_ONLY) kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
+              kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
               e *= cg.x[16 * hb + w];
             }
-            if (!DH_ONLY) {
 #pragma unroll
-              for (int w = 0; w < 16; ++w) sts_u16(kc.at(16 * hb + w), kb[w]);
-            }
+            for (int w = 0; w < 16; ++w) sts_u16(kc.at(16 * hb + w), kb[w]);
             tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
           }
         }
@@ -901,7 +885,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         mbar_arrive(&prep_done[st]);
         mbar_arrive(&eg_ready[b]);
       }
-      if (!DH_ONLY && i >= 1) {
+      if (i >= 1) {
         // epilogue of chunk jj (visited at ii = i - 1), this thread's half:
         //   dk_t = exp(-G_t) acc_t (channel c),  dv_t (value column c),
         //   dg_t = dgp_t - sum_{r >= t in chunk} k_r dk_r + carry,  k dk = kt acc
@@ -1006,16 +990,11 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     // dH = state gradient leaving the unit: dht folded over the document's
     // later pieces (0 in dH-only mode)
     {
-      const float *dhtrow = (!DH_ONLY && a.dht) ? a.dht + ((d * H + h) * KD + c) * VD : nullptr;
+      const float *dhtrow = a.dht ? a.dht + ((d * H + h) * KD + c) * VD : nullptr;
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         float dh[32];
-        if (DH_ONLY) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) dh[e] = 0.f;
-        } else {
-          piece_grad_out<32>(dh, dhtrow, a.lr, a.dr, u - un.piece, un.piece, un.npieces, H, h, c, 32 * cb);
-        }
+        piece_grad_out<32>(dh, dhtrow, a.lr, a.dr, u - un.piece, un.piece, un.npieces, H, h, c, 32 * cb);
         uint32_t r[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(dh[e]);
@@ -1023,21 +1002,18 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
       }
       tmem_st_wait();
     }
-    float decay = 1.f;  // dH-only mode: exp(sum of g over the piece)
     uint32_t ph_egr = 0;
     for (int i = 0; i < nch; ++i) {
       const int j = nch - 1 - i, b = i & 1;
       // (1) masked P and dP -> bf16 operands (dk/dv of chunk i-1, their last
       //     readers, are complete: pdp_full(i) is committed after them)
-      if (!DH_ONLY) {
-        if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        tc_fence_after();
-        mask_tile_to_smem(tP, lane_off, qw, lane, sm + bsm::P);
-        mask_tile_to_smem(tDP, lane_off, qw, lane, sm + bsm::DP);
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(&pdp_ready);
-      }
+      if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      tc_fence_after();
+      mask_tile_to_smem(tP, lane_off, qw, lane, sm + bsm::P);
+      mask_tile_to_smem(tDP, lane_off, qw, lane, sm + bsm::DP);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&pdp_ready);
       // (2) dHh = exp(Gam) dH in TMEM; its bf16 copy replaces chunk i-1's
       //     once dk/dv of chunk i-1 have read that
       if (!mbar_wait(&eg_ready[b], (ph_egr >> b) & 1, WAIT_CYCLES) ||
@@ -1052,12 +1028,11 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         const float eGam = __frcp_rn(__uint_as_float(e1[15]));  // 1 / exp(-Gam)
         tc_fence_before();
         mbar_arrive(&eg_free[b]);
-        decay *= eGam;
         uint8_t *Dt = sm + bsm::DH;
-        const int64_t slot = DH_ONLY ? -1 : ckpt_slot(gc0, doc_c0, j, nch);
+        const int64_t slot = ckpt_slot(gc0, doc_c0, j, nch);
         const float *ck = slot >= 0 ? a.ckpt + ((slot * H + h) * KD + c) * VD : nullptr;
         float bnd = 0.f;
-        bool waited = DH_ONLY || i == 0;
+        bool waited = i == 0;
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t r[32];
@@ -1070,30 +1045,26 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
 #pragma unroll
           for (int w = 0; w < 32; ++w) r[w] = __float_as_uint(eGam * __uint_as_float(r[w]));
           tmem_st32(tDH + lane_off + 32 * cb, r);
-          if (!DH_ONLY) {
-            if (!waited) {
-              if (!mbar_wait(&kv_full, (i - 1) & 1, WAIT_CYCLES)) {
-                atomicExch(&abort_flag, 1);
-                break;
-              }
-              waited = true;
+          if (!waited) {
+            if (!mbar_wait(&kv_full, (i - 1) & 1, WAIT_CYCLES)) {
+              atomicExch(&abort_flag, 1);
+              break;
             }
-#pragma unroll
-            for (int n = 0; n < 32; n += 8)
-              st_shared_v4(smem_u32(Dt + sw128_off(c, 32 * cb + n, 128)),
-                           pack_bf16(__uint_as_float(r[n]), __uint_as_float(r[n + 1])),
-                           pack_bf16(__uint_as_float(r[n + 2]), __uint_as_float(r[n + 3])),
-                           pack_bf16(__uint_as_float(r[n + 4]), __uint_as_float(r[n + 5])),
-                           pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
+            waited = true;
           }
+#pragma unroll
+          for (int n = 0; n < 32; n += 8)
+            st_shared_v4(smem_u32(Dt + sw128_off(c, 32 * cb + n, 128)),
+                         pack_bf16(__uint_as_float(r[n]), __uint_as_float(r[n + 1])),
+                         pack_bf16(__uint_as_float(r[n + 2]), __uint_as_float(r[n + 3])),
+                         pack_bf16(__uint_as_float(r[n + 4]), __uint_as_float(r[n + 5])),
+                         pack_bf16(__uint_as_float(r[n + 6]), __uint_as_float(r[n + 7])));
         }
         if (*abortp) break;
         tmem_st_wait();
-        if (!DH_ONLY) {
-          // exact (S_end (.) dH_end) 1_V at this boundary, for the carry
-          reinterpret_cast<float *>(sm + bsm::BND)[b * 128 + c] = bnd;
-          mbar_arrive(&bnd_ready[b]);
-        }
+        // exact (S_end (.) dH_end) 1_V at this boundary, for the carry
+        reinterpret_cast<float *>(sm + bsm::BND)[b * 128 + c] = bnd;
+        mbar_arrive(&bnd_ready[b]);
       }
       fence_async_smem();
       tc_fence_before();
@@ -1103,10 +1074,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     if (nch > 0 && !*abortp && !mbar_wait(&dh_full, (nch - 1) & 1, WAIT_CYCLES)) atomicExch(&abort_flag, 1);
     tc_fence_after();
     float *dst = nullptr;
-    if (DH_ONLY && nch > 0) {
-      dst = a.lr + ((u * H + h) * KD + c) * VD;
-      a.dr[(u * H + h) * KD + c] = decay;
-    } else if (!DH_ONLY && a.dh0 && un.piece == 0) {
+    if (a.dh0 && un.piece == 0) {
       dst = a.dh0 + ((d * H + h) * KD + c) * VD;
     }
     if (!*abortp && dst) {
@@ -1129,10 +1097,9 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <bool DH_ONLY>
 __global__ void __launch_bounds__(448)
     gla_bwd_rev_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
-  gla_bwd_rev_body<DH_ONLY>(maps, a, blockIdx.x);
+  gla_bwd_rev_body(maps, a, blockIdx.x);
 }
 
 // The two piece passes of the exact sequence split in one launch (they are
@@ -1189,7 +1156,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   const int smA = asm_::BYTES + 1024, smB = bsm::BYTES + 1024;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gla_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smA)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gla_bwd_rev_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
+      (e = cudaFuncSetAttribute(gla_bwd_rev_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
     return e;
   if (Lo.pieces) {
     if (Lo.table &&
@@ -1197,8 +1164,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       return e;
     a.lf = (const float *)(ws + Lo.off_L);
     a.df = (const float *)(ws + Lo.off_D);
-    a.lr = (float *)(ws + Lo.off_Lr);
-    a.dr = (float *)(ws + Lo.off_Dr);
+    a.lr = (const float *)(ws + Lo.off_Lr);
+    a.dr = (const float *)(ws + Lo.off_Dr);
     // local end states of the pieces (forward) and local state gradients at
     // their starts (reverse), in one launch; the consumers fold them
     FwdMaps fm, rm;
@@ -1218,8 +1185,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     FwdArgs ra = fa;
     fa.lbuf = (float *)(ws + Lo.off_L);
     fa.dbuf = (float *)(ws + Lo.off_D);
-    ra.lbuf = a.lr;
-    ra.dbuf = a.dr;
+    ra.lbuf = (float *)(ws + Lo.off_Lr);
+    ra.dbuf = (float *)(ws + Lo.off_Dr);
     const int smP = fsm::BYTES + 1024;
     if ((e = cudaFuncSetAttribute(gla_piece_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smP)) !=
         cudaSuccess)
@@ -1233,7 +1200,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   gla_bwd_dq_kernel<<<grid, 448, smA, st>>>(maps, a);
   mark_launch("gla_bwd_dq_kernel", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gla_bwd_rev_kernel<false><<<grid, 448, smB, st>>>(maps, a);
+  gla_bwd_rev_kernel<<<grid, 448, smB, st>>>(maps, a);
   mark_launch("gla_bwd_rev_kernel", st);
   (void)p;
   return cudaGetLastError();
