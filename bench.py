@@ -400,7 +400,7 @@ def kernel_source_sha():
 
 # ncu kernel names -> the library's launch labels (template argument: mode)
 NCU_LABELS = (("gla_fwd_kernel<0>", "gla_fwd_kernel"), ("gla_fwd_kernel<1>", "gla_fwd_piece_state_kernel"),
-              ("gla_bwd_rev_kernel<0>", "gla_bwd_rev_kernel"), ("gla_piece_pass_kernel", "gla_piece_pass_kernel"),
+              ("gla_bwd_rev_kernel", "gla_bwd_rev_kernel"), ("gla_piece_pass_kernel", "gla_piece_pass_kernel"),
               ("gla_bwd_dq_kernel", "gla_bwd_dq_kernel"))
 
 
@@ -417,7 +417,7 @@ def ingest_traffic(csv_path):
                 "GB": 1024.0 ** 3}
     per = {}
     for r in data:
-        name = r[ix["Kernel Name"]].replace("(bool)", "").replace(" ", "")
+        name = r[ix["Kernel Name"]].replace("(bool)", "").replace("(int)", "").replace(" ", "")
         lab = next((l for key, l in NCU_LABELS if key in name), None)
         if lab is None or r[ix["Metric Name"]] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
