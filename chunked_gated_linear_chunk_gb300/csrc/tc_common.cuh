@@ -67,6 +67,24 @@ __device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, ui
                "r"(d)
                : "memory");
 }
+// Read-only global loads issued where they stand: a volatile asm keeps the
+// compiler from sinking them to their first use, so loads meant for the next
+// chunk stay in flight while the current one is processed.
+__device__ __forceinline__ float ldg_early(const float *p) {
+  float r;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ float2 ldg_early2(const float *p) {
+  float2 r;
+  asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(r.x), "=f"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ float4 ldg_early4(const float *p) {
+  float4 r;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p));
+  return r;
+}
 __device__ __forceinline__ float bf16_at(const uint8_t *tile, uint32_t off) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
 }
@@ -76,14 +94,13 @@ __device__ __forceinline__ void put_bf16(uint8_t *tile, uint32_t off, float x) {
 
 // K-major descriptor step ks (16 elements along K) of a tile whose K extent
 // is split into 64-element column blocks of `rows` rows each.
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks, uint32_t rows) {
-  return sdesc_sw128(base + (uint32_t)(ks >> 2) * rows * 128u + (uint32_t)(ks & 3) * 32u, 16,
-                     1024);
+__device__ __forceinline__ SDesc kdesc(uint32_t base, int ks, uint32_t rows) {
+  return sdesc_sw128(base, 16, 1024) + ((uint32_t)(ks >> 2) * rows * 128u + (uint32_t)(ks & 3) * 32u);
 }
 // MN-major descriptor step ks (16 rows along K) of a tile of K rows whose
 // M/N extent is split into 64-element column blocks `blk` bytes apart.
-__device__ __forceinline__ uint64_t mdesc(uint32_t base, int ks, uint32_t blk) {
-  return sdesc_sw128(base + (uint32_t)ks * 2048u, blk, 1024);
+__device__ __forceinline__ SDesc mdesc(uint32_t base, int ks, uint32_t blk) {
+  return sdesc_sw128(base, blk, 1024) + (uint32_t)ks * 2048u;
 }
 
 
@@ -233,30 +250,62 @@ __device__ __forceinline__ void store_block_bf16(__nv_bfloat16 *row0, int64_t st
   }
 }
 
-// Masked copy of a C x C fp32 accumulator (M = 64 TMEM layout: row r in
-// lane 32 (r / 16) + r % 16) into a bf16 K-major tile [row][col] with the
-// 128-byte swizzle, keeping col <= row and zeroing the rest.  Called by a
-// whole warp of the epilogue warpgroup (warp quarter qw).
+// Orders the uses of registers filled by an earlier tcgen05.ld after a
+// tcgen05.wait::ld that was tied to other registers (volatile asm statements
+// keep their order): lets one wait cover several loads.
+__device__ __forceinline__ void tmem_tie(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+// Masked C x C tiles (causal mask col <= row) in shared memory: bf16
+// K-major [row][col] with the 128-byte swizzle, written from an fp32
+// accumulator in the M = 64 TMEM layout (row r in lane 32 (r / 16) + r % 16).
+// Warp quarter qw owns rows 16 qw .. 16 qw + 15, so its 16-column blocks
+// cb > qw are zero for every chunk: mask_tile_init writes them once, and
+// mask_tile_to_smem then loads and writes only the blocks cb <= qw (the
+// diagonal block cb == qw with the mask).  Nothing else may write the tile.
+__device__ __forceinline__ void mask_block_store(uint8_t *tile, int row, int cb, const uint32_t (&r)[16],
+                                                 bool diag, int lane) {
+#pragma unroll
+  for (int hb = 0; hb < 2; ++hb) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i0 = hb * 8 + 2 * e;
+      const float x0 = (!diag || i0 <= lane) ? __uint_as_float(r[i0]) : 0.f;
+      const float x1 = (!diag || i0 + 1 <= lane) ? __uint_as_float(r[i0 + 1]) : 0.f;
+      w[e] = pack_bf16(x0, x1);
+    }
+    st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), w[0], w[1], w[2], w[3]);
+  }
+}
+__device__ __forceinline__ void mask_tile_init(uint8_t *tile, int qw, int lane) {
+  if (lane < 16) {
+    const int row = qw * 16 + lane;
+    for (int cb = qw + 1; cb < 4; ++cb)
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb)
+        st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), 0u, 0u, 0u, 0u);
+  }
+}
+// Called by a whole warp of the epilogue warpgroup (warp quarter qw).
 __device__ __forceinline__ void mask_tile_to_smem(uint32_t t_acc, uint32_t lane_off, int qw, int lane,
                                                   uint8_t *tile) {
   const int row = qw * 16 + lane;
 #pragma unroll
-  for (int cb = 0; cb < 4; ++cb) {
-    uint32_t r[16];
-    tmem_ld16(t_acc + lane_off + cb * 16, r);
-    tmem_ld_wait(r);
-    if (lane < 16) {
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c0 = cb * 16 + hb * 8 + 2 * e;
-          const float x0 = c0 <= row ? __uint_as_float(r[hb * 8 + 2 * e]) : 0.f;
-          const float x1 = c0 + 1 <= row ? __uint_as_float(r[hb * 8 + 2 * e + 1]) : 0.f;
-          w[e] = pack_bf16(x0, x1);
-        }
-        st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), w[0], w[1], w[2], w[3]);
+  for (int cp = 0; cp < 4; cp += 2) {
+    if (cp <= qw) {
+      uint32_t r0[16], r1[16];
+      tmem_ld16(t_acc + lane_off + cp * 16, r0);
+      tmem_ld16(t_acc + lane_off + cp * 16 + 16, r1);
+      tmem_ld_wait(r0);
+      tmem_tie(r1);
+      if (lane < 16) {
+        mask_block_store(tile, row, cp, r0, cp == qw, lane);
+        if (cp + 1 <= qw) mask_block_store(tile, row, cp + 1, r1, cp + 1 == qw, lane);
       }
     }
   }

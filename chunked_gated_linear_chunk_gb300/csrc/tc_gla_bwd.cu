@@ -35,7 +35,7 @@ namespace glacore {
 namespace tc {
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dO, dgp, dq, g, dk, dv, dg;
+  CUtensorMap q, k, v, dO, dq, g, dk, dv, qt, kt;
 };
 struct BwdArgs {
   Units units;
@@ -46,12 +46,13 @@ struct BwdArgs {
   const float *dht;    // [n_docs,H,K,V] or null
   __nv_bfloat16 *dq, *dk, *dv;
   float *dg, *dh0;
-  float *dgp;    // scratch [BT, H, K] fp32
+  float *dgp;    // scratch [chunk slots, H, C/4, K, 4] fp32: within-chunk suffix sums of q (.) dq
   float *bvec;   // scratch [units, H, K] fp32
   const float *lf, *df;  // forward piece hand-off: [units,H,K,V] end states from zero, [units,H,K] decays
   const float *lr, *dr;  // reverse piece hand-off: [units,H,K,V] state gradients at the piece
                          // starts from zero at their ends, [units,H,K] decays
   float *ckpt;   // [slots,H,K,V] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
+  __nv_bfloat16 *qt, *kt;  // scratch [BT, H, K]: gated q and k (pass A -> pass B)
   int *err;
 };
 
@@ -94,7 +95,7 @@ __device__ __forceinline__ void load_gates(ChanGate &cg, const float *g, int64_t
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const int t = 32 * th + i;
-    cg.x[i] = t < L ? __ldg(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
+    cg.x[i] = t < L ? ldg_early(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
   }
 }
 __device__ __forceinline__ void load_gates_to(float (&x)[32], const float *g, int64_t tok0, int64_t H,
@@ -102,7 +103,7 @@ __device__ __forceinline__ void load_gates_to(float (&x)[32], const float *g, in
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const int t = 32 * th + i;
-    x[i] = t < L ? __ldg(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
+    x[i] = t < L ? ldg_early(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
   }
 }
 // Tokens 32 th + I0 .. 32 th + I0 + N - 1 of load_gates_to: the loads of one
@@ -113,7 +114,7 @@ __device__ __forceinline__ void load_gates_part(float (&x)[32], const float *g, 
 #pragma unroll
   for (int i = I0; i < I0 + N; ++i) {
     const int t = 32 * th + i;
-    x[i] = t < L ? __ldg(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
+    x[i] = t < L ? ldg_early(g + ((tok0 + t) * H + h) * KD + c) : 0.f;
   }
 }
 __device__ __forceinline__ void exchange_gates(ChanGate &cg, float *xch, int c, int th, int L) {
@@ -142,15 +143,16 @@ constexpr uint32_t V = 65536;      // 2 x 16 KB
 constexpr uint32_t DO = 98304;     // 2 x 16 KB
 constexpr uint32_t DP = 131072;    // 8 KB masked dP (bf16 [t][s])
 constexpr uint32_t GT = 139264;    // 32 KB gate tile g [t][c] (fp32, TMA box 32 x 64)
-constexpr uint32_t STG = 172032;   // 32 KB gate-gradient partials (fp32, store source)
-constexpr uint32_t XCH = 204800;   // 2 x 2 x 128 fp32 gate products
-constexpr uint32_t XQ = 206848;    // 2 x 128 fp32: token-half totals of q (.) dq
-constexpr uint32_t BYTES = 207872;
+constexpr uint32_t QT = 172032;    // 16 KB qt = scale q exp(G) (bf16, store source for pass B)
+constexpr uint32_t XCH = 188416;   // 2 x 2 x 128 fp32 gate products
+constexpr uint32_t XQ = 190464;    // 2 x 128 fp32: token-half totals of q (.) dq
+constexpr uint32_t BYTES = 191488;
 }  // namespace asm_
 
 // Thread roles: warp 0 lane 0 TMA loads of k, v, do; lane 1 TMA loads of
-// raw q; lane 2 TMA stores of dq and the gate-gradient partials; lane 3 TMA
-// loads of the gate tile.  Warp 1
+// raw q; lane 2 TMA stores of dq and qt; lane 3
+// TMA loads of the gate tile; lane 4 TMA stores of kt.  Pass B takes the
+// gated operands qt, kt from here instead of gating q and k again.  Warp 1
 // MMA + TMEM.  Warps 2..9 per-channel warps (key channel c = lane of the
 // warp's TMEM quarter, token half th): gate work and kt for chunk j, then
 // the dq / q (.) dq epilogue of chunk j-1 for their half, written to shared
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(448)
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[asm_::NS], empty[asm_::NS], qfull[asm_::NS], qempty[asm_::NS],
       prep_done[asm_::NS], dp_full, dp_ready, dq_full[2], dq_free[2], u_full, s_ready, eg_ready[2],
-      eg_free[2], out_ready, stg_free, g_full, g_free;
+      eg_free[2], out_ready, stg_free, g_full, g_free, kt_read[asm_::NS];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(448)
       mbar_init(&qfull[i], 1);   // raw q, then dq (released by the store thread)
       mbar_init(&qempty[i], 1);
       mbar_init(&prep_done[i], 256);
+      mbar_init(&kt_read[i], 1);  // kt of the stage copied out (lane 4)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&dq_full[i], 1);
@@ -220,7 +223,8 @@ __global__ void __launch_bounds__(448)
       tma_prefetch_desc(&maps.g);
       for (int j = 0; j < nch; ++j) {
         const int st = j % asm_::NS;
-        if (j >= asm_::NS && !mbar_wait(&empty[st], ((j / asm_::NS) - 1) & 1, WAIT_CYCLES))
+        if (j >= asm_::NS && (!mbar_wait(&empty[st], ((j / asm_::NS) - 1) & 1, WAIT_CYCLES) ||
+                              !mbar_wait(&kt_read[st], ((j / asm_::NS) - 1) & 1, WAIT_CYCLES)))
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
@@ -259,16 +263,16 @@ __global__ void __launch_bounds__(448)
     } else if (lane == 2) {
       // stores of full chunks (a ragged chunk is stored by its epilogue threads)
       tma_prefetch_desc(&maps.dq);
-      tma_prefetch_desc(&maps.dgp);
+      tma_prefetch_desc(&maps.qt);
       for (int j = 0; j < nch; ++j) {
         const int st = j % asm_::NS;
         const int64_t tok0 = s0 + (int64_t)j * C;
         if (!mbar_wait(&out_ready, j & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         if (s1 - tok0 >= C) {
-          for (int x = 0; x < 2; ++x)
+          for (int x = 0; x < 2; ++x) {
             tma_store_3d(&maps.dq, sm + asm_::Q + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
-          for (int x = 0; x < 4; ++x)
-            tma_store_3d(&maps.dgp, sm + asm_::STG + x * 8192, 32 * x, h, (int)tok0);
+            tma_store_3d(&maps.qt, sm + asm_::QT + x * 8192, 64 * x, h, (int)tok0);
+          }
           bulk_commit();
           bulk_wait_read_all();
         }
@@ -285,6 +289,26 @@ __global__ void __launch_bounds__(448)
         mbar_expect_tx(&g_full, 32768);
         for (int x = 0; x < 4; ++x) tma_load_3d(sm + asm_::GT + x * 8192, &maps.g, 32 * x, h, tok, &g_full);
       }
+    } else if (lane == 4) {
+      // kt of each full chunk to the workspace once the prep has written it
+      // (a ragged chunk is stored by the prep threads); the stage is
+      // refilled only after this copy has read it
+      tma_prefetch_desc(&maps.kt);
+      uint32_t ph = 0;
+      for (int j = 0; j < nch; ++j) {
+        const int st = j % asm_::NS;
+        const int64_t tok0 = s0 + (int64_t)j * C;
+        if (!mbar_wait(&prep_done[st], (ph >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        ph ^= 1u << st;
+        if (s1 - tok0 >= C) {
+          for (int x = 0; x < 2; ++x)
+            tma_store_3d(&maps.kt, sm + asm_::K + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&kt_read[st]);
+      }
+      bulk_wait_all();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -332,6 +356,7 @@ __global__ void __launch_bounds__(448)
     const int qw = warp & 3, th = (warp - 2) >> 2;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
+    const int64_t gc0 = unit_chunk0(a.units, un);
     uint32_t ph_full = 0, ph_free = 0, ph_dqf = 0;
     const ColF32 gcol(sbase + asm_::GT, 32 * th, c);
     // iteration j: gate work and kt of chunk j, then the epilogue of chunk j-1
@@ -384,6 +409,14 @@ __global__ void __launch_bounds__(448)
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) sts_u16(kc.at(16 * hb + i), kb[i]);
+            if (L < C) {  // ragged chunk: kt rows < L straight to the workspace
+              const int tb = 32 * th + 16 * hb;
+              float kv[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) kv[i] = bf16_bits_to_f32(kb[i]);
+              transpose_4x4_blocks(kv, lane);
+              store_block_bf16(a.kt + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, kv, lane, tb, L);
+            }
           }
         }
         tmem_st_wait();
@@ -403,8 +436,11 @@ __global__ void __launch_bounds__(448)
         if (!mbar_wait(&dq_full[bb], (ph_dqf >> bb) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_dqf ^= 1u << bb;
         if (!mbar_wait(&qfull[stt], (jj / asm_::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        // the qt staging buffer is free once the previous chunk's stores have read it
+        if (jj >= 1 && !mbar_wait(&stg_free, (jj - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
         const ColBf16 qc(sbase + asm_::Q + stt * 16384, 32 * th, c);
+        const ColBf16 qtc(sbase + asm_::QT, 32 * th, c);
         float sv[32];
         float suf = 0.f;
 #pragma unroll
@@ -418,19 +454,26 @@ __global__ void __launch_bounds__(448)
           for (int i = 0; i < 16; ++i) qb[i] = lds_u16(qc.at(16 * blk + i));
           tmem_ld_wait(acc);
           tmem_ld_wait(eg);
-          float dqv[16];
+          float dqv[16], qtv[16];
 #pragma unroll
           for (int i = 15; i >= 0; --i) {
-            dqv[i] = a.scale * __uint_as_float(eg[i]) * __uint_as_float(acc[i]);
-            if (tb + i < L) suf += bf16_bits_to_f32(qb[i]) * dqv[i];
+            const float sg = a.scale * __uint_as_float(eg[i]);
+            const float qf = bf16_bits_to_f32(qb[i]);
+            dqv[i] = sg * __uint_as_float(acc[i]);
+            qtv[i] = sg * qf;  // qt = scale q exp(G), the gated q of pass B
+            if (tb + i < L) suf += qf * dqv[i];
             sv[16 * blk + i] = suf;
           }
           if (L == C) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) sts_u16(qc.at(16 * blk + i), f32_to_bf16_bits(dqv[i]));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sts_u16(qtc.at(16 * blk + i), f32_to_bf16_bits(qtv[i]));
           } else {
             transpose_4x4_blocks(dqv, lane);
             store_block_bf16(a.dq + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, dqv, lane, tb, L);
+            transpose_4x4_blocks(qtv, lane);
+            store_block_bf16(a.qt + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, qtv, lane, tb, L);
           }
         }
         tc_fence_before();
@@ -438,24 +481,17 @@ __global__ void __launch_bounds__(448)
         // the low half adds the high half's total
         float *xq = reinterpret_cast<float *>(sm + asm_::XQ) + bb * 128;
         if (th == 1) xq[c] = suf;
-        // the staging buffer is free once the previous chunk's stores have read it
-        if (jj >= 1 && !mbar_wait(&stg_free, (jj - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         named_bar(2, 256);
         const float add = th == 0 ? xq[c] : 0.f;
-        if (L == C) {
-          const ColF32 gc(sbase + asm_::STG, 32 * th, c);
+        {
+          // partials in the chunk-slot layout of the scratch: four tokens of
+          // one channel per 16 bytes, [token quad][channel], so each warp
+          // store covers 512 contiguous bytes (read back the same way by pass B)
+          float4 *dst = reinterpret_cast<float4 *>(a.dgp) + ((gc0 + jj) * H + h) * (int64_t)(KD * C / 4) + c;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sts_f32(gc.at(i), sv[i] + add);
-        } else {
-#pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = sv[16 * blk + i] + add;
-            const int tb = 32 * th + 16 * blk;
-            transpose_4x4_blocks(v, lane);
-            store_block_f32(a.dgp + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
-          }
+          for (int i = 0; i < 8; ++i)
+            dst[(8 * th + i) * KD] =
+                make_float4(sv[4 * i] + add, sv[4 * i + 1] + add, sv[4 * i + 2] + add, sv[4 * i + 3] + add);
         }
         fence_async_smem();
         mbar_arrive(&out_ready);
@@ -466,6 +502,7 @@ __global__ void __launch_bounds__(448)
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
+    mask_tile_init(sm + asm_::DP, qw, lane);
     // S (TMEM) = state entering the unit (h0 folded over the document's
     // earlier pieces), bf16 copy (TMEM A operand) for chunk 0's readout
     {
@@ -596,15 +633,15 @@ __global__ void __launch_bounds__(448)
 // pass B
 // ===========================================================================
 namespace bsm {  // shared-memory carve-up (bytes)
-constexpr int NS = 2;
-constexpr uint32_t Q = 0;          // 2 x 16 KB q, then qt in place
-constexpr uint32_t K = 32768;      // 2 x 16 KB k, then kt in place, then dk (store source)
-constexpr uint32_t V = 65536;      // 2 x 16 KB v, then dv (store source)
-constexpr uint32_t DO = 98304;     // 2 x 16 KB
-constexpr uint32_t P = 131072;     // 8 KB masked P  (bf16 [t][s])
-constexpr uint32_t DP = 139264;    // 8 KB masked dP (bf16 [t][s])
-constexpr uint32_t DH = 147456;    // 32 KB dHh (bf16 [c][v])
-constexpr uint32_t DG = 180224;    // 32 KB gate-gradient partials from the dq pass, then dg
+constexpr int NS = 2;               // stages of the qt / do ring
+constexpr int NK = 3;               // stages of the kt / v ring (held until dk / dv are stored)
+constexpr uint32_t Q = 0;          // 2 x 16 KB qt (gated by pass A)
+constexpr uint32_t DO = 32768;     // 2 x 16 KB
+constexpr uint32_t K = 65536;      // 3 x 16 KB kt (gated by pass A), then dk (store source)
+constexpr uint32_t V = 114688;     // 3 x 16 KB v, then dv (store source)
+constexpr uint32_t P = 163840;     // 8 KB masked P  (bf16 [t][s])
+constexpr uint32_t DP = 172032;    // 8 KB masked dP (bf16 [t][s])
+constexpr uint32_t DH = 180224;    // 32 KB dHh (bf16 [c][v])
 constexpr uint32_t XCH = 212992;   // 2 x 2 x 128 fp32 gate products
 constexpr uint32_t XK = 215040;    // 2 x 2 x 128 fp32: token-half totals of k (.) dk
 constexpr uint32_t BND = 217088;   // 2 x 128 fp32: exact gate-gradient carry at checkpoints
@@ -620,9 +657,9 @@ constexpr uint32_t BYTES = 218112;
 __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdArgs &a, unsigned bx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full[bsm::NS], empty[bsm::NS], kfull[bsm::NS], kempty[bsm::NS],
-      prep_done[bsm::NS], out_ready[bsm::NS], pdp_full, pdp_ready, dh_ready, dh_full, kv_full, kv_free,
-      eg_ready[2], eg_free[2], bnd_ready[2], dg_full;
+  __shared__ uint64_t full[bsm::NS], empty[bsm::NS], kfull[bsm::NK], kempty[bsm::NK],
+      prep_done[bsm::NS], out_ready[bsm::NK], pdp_full, pdp_ready, dh_ready, dh_full, kv_full, kv_free,
+      eg_ready[2], eg_free[2], bnd_ready[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -644,9 +681,11 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     for (int i = 0; i < bsm::NS; ++i) {
       mbar_init(&full[i], 1);    // q, do: released by the MMA commit
       mbar_init(&empty[i], 1);
-      mbar_init(&kfull[i], 1);   // k, v (then kt, dk, dv): released by the store thread
-      mbar_init(&kempty[i], 1);
       mbar_init(&prep_done[i], 256);
+    }
+    for (int i = 0; i < bsm::NK; ++i) {
+      mbar_init(&kfull[i], 1);   // kt, v (then dk, dv): released by the store thread
+      mbar_init(&kempty[i], 1);
       mbar_init(&out_ready[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
@@ -660,7 +699,6 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     mbar_init(&dh_full, 1);
     mbar_init(&kv_full, 1);
     mbar_init(&kv_free, 256);
-    mbar_init(&dg_full, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -677,7 +715,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
   if (warp == 0) {
     if (lane == 0) {
       // ring of q, do: released by the MMA commit
-      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.qt);
       tma_prefetch_desc(&maps.dO);
       tma_prefetch_desc(&maps.g);
       for (int i = 0; i < nch; ++i) {
@@ -689,74 +727,53 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         if (j - 2 >= 0) {
           const int tp = tok - 2 * C;
           for (int x = 0; x < 128; x += 64) {
-            tma_prefetch_3d(&maps.q, x, h, tp);
+            tma_prefetch_3d(&maps.qt, x, h, tp);
             tma_prefetch_3d(&maps.dO, x, h, tp);
-            tma_prefetch_3d(&maps.k, x, h, tp);
+            tma_prefetch_3d(&maps.kt, x, h, tp);
             tma_prefetch_3d(&maps.v, x, h, tp);
           }
-          for (int x = 0; x < 128; x += 32) {
-            tma_prefetch_3d(&maps.g, x, h, tp);
-            tma_prefetch_3d(&maps.dgp, x, h, tp);
-          }
+          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
         }
         mbar_expect_tx(&full[st], 2 * 16384);
         for (int x = 0; x < 2; ++x) {
-          tma_load_3d(sm + bsm::Q + st * 16384 + x * 8192, &maps.q, 64 * x, h, tok, &full[st]);
+          tma_load_3d(sm + bsm::Q + st * 16384 + x * 8192, &maps.qt, 64 * x, h, tok, &full[st]);
           tma_load_3d(sm + bsm::DO + st * 16384 + x * 8192, &maps.dO, 64 * x, h, tok, &full[st]);
         }
       }
     } else if (lane == 1) {
       // ring of k and v: released once dk and dv (written over them) are stored
-      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.kt);
       tma_prefetch_desc(&maps.v);
       for (int i = 0; i < nch; ++i) {
-        const int j = nch - 1 - i, st = i % bsm::NS;
-        if (i >= bsm::NS && !mbar_wait(&kempty[st], ((i / bsm::NS) - 1) & 1, WAIT_CYCLES))
+        const int j = nch - 1 - i, st = i % bsm::NK;
+        if (i >= bsm::NK && !mbar_wait(&kempty[st], ((i / bsm::NK) - 1) & 1, WAIT_CYCLES))
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
         mbar_expect_tx(&kfull[st], 2 * 16384);
         for (int x = 0; x < 2; ++x) {
-          tma_load_3d(sm + bsm::K + st * 16384 + x * 8192, &maps.k, 64 * x, h, tok, &kfull[st]);
+          tma_load_3d(sm + bsm::K + st * 16384 + x * 8192, &maps.kt, 64 * x, h, tok, &kfull[st]);
           tma_load_3d(sm + bsm::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &kfull[st]);
         }
       }
     } else if (lane == 2) {
-      // gate-gradient partials in, dk / dv / dg of full chunks out (a ragged
-      // chunk is stored by its epilogue threads)
-      tma_prefetch_desc(&maps.dgp);
+      // dk / dv of full chunks out (a ragged chunk is stored by its epilogue
+      // threads); the kt / v stage is refilled once they have been read
       tma_prefetch_desc(&maps.dk);
       tma_prefetch_desc(&maps.dv);
-      tma_prefetch_desc(&maps.dg);
-      if (nch > 0) {
-        mbar_expect_tx(&dg_full, 32768);
-        for (int x = 0; x < 4; ++x)
-          tma_load_3d(sm + bsm::DG + x * 8192, &maps.dgp, 32 * x, h, (int)(s0 + (int64_t)(nch - 1) * C),
-                      &dg_full);
-      }
       for (int i = 0; i < nch; ++i) {
-        const int j = nch - 1 - i, st = i % bsm::NS;
+        const int j = nch - 1 - i, st = i % bsm::NK;
         const int64_t tok0 = s0 + (int64_t)j * C;
-        if (!mbar_wait(&out_ready[st], (i / bsm::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if (!mbar_wait(&out_ready[st], (i / bsm::NK) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         if (s1 - tok0 >= C) {
           for (int x = 0; x < 2; ++x) {
             tma_store_3d(&maps.dk, sm + bsm::K + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
             tma_store_3d(&maps.dv, sm + bsm::V + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
           }
           bulk_commit();
-          for (int x = 0; x < 4; ++x) tma_store_3d(&maps.dg, sm + bsm::DG + x * 8192, 32 * x, h, (int)tok0);
-          bulk_commit();
-          bulk_wait_read_all_but_one();  // the k / v stage can be refilled
-          mbar_arrive(&kempty[st]);
           bulk_wait_read_all();
-        } else {
-          mbar_arrive(&kempty[st]);
         }
-        if (i + 1 < nch) {
-          mbar_expect_tx(&dg_full, 32768);
-          for (int x = 0; x < 4; ++x)
-            tma_load_3d(sm + bsm::DG + x * 8192, &maps.dgp, 32 * x, h, (int)(tok0 - C), &dg_full);
-        }
+        mbar_arrive(&kempty[st]);
       }
       bulk_wait_all();
     }
@@ -770,10 +787,13 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
       uint32_t ph_prep = 0;
       const uint32_t pa = sbase + bsm::P, dpa = sbase + bsm::DP, dha = sbase + bsm::DH;
       for (int i = 0; i < nch; ++i) {
-        const int st = i % bsm::NS;
-        const uint32_t qa = sbase + bsm::Q + st * 16384, kta = sbase + bsm::K + st * 16384;
-        const uint32_t va = sbase + bsm::V + st * 16384, doa = sbase + bsm::DO + st * 16384;
-        if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        const int st = i % bsm::NS, sk = i % bsm::NK;
+        const uint32_t qa = sbase + bsm::Q + st * 16384, kta = sbase + bsm::K + sk * 16384;
+        const uint32_t va = sbase + bsm::V + sk * 16384, doa = sbase + bsm::DO + st * 16384;
+        if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES) ||
+            !mbar_wait(&full[st], (i / bsm::NS) & 1, WAIT_CYCLES) ||
+            !mbar_wait(&kfull[sk], (i / bsm::NK) & 1, WAIT_CYCLES))
+          BW_FAIL_AND_BREAK
         ph_prep ^= 1u << st;
         tc_fence_after();
 #pragma unroll
@@ -811,14 +831,14 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     const int qw = warp & 3, th = (warp - 2) >> 2;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    uint32_t ph_full = 0, ph_free = 0;
+    uint32_t ph_free = 0;
     float carry = a.bvec ? a.bvec[(u * H + h) * KD + c] : 0.f;
     float xn[32];  // gates of the next chunk (in visiting order)
     if (nch > 0) {
       const int64_t tl = s0 + (int64_t)(nch - 1) * C;
       load_gates_to(xn, a.g, tl, H, h, c, th, (int)min((int64_t)C, s1 - tl));
     }
-    // iteration i: qt, kt, exp(-G) of chunk nch-1-i, then the epilogue of the previous one
+    // iteration i: exp(-G) of chunk nch-1-i, then the epilogue of the previous one
     for (int i = 0; i <= nch; ++i) {
       if (i < nch) {
         const int j = nch - 1 - i, st = i % bsm::NS, b = i & 1;
@@ -828,56 +848,43 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
 #pragma unroll
         for (int w = 0; w < 32; ++w) cg.x[w] = xn[w];
         if (j >= 1) load_gates_to(xn, a.g, tok0 - C, H, h, c, th, C);
-        if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        ph_full ^= 1u << st;
         exchange_gates(cg, reinterpret_cast<float *>(sm + bsm::XCH) + b * 256, c, th, L);
         const float inv = __frcp_rn(cg.total);
-        // qt = scale q exp(G) in place
-        {
-          const ColBf16 qc(sbase + bsm::Q + st * 16384, 32 * th, c);
-          float pre = cg.before * a.scale;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            uint16_t qb[16];
-#pragma unroll
-            for (int w = 0; w < 16; ++w) qb[w] = lds_u16(qc.at(16 * hb + w));
-#pragma unroll
-            for (int w = 0; w < 16; ++w) {
-              const int t = 32 * th + 16 * hb + w;
-              pre *= cg.x[16 * hb + w];
-              qb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(qb[w]) * pre : 0.f);
-            }
-#pragma unroll
-            for (int w = 0; w < 16; ++w) sts_u16(qc.at(16 * hb + w), qb[w]);
-          }
-        }
-        // kt = k exp(-G) in place; exp(-G) -> TMEM
+        // exp(-G) -> TMEM for the dk epilogue and the state step (qt and kt
+        // arrive gated from pass A)
         if (i >= 2) {
           if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
           ph_free ^= 1u << b;
         }
-        if (!mbar_wait(&kfull[st], (i / bsm::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
         {
-          const ColBf16 kc(sbase + bsm::K + st * 16384, 32 * th, c);
           float e = cg.after * inv;  // exp(-G_t), walking t downwards
 #pragma unroll
           for (int hb = 1; hb >= 0; --hb) {
             uint32_t r[16];
-            uint16_t kb[16];
-#pragma unroll
-            for (int w = 0; w < 16; ++w) kb[w] = lds_u16(kc.at(16 * hb + w));
 #pragma unroll
             for (int w = 15; w >= 0; --w) {
-              const int t = 32 * th + 16 * hb + w;
               r[w] = __float_as_uint(e);
-              kb[w] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[w]) * e : 0.f);
               e *= cg.x[16 * hb + w];
             }
-#pragma unroll
-            for (int w = 0; w < 16; ++w) sts_u16(kc.at(16 * hb + w), kb[w]);
             tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
           }
+        }
+        if (L < C) {
+          // ragged chunk: the tile rows t >= L hold the next document's
+          // tokens; qt and kt must be zero there
+          const int sk = i % bsm::NK;
+          if (!mbar_wait(&full[st], (i / bsm::NS) & 1, WAIT_CYCLES) ||
+              !mbar_wait(&kfull[sk], (i / bsm::NK) & 1, WAIT_CYCLES))
+            BW_FAIL_AND_BREAK
+          const ColBf16 qc(sbase + bsm::Q + st * 16384, 32 * th, c);
+          const ColBf16 kc(sbase + bsm::K + sk * 16384, 32 * th, c);
+#pragma unroll
+          for (int w = 0; w < 32; ++w)
+            if (32 * th + w >= L) {
+              sts_u16(qc.at(w), 0);
+              sts_u16(kc.at(w), 0);
+            }
         }
         tmem_st_wait();
         fence_async_smem();
@@ -889,12 +896,20 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         // epilogue of chunk jj (visited at ii = i - 1), this thread's half:
         //   dk_t = exp(-G_t) acc_t (channel c),  dv_t (value column c),
         //   dg_t = dgp_t - sum_{r >= t in chunk} k_r dk_r + carry,  k dk = kt acc
-        const int ii = i - 1, jj = nch - 1 - ii, bb = ii & 1, stt = ii % bsm::NS;
+        const int ii = i - 1, jj = nch - 1 - ii, bb = ii & 1, stt = ii % bsm::NK;
         const int64_t tok0 = s0 + (int64_t)jj * C;
         const int L = (int)min((int64_t)C, s1 - tok0);
+        // q (.) dq partials of channel c, this half's tokens (chunk-slot
+        // layout of the scratch written by pass A: [token quad][channel] x 4
+        // tokens), loaded while the products complete; the chunk's total is
+        // the partial at its first token
+        const float *gp = a.dgp + ((gc0 + jj) * H + h) * (int64_t)(KD * C) + 4 * c;
+        float4 qp4[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) qp4[w] = ldg_early4(gp + (8 * th + w) * (4 * KD));
+        const float qtot = ldg_early(gp);
         if (!mbar_wait(&kv_full, ii & 1, WAIT_CYCLES) ||
-            !mbar_wait(&bnd_ready[bb], (ii >> 1) & 1, WAIT_CYCLES) ||
-            !mbar_wait(&dg_full, ii & 1, WAIT_CYCLES))
+            !mbar_wait(&bnd_ready[bb], (ii >> 1) & 1, WAIT_CYCLES))
           BW_FAIL_AND_BREAK
         tc_fence_after();
         // the carry restarts from the exact boundary term at a checkpoint
@@ -903,9 +918,6 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
                               : carry;
         const ColBf16 kc(sbase + bsm::K + stt * 16384, 32 * th, c);
         const ColBf16 vc(sbase + bsm::V + stt * 16384, 32 * th, c);
-        const ColF32 gc(sbase + bsm::DG, 32 * th, c);
-        // the chunk's q (.) dq total is the partial at its first token
-        const float qtot = lds_f32(sbase + bsm::DG + sw128_off_f32(0, c, 64));
         float dgv[32];
         float sk = 0.f;
 #pragma unroll
@@ -917,10 +929,15 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           float qp[16];
           uint16_t kb[16];
 #pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            qp[w] = lds_f32(gc.at(16 * blk + w));
-            kb[w] = lds_u16(kc.at(16 * blk + w));
+          for (int w = 0; w < 4; ++w) {
+            const float4 q4 = qp4[4 * blk + w];
+            qp[4 * w] = q4.x;
+            qp[4 * w + 1] = q4.y;
+            qp[4 * w + 2] = q4.z;
+            qp[4 * w + 3] = q4.w;
           }
+#pragma unroll
+          for (int w = 0; w < 16; ++w) kb[w] = lds_u16(kc.at(16 * blk + w));
           tmem_ld_wait(acc);
           tmem_ld_wait(eg);
           float dkv[16];
@@ -963,19 +980,14 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         named_bar(2, 256);
         const float other = xk[(1 - th) * 128 + c];
         const float off = th == 0 ? other : 0.f;
-        if (L == C) {
 #pragma unroll
-          for (int w = 0; w < 32; ++w) sts_f32(gc.at(w), dgv[w] - off);
-        } else {
+        for (int blk = 0; blk < 2; ++blk) {
+          float v[16];
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
-            float v[16];
-#pragma unroll
-            for (int w = 0; w < 16; ++w) v[w] = dgv[16 * blk + w] - off;
-            const int tb = 32 * th + 16 * blk;
-            transpose_4x4_blocks(v, lane);
-            store_block_f32(a.dg + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
-          }
+          for (int w = 0; w < 16; ++w) v[w] = dgv[16 * blk + w] - off;
+          const int tb = 32 * th + 16 * blk;
+          transpose_4x4_blocks(v, lane);
+          store_block_f32(a.dg + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
         }
         carry = cin + qtot - (sk + other);
         fence_async_smem();
@@ -987,6 +999,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
+    mask_tile_init(sm + bsm::P, qw, lane);
+    mask_tile_init(sm + bsm::DP, qw, lane);
     // dH = state gradient leaving the unit: dht folded over the document's
     // later pieces (0 in dH-only mode)
     {
@@ -1128,12 +1142,12 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
       !make_map(&maps.dO, dO, true, VD, pr.H, BT, 64) ||
-      !make_map(&maps.dgp, dgp, false, KD, pr.H, BT, 32) ||
       !make_map(&maps.dq, dq, true, KD, pr.H, BT, 64) ||
       !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32) ||
       !make_map(&maps.dk, dk, true, KD, pr.H, BT, 64) ||
       !make_map(&maps.dv, dv, true, VD, pr.H, BT, 64) ||
-      !make_map(&maps.dg, dg, false, KD, pr.H, BT, 32))
+      !make_map(&maps.qt, ws + Lo.off_qt, true, KD, pr.H, BT, 64) ||
+      !make_map(&maps.kt, ws + Lo.off_kt, true, KD, pr.H, BT, 64))
     return cudaErrorInvalidValue;
   BwdArgs a;
   memset(&a, 0, sizeof(a));
@@ -1151,6 +1165,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   a.dgp = dgp;
   a.bvec = (float *)(ws + Lo.off_bvec);
   a.ckpt = (float *)(ws + Lo.off_ckpt);
+  a.qt = (__nv_bfloat16 *)(ws + Lo.off_qt);
+  a.kt = (__nv_bfloat16 *)(ws + Lo.off_kt);
   a.err = pr.err;
   const dim3 grid((unsigned)Lo.max_units, (unsigned)pr.H);
   const int smA = asm_::BYTES + 1024, smB = bsm::BYTES + 1024;

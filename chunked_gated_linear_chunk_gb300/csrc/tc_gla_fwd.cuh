@@ -460,8 +460,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        x[i] = (t0 + i < LL) ? __ldg(reinterpret_cast<const float2 *>(gp + (int64_t)i * a.H * KD))
-                             : make_float2(0.f, 0.f);
+        x[i] = (t0 + i < LL) ? ldg_early2(gp + (int64_t)i * a.H * KD) : make_float2(0.f, 0.f);
     };
     if (nch > 0) load_x(0, xn);
     for (int j = 0; j < nch; ++j) {
@@ -517,6 +516,8 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     }
     float decay = 1.f;  // state-only mode: exp(sum of g over the piece)
     if (!STATE_ONLY) {
+      mask_tile_init(sm + fsm::P, qw, lane);
+      mask_tile_init(sm + fsm::P + 8192, qw, lane);
       store_state_bf16(sm + fsm::S + 16384, c, S);
       fence_async_smem();
       mbar_arrive(&s_ready[1]);
@@ -534,24 +535,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       }
       ph_p ^= 1u << b;
       tc_fence_after();
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[16];
-        tmem_ld16(tP + lane_off + cb * 16, r);
-        tmem_ld_wait(r);
-        if (lane < 16) {
-          float x[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] = (cb * 16 + i <= prow) ? __uint_as_float(r[i]) : 0.f;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-            st_shared_v4(smem_u32(sm + fsm::P + b * 8192 + sw128_off(prow, cb * 16 + hb * 8, 64)),
-                         pack_bf16(x[hb * 8 + 0], x[hb * 8 + 1]),
-                         pack_bf16(x[hb * 8 + 2], x[hb * 8 + 3]),
-                         pack_bf16(x[hb * 8 + 4], x[hb * 8 + 5]),
-                         pack_bf16(x[hb * 8 + 6], x[hb * 8 + 7]));
-        }
-      }
+      mask_tile_to_smem(tP, lane_off, qw, lane, sm + fsm::P + b * 8192);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[b]);
@@ -565,12 +549,17 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       tc_fence_after();
       const float eG = reinterpret_cast<const float *>(sm + fsm::GAM)[(j & 3) * 128 + c];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[16];
-        tmem_ld16(tU + lane_off + cb * 16, r);
+      for (int cp = 0; cp < 4; cp += 2) {
+        uint32_t r[16], r2[16];
+        tmem_ld16(tU + lane_off + cp * 16, r);
+        tmem_ld16(tU + lane_off + cp * 16 + 16, r2);
         tmem_ld_wait(r);
+        tmem_tie(r2);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) S[cb * 16 + i] = eG * (S[cb * 16 + i] + __uint_as_float(r[i]));
+        for (int i = 0; i < 16; ++i) {
+          S[cp * 16 + i] = eG * (S[cp * 16 + i] + __uint_as_float(r[i]));
+          S[cp * 16 + 16 + i] = eG * (S[cp * 16 + 16 + i] + __uint_as_float(r2[i]));
+        }
       }
       if (STATE_ONLY) {
         decay *= eG;
@@ -589,20 +578,26 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       ph_o ^= 1u << b;
       tc_fence_after();
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[16];
-        tmem_ld16(tO + lane_off + cb * 16, r);
-        tmem_ld_wait(r);
+      for (int cp = 0; cp < 4; cp += 2) {
+        uint32_t r[2][16];
+        tmem_ld16(tO + lane_off + cp * 16, r[0]);
+        tmem_ld16(tO + lane_off + cp * 16 + 16, r[1]);
+        tmem_ld_wait(r[0]);
+        tmem_tie(r[1]);
         if (lane < 16 && prow < L) {
-          __nv_bfloat16 *dst = a.o + ((tok0 + prow) * H + h) * VD + v0 + cb * 16;
-          st_global_v4(dst, pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1])),
-                       pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3])),
-                       pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5])),
-                       pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7])));
-          st_global_v4(dst + 8, pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9])),
-                       pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11])),
-                       pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13])),
-                       pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15])));
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {
+            __nv_bfloat16 *dst = a.o + ((tok0 + prow) * H + h) * VD + v0 + (cp + hc) * 16;
+            const uint32_t *x = r[hc];
+            st_global_v4(dst, pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                         pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                         pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                         pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+            st_global_v4(dst + 8, pack_bf16(__uint_as_float(x[8]), __uint_as_float(x[9])),
+                         pack_bf16(__uint_as_float(x[10]), __uint_as_float(x[11])),
+                         pack_bf16(__uint_as_float(x[12]), __uint_as_float(x[13])),
+                         pack_bf16(__uint_as_float(x[14]), __uint_as_float(x[15])));
+          }
         }
       }
       tc_fence_before();

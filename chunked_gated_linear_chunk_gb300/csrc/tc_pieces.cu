@@ -106,6 +106,7 @@ TcLayout tc_layout(const glacore_problem *p, bool backward) {
   const size_t state = (size_t)KD * VD * sizeof(float);
   size_t off = 0;
   L.off_units = L.off_L = L.off_D = L.off_Lr = L.off_Dr = L.off_dgp = L.off_bvec = L.off_ckpt = 0;
+  L.off_qt = L.off_kt = 0;
   // chunks of all documents (upper bound) -> checkpoint slots
   const int64_t chunks = p->segment_ids ? (p->B * p->T + C - 1) / C + p->n_seqs
                                         : p->B * ((p->T + C - 1) / C);
@@ -127,12 +128,18 @@ TcLayout tc_layout(const glacore_problem *p, bool backward) {
     }
   }
   if (backward) {
+    // q (.) dq partials per chunk slot (global chunk index), channel-major
     L.off_dgp = off;
-    off = al256(off + (size_t)p->B * p->T * H * KD * sizeof(float));
+    off = al256(off + (size_t)chunks * H * KD * C * sizeof(float));
     L.off_bvec = off;
     off = al256(off + mu * H * KD * sizeof(float));
     L.off_ckpt = off;
     off = al256(off + (size_t)L.ckpt_slots * H * state);
+    // gated operands of pass B, written by pass A: qt = scale q exp(G), kt = k exp(-G)
+    L.off_qt = off;
+    off = al256(off + (size_t)p->B * p->T * H * KD * 2);
+    L.off_kt = off;
+    off = al256(off + (size_t)p->B * p->T * H * KD * 2);
   }
   L.total = off;
   return L;

@@ -262,33 +262,43 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 // 1024-byte aligned).  K-major operands: sbo = distance between 8-row groups
 // along M/N, lbo unused.  MN-major operands: lbo = distance between
 // 64-element blocks along M/N, sbo = distance between 8-row groups along K.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+// Kept as two 32-bit words: the high word depends only on the strides (a
+// constant at every call site) and the start address sits in the low 14
+// bits of the low word, so a descriptor displaced by a fixed byte offset is
+// one 32-bit add (addresses stay below 256 KB, so the field cannot carry).
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  SDesc d;
+  d.lo = ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+  d.hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14)  // bit 46: descriptor version for tcgen05
+         | (2u << 29);                       // bits 61-63: 128-byte swizzle
+  return d;
+}
+__device__ __forceinline__ SDesc operator+(SDesc d, uint32_t bytes) {
+  d.lo += bytes >> 4;
   return d;
 }
 
 // D[tmem] (+)= A * B^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %6, 0;\n"
+      " mov.b64 da, {%1, %2};\n mov.b64 db, {%3, %4};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Same with the A operand in TMEM (row i of A in lane i, K-major, two bf16
 // per 32-bit column: one K-step of 16 is 8 columns).
-__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %5, 0;\n mov.b64 db, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrives once on the mbarrier at the same shared-memory offset in every CTA
