@@ -9,7 +9,7 @@ namespace glacore {
 namespace tc {
 
 template <int MODE>
-__global__ void __launch_bounds__(448)
+__global__ void __launch_bounds__(448, 1)
     gla_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
   gla_fwd_body<MODE>(maps, a, blockIdx.x);
 }

@@ -157,7 +157,7 @@ constexpr uint32_t BYTES = 191488;
 // warp's TMEM quarter, token half th): gate work and kt for chunk j, then
 // the dq / q (.) dq epilogue of chunk j-1 for their half, written to shared
 // memory for the TMA stores.  Warps 10..13 mask dP and scale the state.
-__global__ void __launch_bounds__(448)
+__global__ void __launch_bounds__(448, 1)
     gla_bwd_dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1121,7 +1121,7 @@ __global__ void __launch_bounds__(448)
 // value halves: CTAs x < nfwd the forward state pass (end state and decay of
 // every piece but the last of a document), the rest the reverse pass (state
 // gradient at the start of every piece but the first, from zero at its end).
-__global__ void __launch_bounds__(448)
+__global__ void __launch_bounds__(448, 1)
     gla_piece_pass_kernel(const __grid_constant__ FwdMaps fm, const FwdArgs fa,
                           const __grid_constant__ FwdMaps rm, const FwdArgs ra, unsigned nfwd) {
   if (blockIdx.x < nfwd)

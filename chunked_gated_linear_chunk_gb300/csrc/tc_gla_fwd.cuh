@@ -187,11 +187,18 @@ __device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[1
 // prep_chunk: exp(G_t) by prefix products, exp(Gam - G_t) by suffix
 // products, one exponential per element; the eight token groups exchange
 // their products through xch.
-// rev (reverse state-gradient pass): the tile in the k slot holds q and
-// becomes scale q exp(G - Gam) (prefix products) instead of k exp(-G).
-__device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (&x)[8], float *gam, float *xch,
+// accum (the state-only piece passes): the k-slot tile is scaled for a
+// product accumulated over the whole piece instead of a per-chunk state
+// step: with dec = (dec0, dec1) the decay of the channels over the chunks
+// already visited, it becomes k exp(Gam - G) dec (forward pass, chunks
+// visited last to first: the decay from each token to the piece end), or,
+// when rev, holds q and becomes scale q exp(G) dec (reverse pass, chunks
+// first to last: the decay from the piece start to each token).  Returns
+// exp(Gam) of the two channels.
+__device__ __forceinline__ float2 prep_chunk_pair(uint32_t q, uint32_t k, float2 (&x)[8], float *gam, float *xch,
                                                 int pw, int lane, int rank, int L, float scale, bool with_q,
-                                                bool rev) {
+                                                bool rev, bool accum = false,
+                                                float2 dec = make_float2(1.f, 1.f)) {
   const int c0 = 64 * rank + 2 * lane;
   const int t0 = 8 * pw;
   float p0 = 1.f, p1 = 1.f;
@@ -244,7 +251,7 @@ __device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (
     for (int i = 0; i < 8; ++i) sts_u32(q + off[i], v[i]);
   }
   if (!rev) {
-    float a0 = suf0 * __frcp_rn(T0), a1 = suf1 * __frcp_rn(T1);
+    float a0 = accum ? suf0 * dec.x : suf0 * __frcp_rn(T0), a1 = accum ? suf1 * dec.y : suf1 * __frcp_rn(T1);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
 #pragma unroll
@@ -257,7 +264,8 @@ __device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (
 #pragma unroll
     for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
   } else {
-    float a0 = scale * pre0 * __frcp_rn(T0), a1 = scale * pre1 * __frcp_rn(T1);
+    float a0 = accum ? scale * pre0 * dec.x : scale * pre0 * __frcp_rn(T0),
+          a1 = accum ? scale * pre1 * dec.y : scale * pre1 * __frcp_rn(T1);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
 #pragma unroll
@@ -270,10 +278,11 @@ __device__ __forceinline__ void prep_chunk_pair(uint32_t q, uint32_t k, float2 (
 #pragma unroll
     for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
   }
-  if (pw == 0) {
+  if (pw == 0 && !accum) {
     gam[c0] = T0;
     gam[c0 + 1] = T1;
   }
+  return make_float2(T0, T1);
 }
 
 __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float (&S)[64]) {
@@ -284,10 +293,15 @@ __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float
                  pack_bf16(S[n + 6], S[n + 7]));
 }
 
-// STATE_ONLY (MODE != FWD_MAIN): the piece passes of the exact sequence split -- only the state
-// recurrence from a zero state (no q, no output); writes the piece's end
-// state and its total decay.  Pieces that end their document have nothing
-// to contribute and exit.
+// STATE_ONLY (MODE != FWD_MAIN): the piece passes of the exact sequence
+// split -- the piece's end state from a zero state (no q, no output) and its
+// total decay.  Unrolled over the piece, that state is one product
+//   L = sum_t diag(exp(sum of g after t in the piece)) k_t v_t^T = Khat^T V,
+// so each chunk's k is scaled by its decay to the piece end (chunks visited
+// last to first, the decay of the visited chunks carried per channel) and
+// its product accumulates in TMEM: no per-chunk state step.  The reverse pass
+// likewise accumulates scale q exp(prefix of g from the piece start) times do.
+// Pieces that end their document have nothing to contribute and exit.
 template <int MODE>
 __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs &a, unsigned bx) {
   constexpr bool STATE_ONLY = MODE != FWD_MAIN;
@@ -313,8 +327,9 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   // piece, the reverse pass nothing from its first
   const bool idle = STATE_ONLY && (REV ? un.piece == 0 : last_piece);
   const int nch = idle ? 0 : (int)((s1 - s0 + C - 1) / C);
-  // chunk visited at iteration j (the reverse pass walks backwards)
-  auto chunk_tok = [&](int j) -> int64_t { return s0 + (int64_t)(REV ? nch - 1 - j : j) * C; };
+  // chunk visited at iteration j (the forward state pass walks backwards)
+  constexpr bool BACK = MODE == FWD_STATE;
+  auto chunk_tok = [&](int j) -> int64_t { return s0 + (int64_t)(BACK ? nch - 1 - j : j) * C; };
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -404,18 +419,13 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         }
         ph_prep ^= 1u << st;
         if (STATE_ONLY) {
-          // the epilogue has folded chunk j-1 into S (so U[b] is free, and the
-          // gate products of chunk j-1 are read before the prep, which runs
-          // at most NS chunks ahead of this commit, reuses their buffer)
-          if (j >= 1) {
-            if (!mbar_wait(&s_ready[b ^ 1], (ph_sr >> (b ^ 1)) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
-            ph_sr ^= 1u << (b ^ 1);
-          }
+          // one accumulator over the whole piece (U[0])
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) mma_bf16(tU, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, ks);
-          mma_commit(&u_full[b]);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tbase + 128, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, (j > 0 || ks > 0) ? 1u : 0u);
           mma_commit_multicast(&empty[st], 3);
+          if (j == nch - 1) mma_commit(&u_full[0]);
           continue;
         }
         tc_fence_after();
@@ -452,6 +462,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     const int c0 = 64 * vb + 2 * lane, t0 = 8 * pw;
     const uint32_t rem = mapa_shared(sbase, peer);  // the peer's tiles
     uint32_t ph_full = 0;
+    float2 dec = make_float2(1.f, 1.f);  // state-only: decay of the channels over the visited chunks
     // gates of chunk j+1 are loaded into registers while chunk j is prepared
     float2 xn[8];
     auto load_x = [&](int jj, float2 (&x)[8]) {
@@ -476,10 +487,14 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       // this CTA's 64-column block of q, k and its gate totals (byte offsets)
       const uint32_t qo = fsm::Q + s * 16384 + vb * 8192, ko = fsm::K + s * 16384 + vb * 8192,
                      go = fsm::GAM + (j & 3) * 512 + vb * 256;
-      prep_chunk_pair(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
+      const float2 tot = prep_chunk_pair(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
                       reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
                       reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 1024, pw, lane, vb, L, a.scale,
-                      !STATE_ONLY, REV);
+                      !STATE_ONLY, REV, STATE_ONLY, dec);
+      if (STATE_ONLY) {
+        dec.x *= tot.x;
+        dec.y *= tot.y;
+      }
       fence_async_smem();
       // copy the prepared blocks into the peer's tiles (bulk copies that
       // complete on the peer's barriers; one arrive there stands for the
@@ -491,11 +506,18 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         mbar_arrive_expect_tx_cluster(pbar, STATE_ONLY ? 8192u : 16384u);
         if (!STATE_ONLY) bulk_copy_to_cluster(rem + qo, sbase + qo, 8192, pbar);
         bulk_copy_to_cluster(rem + ko, sbase + ko, 8192, pbar);
-        mbar_arrive_expect_tx_cluster(gbar, 256u);
-        bulk_copy_to_cluster(rem + go, sbase + go, 256, gbar);
+        if (!STATE_ONLY) {
+          mbar_arrive_expect_tx_cluster(gbar, 256u);
+          bulk_copy_to_cluster(rem + go, sbase + go, 256, gbar);
+        }
       }
       mbar_arrive(&prep_done[s]);
-      mbar_arrive(&gam_ready[j & 3]);
+      if (!STATE_ONLY) mbar_arrive(&gam_ready[j & 3]);
+    }
+    // state-only: the piece's total decay of this CTA's 64 channels
+    if (STATE_ONLY && nch > 0 && pw == 0 && !*abortp) {
+      a.dbuf[(u * a.H + h) * KD + c0] = dec.x;
+      a.dbuf[(u * a.H + h) * KD + c0 + 1] = dec.y;
     }
   } else {
     // ---------------- epilogue warpgroup ----------------
@@ -514,7 +536,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
       piece_state_in<64>(S, h0row, a.lbuf, a.dbuf, u - un.piece, un.piece, H, h, c, v0);
     }
-    float decay = 1.f;  // state-only mode: exp(sum of g over the piece)
     if (!STATE_ONLY) {
       mask_tile_init(sm + fsm::P, qw, lane);
       mask_tile_init(sm + fsm::P + 8192, qw, lane);
@@ -523,7 +544,28 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       mbar_arrive(&s_ready[1]);
     }
     uint32_t ph_p = 0, ph_u = 0, ph_o = 0;
-    for (int j = 0; j < nch; ++j) {
+    if (STATE_ONLY && nch > 0) {
+      // the piece's accumulated product is its end state
+      if (mbar_wait(&u_full[0], 0, WAIT_CYCLES)) {
+        tc_fence_after();
+#pragma unroll
+        for (int cp = 0; cp < 4; cp += 2) {
+          uint32_t r[16], r2[16];
+          tmem_ld16(tbase + 128 + lane_off + cp * 16, r);
+          tmem_ld16(tbase + 128 + lane_off + cp * 16 + 16, r2);
+          tmem_ld_wait(r);
+          tmem_tie(r2);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            S[cp * 16 + i] = __uint_as_float(r[i]);
+            S[cp * 16 + 16 + i] = __uint_as_float(r2[i]);
+          }
+        }
+      } else {
+        atomicExch(&abort_flag, 1);
+      }
+    }
+    for (int j = 0; j < (STATE_ONLY ? 0 : nch); ++j) {
       const int b = j & 1;
       const int64_t tok0 = chunk_tok(j);
       const int L = (int)min((int64_t)C, s1 - tok0);
@@ -560,12 +602,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
           S[cp * 16 + i] = eG * (S[cp * 16 + i] + __uint_as_float(r[i]));
           S[cp * 16 + 16 + i] = eG * (S[cp * 16 + 16 + i] + __uint_as_float(r2[i]));
         }
-      }
-      if (STATE_ONLY) {
-        decay *= eG;
-        tc_fence_before();
-        mbar_arrive(&s_ready[b]);
-        continue;
       }
       store_state_bf16(sm + fsm::S + b * 16384, c, S);
       fence_async_smem();
@@ -605,7 +641,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     float *dst = nullptr;
     if (STATE_ONLY && nch > 0) {
       dst = a.lbuf + ((u * H + h) * KD + c) * VD + v0;
-      if (vb == 0) a.dbuf[(u * H + h) * KD + c] = decay;
     } else if (!STATE_ONLY && a.ht && last_piece) {
       dst = a.ht + ((d * H + h) * KD + c) * VD + v0;
     }
