@@ -115,6 +115,14 @@ inline cudaError_t launch_pairs(void (*kernel)(Params...), dim3 grid, int smem, 
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+struct FwdMaps;
+struct FwdArgs;
+// The piece passes of the exact sequence split (tc_pieces.cu): the forward
+// pass (local end state and total decay of every piece but the last of its
+// document) and, when rm / ra are given, the reverse pass (local state
+// gradient at the start of every piece but the first) in one launch.
+cudaError_t launch_piece_states(const FwdMaps &fm, const FwdArgs &fa, const FwdMaps *rm, const FwdArgs *ra,
+                                int64_t units, int64_t H, cudaStream_t st);
 cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void *o, float *ht,
                 char *ws, cudaStream_t st);
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,

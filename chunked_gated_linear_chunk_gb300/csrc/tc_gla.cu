@@ -51,8 +51,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   a.err = pr.err;
   const int smem = fsm::BYTES + 1024;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gla_fwd_kernel<FWD_MAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(gla_fwd_kernel<FWD_STATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(gla_fwd_kernel<FWD_MAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const dim3 grid((unsigned)(2 * Lo.max_units), (unsigned)pr.H);
   if (Lo.pieces) {
@@ -63,8 +62,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
     a.dbuf = (float *)(ws + Lo.off_D);
     FwdArgs as = a;
     as.ht = nullptr;
-    if ((e = launch_pairs(gla_fwd_kernel<FWD_STATE>, grid, smem, st, maps, as)) != cudaSuccess) return e;
-    mark_launch("gla_fwd_piece_state_kernel", st);
+    if ((e = launch_piece_states(maps, as, nullptr, nullptr, Lo.max_units, pr.H, st)) != cudaSuccess) return e;
   }
   if ((e = launch_pairs(gla_fwd_kernel<FWD_MAIN>, grid, smem, st, maps, a)) != cudaSuccess) return e;
   mark_launch("gla_fwd_kernel", st);

@@ -1116,20 +1116,6 @@ __global__ void __launch_bounds__(448)
   gla_bwd_rev_body(maps, a, blockIdx.x);
 }
 
-// The two piece passes of the exact sequence split in one launch (they are
-// independent), both modes of the forward kernel body in clusters of two
-// value halves: CTAs x < nfwd the forward state pass (end state and decay of
-// every piece but the last of a document), the rest the reverse pass (state
-// gradient at the start of every piece but the first, from zero at its end).
-__global__ void __launch_bounds__(448, 1)
-    gla_piece_pass_kernel(const __grid_constant__ FwdMaps fm, const FwdArgs fa,
-                          const __grid_constant__ FwdMaps rm, const FwdArgs ra, unsigned nfwd) {
-  if (blockIdx.x < nfwd)
-    gla_fwd_body<FWD_STATE>(fm, fa, blockIdx.x);
-  else
-    gla_fwd_body<REV_STATE>(rm, ra, blockIdx.x - nfwd);
-}
-
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,
                 const float *dht, void *dq, void *dk, void *dv, float *dg, float *dh0, char *ws,
                 cudaStream_t st) {
@@ -1203,15 +1189,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     fa.dbuf = (float *)(ws + Lo.off_D);
     ra.lbuf = (float *)(ws + Lo.off_Lr);
     ra.dbuf = (float *)(ws + Lo.off_Dr);
-    const int smP = fsm::BYTES + 1024;
-    if ((e = cudaFuncSetAttribute(gla_piece_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smP)) !=
-        cudaSuccess)
-      return e;
-    const unsigned nfwd = (unsigned)(2 * Lo.max_units);
-    if ((e = launch_pairs(gla_piece_pass_kernel, dim3(2 * nfwd, (unsigned)pr.H), smP, st, fm, fa, rm, ra, nfwd)) !=
-        cudaSuccess)
-      return e;
-    mark_launch("gla_piece_pass_kernel", st);
+    if ((e = launch_piece_states(fm, fa, &rm, &ra, Lo.max_units, pr.H, st)) != cudaSuccess) return e;
   }
   gla_bwd_dq_kernel<<<grid, 448, smA, st>>>(maps, a);
   mark_launch("gla_bwd_dq_kernel", st);

@@ -16,7 +16,7 @@
 // tc.cuh); the local states come from state-only modes of the forward and
 // reverse kernels.  This file builds the unit table of packed documents and
 // sizes the workspace.
-#include "tc.cuh"
+#include "tc_gla_fwd.cuh"
 
 namespace glacore {
 namespace tc {
@@ -67,6 +67,232 @@ cudaError_t launch_build_units(const Docs &docs, int64_t plen, Unit *units, int6
                                cudaStream_t st) {
   build_units_kernel<<<1, 1024, 0, st>>>(docs, plen, units, max_units);
   mark_launch("build_units", st);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// The piece passes.  Unrolled over a piece, its local end state is one
+// product, L = sum_t diag(exp(sum of g after t in the piece)) k_t v_t^T =
+// Khat^T V (and the reverse pass's state gradient at the piece start is
+// sum_t diag(exp(sum of g from the piece start to t)) scale q_t do_t^T), so
+// each chunk's k (q) is scaled by its decay to the piece end (from the piece
+// start) and its product accumulates in TMEM: no per-chunk state step.
+// One CTA per (unit, head, key-channel half kb) accumulates
+//   L[kb rows]^T = V^T khat[:, kb]      (128 value lanes x 64 channel columns)
+// so no CTA needs another's prepared tile.  320 threads, about 100 KB of
+// shared memory and 64 TMEM columns: two CTAs share an SM.
+//   warp 0     TMA: the kb block of k (q) and all of v (do), 4-stage ring;
+//              L2 prefetch of the gates two chunks ahead
+//   warp 1     TMEM owner and MMA issuer
+//   warps 2..9 prep (gates straight from L2, prefix / suffix products, the
+//              kb block scaled in place), then the store of L and of the
+//              piece's total decay of their channels
+// ---------------------------------------------------------------------------
+namespace psm {
+constexpr int NS = 4;
+constexpr uint32_t K = 0;         // 4 x 8 KB: the kb column block of k (q), gated in place
+constexpr uint32_t V = 32768;     // 4 x 16 KB: v (do), 128 columns
+constexpr uint32_t XCH = 98304;   // 2 x 8 x 128 fp32 eighth-chunk gate products
+constexpr uint32_t BYTES = 106496;
+}  // namespace psm
+
+// bx: CTA index of the pass (2 per unit).  With uniform rows (implicit
+// units, npr pieces per row) only the units that contribute are launched:
+// CTA pair w is piece w % (npr - 1) (+1 for the reverse pass) of row
+// w / (npr - 1); with a unit table (npr = 0) every unit is launched and the
+// ones with nothing to contribute exit.
+template <bool REV>
+__device__ __forceinline__ void piece_state_body(const FwdMaps &maps, const FwdArgs &a, unsigned bx, int npr) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[psm::NS], empty[psm::NS], prep_done[psm::NS], u_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = bx & 1, h = blockIdx.y;
+  const int64_t w = bx >> 1;
+  const int64_t u = npr > 1 ? (w / (npr - 1)) * npr + w % (npr - 1) + (REV ? 1 : 0) : w;
+  const Unit un = a.units.get(u);
+  const int64_t s0 = un.start, s1 = un.end;
+  // the forward pass has nothing to hand on from a document's last piece,
+  // the reverse pass nothing from its first
+  if (REV ? un.piece == 0 : un.piece == un.npieces - 1) return;
+  const int nch = (int)((s1 - s0 + C - 1) / C);
+  if (nch <= 0) return;
+  // forward pass: chunks last to first (decay to the piece end); reverse: first to last
+  auto chunk_tok = [&](int j) -> int64_t { return s0 + (int64_t)(REV ? j : nch - 1 - j) * C; };
+
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, 64);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < psm::NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&prep_done[i], 256);
+    }
+    mbar_init(&u_done, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  const uint32_t sbase = smem_u32(sm);
+  volatile int *abortp = &abort_flag;
+#define PS_FAIL_AND_BREAK       \
+  {                             \
+    atomicExch(&abort_flag, 1); \
+    break;                      \
+  }
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.g);
+      for (int j = 0; j < nch; ++j) {
+        const int s = j % psm::NS;
+        if (j >= psm::NS && !mbar_wait(&empty[s], ((j / psm::NS) - 1) & 1, WAIT_CYCLES)) PS_FAIL_AND_BREAK
+        if (*abortp) break;
+        const int tok = (int)chunk_tok(j);
+        for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
+          const int tp = (int)chunk_tok(jp);
+          tma_prefetch_3d(&maps.g, 64 * kb, h, tp);
+          tma_prefetch_3d(&maps.g, 64 * kb + 32, h, tp);
+        }
+        mbar_expect_tx(&full[s], 8192 + 16384);
+        tma_load_3d(sm + psm::K + s * 8192, &maps.k, 64 * kb, h, tok, &full[s]);
+        tma_load_3d(sm + psm::V + s * 16384, &maps.v, 0, h, tok, &full[s]);
+        tma_load_3d(sm + psm::V + s * 16384 + 8192, &maps.v, 64, h, tok, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idU = idesc_bf16(128, 64, true, true);
+      uint32_t ph = 0;
+      for (int j = 0; j < nch; ++j) {
+        const int s = j % psm::NS;
+        if (!mbar_wait(&prep_done[s], (ph >> s) & 1, WAIT_CYCLES)) PS_FAIL_AND_BREAK
+        ph ^= 1u << s;
+        tc_fence_after();
+        const uint32_t ka = sbase + psm::K + s * 8192, va = sbase + psm::V + s * 16384;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tbase, mdesc(va, ks, 8192), mdesc(ka, ks, 8192), idU, (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+        if (j == nch - 1) mma_commit(&u_done);
+      }
+      // the last commits have landed before the CTA leaves
+      for (int j = max(0, nch - psm::NS); j < nch && !*abortp; ++j)
+        if (!mbar_wait(&empty[j % psm::NS], (j / psm::NS) & 1, WAIT_CYCLES)) atomicExch(&abort_flag, 1);
+    }
+  } else {
+    // prep warps: channels c0, c0 + 1 of this CTA's half, tokens 8 pw .. 8 pw + 7
+    const int pw = warp - 2;
+    const int c0 = 64 * kb + 2 * lane, t0 = 8 * pw;
+    uint32_t ph_full = 0;
+    float2 dec = make_float2(1.f, 1.f);  // decay of the channels over the visited chunks
+    float2 xn[8];
+    auto load_x = [&](int jj, float2 (&x)[8]) {
+      const int64_t tk = chunk_tok(jj);
+      const int LL = (int)min((int64_t)C, s1 - tk);
+      const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        x[i] = (t0 + i < LL) ? ldg_early2(gp + (int64_t)i * a.H * KD) : make_float2(0.f, 0.f);
+    };
+    load_x(0, xn);
+    for (int j = 0; j < nch; ++j) {
+      const int s = j % psm::NS;
+      const int L = (int)min((int64_t)C, s1 - chunk_tok(j));
+      float2 x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = xn[i];
+      if (j + 1 < nch) load_x(j + 1, xn);
+      // on a failed wait the warps still pass the named barrier inside the
+      // prep (all eight must), with the abort recorded
+      if (!mbar_wait(&full[s], (ph_full >> s) & 1, WAIT_CYCLES)) atomicExch(&abort_flag, 1);
+      ph_full ^= 1u << s;
+      // the kb block sits in an 8 KB slot: pass the tile base one block lower for kb = 1
+      const uint32_t kt = sbase + psm::K + s * 8192 - (uint32_t)kb * 8192u;
+      const float2 tot = prep_chunk_pair(kt, kt, x, nullptr, reinterpret_cast<float *>(sm + psm::XCH) + (j & 1) * 1024,
+                                         pw, lane, kb, L, a.scale, false, REV, true, dec);
+      dec.x *= tot.x;
+      dec.y *= tot.y;
+      fence_async_smem();
+      mbar_arrive(&prep_done[s]);
+    }
+    if (pw == 0 && !*abortp) {
+      a.dbuf[(u * a.H + h) * KD + c0] = dec.x;
+      a.dbuf[(u * a.H + h) * KD + c0 + 1] = dec.y;
+    }
+    // L^T in TMEM: lane = value column v, column = channel 64 kb + col.  Warps
+    // of the same lane quarter split the 64 columns.
+    const int v = 32 * (warp & 3) + lane, half = (warp - 2) >> 2;
+    const bool done = mbar_wait(&u_done, 0, WAIT_CYCLES);
+    __syncwarp();
+    if (done) {
+      tc_fence_after();
+      uint32_t r[16], r2[16];
+      const uint32_t ta = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * half;
+      tmem_ld16(ta, r);
+      tmem_ld16(ta + 16, r2);
+      tmem_ld_wait(r);
+      tmem_tie(r2);
+      if (!*abortp) {
+        float *dst = a.lbuf + ((u * a.H + h) * KD + 64 * kb + 32 * half) * VD + v;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          dst[(int64_t)i * VD] = __uint_as_float(r[i]);
+          dst[(int64_t)(16 + i) * VD] = __uint_as_float(r2[i]);
+        }
+      }
+    } else {
+      atomicExch(&abort_flag, 1);
+    }
+  }
+#undef PS_FAIL_AND_BREAK
+  tc_fence_before();
+  __syncthreads();
+  if (*abortp && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_TIMEOUT);
+  if (warp == 1) tmem_dealloc(tbase, 64);
+}
+
+// CTAs x < nfwd: forward piece pass (key half x % 2); the rest the reverse
+// piece pass (x - nfwd likewise).
+__global__ void __launch_bounds__(320, 2)
+    piece_state_kernel(const __grid_constant__ FwdMaps fm, const FwdArgs fa, const __grid_constant__ FwdMaps rm,
+                       const FwdArgs ra, unsigned nfwd, int npr) {
+  if (blockIdx.x < nfwd)
+    piece_state_body<false>(fm, fa, blockIdx.x, npr);
+  else
+    piece_state_body<true>(rm, ra, blockIdx.x - nfwd, npr);
+}
+
+cudaError_t launch_piece_states(const FwdMaps &fm, const FwdArgs &fa, const FwdMaps *rm, const FwdArgs *ra,
+                                int64_t units, int64_t H, cudaStream_t st) {
+  const int smem = psm::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(piece_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // all of the unified L1 / shared memory as shared memory, so that two CTAs fit on an SM
+  e = cudaFuncSetAttribute(piece_state_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  // uniform rows: launch only the npr - 1 contributing pieces of each row
+  int npr = 0;
+  int64_t work = units;
+  if (!fa.units.table && fa.units.plen > 0) {
+    npr = (int)((fa.units.docs.T + fa.units.plen - 1) / fa.units.plen);
+    work = (units / npr) * (npr - 1);
+  }
+  if (work <= 0) return cudaSuccess;
+  const unsigned nfwd = (unsigned)(2 * work);
+  const dim3 grid(rm ? 2 * nfwd : nfwd, (unsigned)H);
+  piece_state_kernel<<<grid, 320, smem, st>>>(fm, fa, rm ? *rm : fm, ra ? *ra : fa, nfwd, npr);
+  mark_launch("piece_state_kernel", st);
   return cudaGetLastError();
 }
 
