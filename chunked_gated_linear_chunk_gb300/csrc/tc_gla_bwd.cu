@@ -844,6 +844,9 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         const int j = nch - 1 - i, st = i % bsm::NS, b = i & 1;
         const int64_t tok0 = s0 + (int64_t)j * C;
         const int L = (int)min((int64_t)C, s1 - tok0);
+        // the q (.) dq partials of this chunk (read by its epilogue in the
+        // next iteration) into L2: 32 KB, one 128-byte line per thread
+        prefetch_l2(a.dgp + ((gc0 + j) * H + h) * (int64_t)(KD * C) + (th * 128 + c) * 32);
         ChanGate cg;
 #pragma unroll
         for (int w = 0; w < 32; ++w) cg.x[w] = xn[w];
@@ -980,14 +983,13 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         named_bar(2, 256);
         const float other = xk[(1 - th) * 128 + c];
         const float off = th == 0 ? other : 0.f;
+        {
+          // channel c of token t: each warp store covers one token's 32
+          // consecutive channels (128 contiguous bytes)
+          float *dgc = a.dg + ((tok0 + 32 * th) * H + h) * KD + c;
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          float v[16];
-#pragma unroll
-          for (int w = 0; w < 16; ++w) v[w] = dgv[16 * blk + w] - off;
-          const int tb = 32 * th + 16 * blk;
-          transpose_4x4_blocks(v, lane);
-          store_block_f32(a.dg + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, v, lane, tb, L);
+          for (int w = 0; w < 32; ++w)
+            if (32 * th + w < L) dgc[(int64_t)w * H * KD] = dgv[w] - off;
         }
         carry = cin + qtot - (sk + other);
         fence_async_smem();
