@@ -53,6 +53,7 @@ struct BwdArgs {
                          // starts from zero at their ends, [units,H,K] decays
   float *ckpt;   // [slots,H,K,V] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
   __nv_bfloat16 *qt, *kt;  // scratch [BT, H, K]: gated q and k (pass A -> pass B)
+  float *eng;    // scratch [chunk slots, H, C/4, K, 4] fp32: exp(-G) (pass A -> pass B)
   int *err;
 };
 
@@ -401,14 +402,23 @@ __global__ void __launch_bounds__(448, 1)
             uint16_t kb[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) kb[i] = lds_u16(kc.at(16 * hb + i));
+            float en[16];  // exp(-G_t)
 #pragma unroll
             for (int i = 15; i >= 0; --i) {
               const int t = 32 * th + 16 * hb + i;
+              en[i] = sc;
               kb[i] = f32_to_bf16_bits(t < L ? bf16_bits_to_f32(kb[i]) * sc : 0.f);
               sc *= cg.x[16 * hb + i];
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) sts_u16(kc.at(16 * hb + i), kb[i]);
+            {
+              // exp(-G) for pass B, chunk-slot layout as the partials
+              float4 *dst = reinterpret_cast<float4 *>(a.eng) + ((gc0 + j) * H + h) * (int64_t)(KD * C / 4) + c;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[(8 * th + 4 * hb + q) * KD] = make_float4(en[4 * q], en[4 * q + 1], en[4 * q + 2], en[4 * q + 3]);
+            }
             if (L < C) {  // ragged chunk: kt rows < L straight to the workspace
               const int tb = 32 * th + 16 * hb;
               float kv[16];
@@ -642,7 +652,6 @@ constexpr uint32_t V = 114688;     // 3 x 16 KB v, then dv (store source)
 constexpr uint32_t P = 163840;     // 8 KB masked P  (bf16 [t][s])
 constexpr uint32_t DP = 172032;    // 8 KB masked dP (bf16 [t][s])
 constexpr uint32_t DH = 180224;    // 32 KB dHh (bf16 [c][v])
-constexpr uint32_t XCH = 212992;   // 2 x 2 x 128 fp32 gate products
 constexpr uint32_t XK = 215040;    // 2 x 2 x 128 fp32: token-half totals of k (.) dk
 constexpr uint32_t BND = 217088;   // 2 x 128 fp32: exact gate-gradient carry at checkpoints
 constexpr uint32_t BYTES = 218112;
@@ -732,7 +741,6 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
             tma_prefetch_3d(&maps.kt, x, h, tp);
             tma_prefetch_3d(&maps.v, x, h, tp);
           }
-          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
         }
         mbar_expect_tx(&full[st], 2 * 16384);
         for (int x = 0; x < 2; ++x) {
@@ -833,11 +841,15 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     uint32_t ph_free = 0;
     float carry = a.bvec ? a.bvec[(u * H + h) * KD + c] : 0.f;
-    float xn[32];  // gates of the next chunk (in visiting order)
-    if (nch > 0) {
-      const int64_t tl = s0 + (int64_t)(nch - 1) * C;
-      load_gates_to(xn, a.g, tl, H, h, c, th, (int)min((int64_t)C, s1 - tl));
-    }
+    // exp(-G) of the next chunk (in visiting order), this half's tokens, as
+    // written by pass A (chunk-slot layout: [token quad][channel] x 4)
+    float4 en4[8];
+    auto load_en = [&](int jj) {
+      const float *ep = a.eng + ((gc0 + jj) * H + h) * (int64_t)(KD * C) + 4 * c;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) en4[w] = ldg_early4(ep + (8 * th + w) * (4 * KD));
+    };
+    if (nch > 0) load_en(nch - 1);
     // iteration i: exp(-G) of chunk nch-1-i, then the epilogue of the previous one
     for (int i = 0; i <= nch; ++i) {
       if (i < nch) {
@@ -847,31 +859,28 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         // the q (.) dq partials of this chunk (read by its epilogue in the
         // next iteration) into L2: 32 KB, one 128-byte line per thread
         prefetch_l2(a.dgp + ((gc0 + j) * H + h) * (int64_t)(KD * C) + (th * 128 + c) * 32);
-        ChanGate cg;
+        float4 e4[8];
 #pragma unroll
-        for (int w = 0; w < 32; ++w) cg.x[w] = xn[w];
-        if (j >= 1) load_gates_to(xn, a.g, tok0 - C, H, h, c, th, C);
-        exchange_gates(cg, reinterpret_cast<float *>(sm + bsm::XCH) + b * 256, c, th, L);
-        const float inv = __frcp_rn(cg.total);
-        // exp(-G) -> TMEM for the dk epilogue and the state step (qt and kt
-        // arrive gated from pass A)
+        for (int w = 0; w < 8; ++w) e4[w] = en4[w];
+        if (j >= 1) load_en(j - 1);
+        // exp(-G) -> TMEM for the dk epilogue and the state step
         if (i >= 2) {
           if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
           ph_free ^= 1u << b;
         }
         tc_fence_after();
-        {
-          float e = cg.after * inv;  // exp(-G_t), walking t downwards
 #pragma unroll
-          for (int hb = 1; hb >= 0; --hb) {
-            uint32_t r[16];
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t r[16];
 #pragma unroll
-            for (int w = 15; w >= 0; --w) {
-              r[w] = __float_as_uint(e);
-              e *= cg.x[16 * hb + w];
-            }
-            tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
+          for (int q = 0; q < 4; ++q) {
+            const float4 e = e4[4 * hb + q];
+            r[4 * q] = __float_as_uint(e.x);
+            r[4 * q + 1] = __float_as_uint(e.y);
+            r[4 * q + 2] = __float_as_uint(e.z);
+            r[4 * q + 3] = __float_as_uint(e.w);
           }
+          tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
         }
         if (L < C) {
           // ragged chunk: the tile rows t >= L hold the next document's
@@ -1154,6 +1163,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   a.bvec = (float *)(ws + Lo.off_bvec);
   a.ckpt = (float *)(ws + Lo.off_ckpt);
   a.qt = (__nv_bfloat16 *)(ws + Lo.off_qt);
+  a.eng = (float *)(ws + Lo.off_eng);
   a.kt = (__nv_bfloat16 *)(ws + Lo.off_kt);
   a.err = pr.err;
   const dim3 grid((unsigned)Lo.max_units, (unsigned)pr.H);
