@@ -195,37 +195,44 @@ __device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[1
 // when rev, holds q and becomes scale q exp(G) dec (reverse pass, chunks
 // first to last: the decay from the piece start to each token).  Returns
 // exp(Gam) of the two channels.
+// Packed fp32 pairs (the thread's two channels): one mul.rn.f32x2 per pair,
+// rounded exactly as two scalar multiplies.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n mul.rn.f32x2 z, x, y;\n"
+      " mov.b64 {%0, %1}, z;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
 __device__ __forceinline__ float2 prep_chunk_pair(uint32_t q, uint32_t k, float2 (&x)[8], float *gam, float *xch,
                                                 int pw, int lane, int rank, int L, float scale, bool with_q,
                                                 bool rev, bool accum = false,
                                                 float2 dec = make_float2(1.f, 1.f)) {
   const int c0 = 64 * rank + 2 * lane;
   const int t0 = 8 * pw;
-  float p0 = 1.f, p1 = 1.f;
+  const float2 one = make_float2(1.f, 1.f);
+  float2 p = one;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const bool ok = t0 + i < L;
-    x[i].x = ok ? __expf(x[i].x) : 1.f;
-    x[i].y = ok ? __expf(x[i].y) : 1.f;
-    p0 *= x[i].x;
-    p1 *= x[i].y;
+    x[i] = (t0 + i < L) ? make_float2(__expf(x[i].x), __expf(x[i].y)) : one;
+    p = mul2(p, x[i]);
   }
-  xch[pw * 128 + c0] = p0;
-  xch[pw * 128 + c0 + 1] = p1;
+  *reinterpret_cast<float2 *>(xch + pw * 128 + c0) = p;
   named_bar(1, 256);
-  float pre0 = 1.f, pre1 = 1.f, suf0 = 1.f, suf1 = 1.f;
+  float2 pre = one, suf = one;
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const float e0 = xch[u * 128 + c0], e1 = xch[u * 128 + c0 + 1];
-    if (u < pw) {
-      pre0 *= e0;
-      pre1 *= e1;
-    } else if (u > pw) {
-      suf0 *= e0;
-      suf1 *= e1;
-    }
+    const float2 e = *reinterpret_cast<const float2 *>(xch + u * 128 + c0);
+    if (u < pw)
+      pre = mul2(pre, e);
+    else if (u > pw)
+      suf = mul2(suf, e);
   }
-  const float T0 = pre0 * p0 * suf0, T1 = pre1 * p1 * suf1;  // exp(Gam)
+  const float2 T = mul2(mul2(pre, p), suf);  // exp(Gam)
   // byte offsets of rows t0 .. t0+7 of the column pair (c0, c0+1) in a tile
   uint32_t off[8];
   {
@@ -234,55 +241,52 @@ __device__ __forceinline__ float2 prep_chunk_pair(uint32_t q, uint32_t k, float2
 #pragma unroll
     for (int i = 0; i < 8; ++i) off[i] = b + ((cch ^ (uint32_t)i) << 4) + (uint32_t)i * 128u;
   }
+  const float2 sc2 = make_float2(scale, scale);
   uint32_t v[8];
   if (with_q) {
-    const float sp0 = scale * pre0, sp1 = scale * pre1;
-    float a0 = sp0, a1 = sp1;
+    float2 a = mul2(sc2, pre);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = lds_u32(q + off[i]);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      a0 *= x[i].x;
-      a1 *= x[i].y;
-      const __nv_bfloat162 qq = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
-      v[i] = (t0 + i < L) ? pack_bf16(__low2float(qq) * a0, __high2float(qq) * a1) : 0u;
+      a = mul2(a, x[i]);
+      const float2 r = mul2(bf2_to_f2(v[i]), a);
+      v[i] = (t0 + i < L) ? pack_bf16(r.x, r.y) : 0u;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sts_u32(q + off[i], v[i]);
   }
+  const float2 rT = accum ? dec : make_float2(__frcp_rn(T.x), __frcp_rn(T.y));
   if (!rev) {
-    float a0 = accum ? suf0 * dec.x : suf0 * __frcp_rn(T0), a1 = accum ? suf1 * dec.y : suf1 * __frcp_rn(T1);
+    float2 a = mul2(suf, rT);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
 #pragma unroll
     for (int i = 7; i >= 0; --i) {
-      const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
-      v[i] = (t0 + i < L) ? pack_bf16(__low2float(kk) * a0, __high2float(kk) * a1) : 0u;
-      a0 *= x[i].x;
-      a1 *= x[i].y;
+      const float2 r = mul2(bf2_to_f2(v[i]), a);
+      v[i] = (t0 + i < L) ? pack_bf16(r.x, r.y) : 0u;
+      a = mul2(a, x[i]);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
   } else {
-    float a0 = accum ? scale * pre0 * dec.x : scale * pre0 * __frcp_rn(T0),
-          a1 = accum ? scale * pre1 * dec.y : scale * pre1 * __frcp_rn(T1);
+    float2 a = mul2(mul2(sc2, pre), rT);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      a0 *= x[i].x;
-      a1 *= x[i].y;
-      const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
-      v[i] = (t0 + i < L) ? pack_bf16(__low2float(kk) * a0, __high2float(kk) * a1) : 0u;
+      a = mul2(a, x[i]);
+      const float2 r = mul2(bf2_to_f2(v[i]), a);
+      v[i] = (t0 + i < L) ? pack_bf16(r.x, r.y) : 0u;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
   }
   if (pw == 0 && !accum) {
-    gam[c0] = T0;
-    gam[c0 + 1] = T1;
+    gam[c0] = T.x;
+    gam[c0 + 1] = T.y;
   }
-  return make_float2(T0, T1);
+  return T;
 }
 
 __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float (&S)[64]) {
