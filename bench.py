@@ -456,7 +456,7 @@ def kernel_source_sha():
 
 
 # ncu kernel names -> the library's launch labels (template argument: mode)
-NCU_LABELS = (("gla_fwd_kernel<0>", "gla_fwd_kernel"), ("piece_state_kernel", "piece_state_kernel"),
+NCU_LABELS = (("gla_fwd_kernel", "gla_fwd_kernel"), ("piece_state_kernel", "piece_state_kernel"),
               ("gla_bwd_rev_kernel", "gla_bwd_rev_kernel"), ("gla_bwd_dq_kernel", "gla_bwd_dq_kernel"))
 
 

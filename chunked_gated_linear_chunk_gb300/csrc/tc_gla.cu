@@ -8,10 +8,9 @@
 namespace glacore {
 namespace tc {
 
-template <int MODE>
 __global__ void __launch_bounds__(448, 1)
     gla_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
-  gla_fwd_body<MODE>(maps, a, blockIdx.x);
+  gla_fwd_body(maps, a, blockIdx.x);
 }
 
 // =========================================================================
@@ -51,7 +50,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   a.err = pr.err;
   const int smem = fsm::BYTES + 1024;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gla_fwd_kernel<FWD_MAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(gla_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const dim3 grid((unsigned)(2 * Lo.max_units), (unsigned)pr.H);
   if (Lo.pieces) {
@@ -64,7 +63,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
     as.ht = nullptr;
     if ((e = launch_piece_states(maps, as, nullptr, nullptr, Lo.max_units, pr.H, st)) != cudaSuccess) return e;
   }
-  if ((e = launch_pairs(gla_fwd_kernel<FWD_MAIN>, grid, smem, st, maps, a)) != cudaSuccess) return e;
+  if ((e = launch_pairs(gla_fwd_kernel, grid, smem, st, maps, a)) != cudaSuccess) return e;
   mark_launch("gla_fwd_kernel", st);
   return cudaSuccess;
 }

@@ -47,13 +47,6 @@ namespace tc {
 //               registers, thread c holds row c), output stores
 // TMEM (512 columns): P[2] at 0/64, U[2] at 128/192, O[2] at 256/320.
 // =========================================================================
-// Modes of the forward kernel body: the forward itself, and the two
-// state-only passes of the exact sequence split (forward: each piece's end
-// state from zero; reverse: each piece's state gradient at its start from
-// zero at its end -- maps.k / maps.v then hold q / do, chunks run backwards,
-// and the k-slot factor is scale exp(G - Gam)).
-constexpr int FWD_MAIN = 0, FWD_STATE = 1, REV_STATE = 2;
-
 struct FwdMaps {
   CUtensorMap q, k, v, g;
 };
@@ -64,8 +57,8 @@ struct FwdArgs {
   const float *g;
   const float *h0;    // [n_docs,H,K,V] state entering the document, or null
   float *ht;          // [n_docs,H,K,V] final state (written by the last piece)
-  float *lbuf;        // [units,H,K,V] piece end state from zero (state-only mode writes it)
-  float *dbuf;        // [units,H,K] exp(sum of g over the piece) (state-only mode writes it)
+  float *lbuf;        // [units,H,K,V] piece end state from zero (written by the piece pass)
+  float *dbuf;        // [units,H,K] exp(sum of g over the piece) (written by the piece pass)
   __nv_bfloat16 *o;
   int *err;
 };
@@ -297,19 +290,7 @@ __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float
                  pack_bf16(S[n + 6], S[n + 7]));
 }
 
-// STATE_ONLY (MODE != FWD_MAIN): the piece passes of the exact sequence
-// split -- the piece's end state from a zero state (no q, no output) and its
-// total decay.  Unrolled over the piece, that state is one product
-//   L = sum_t diag(exp(sum of g after t in the piece)) k_t v_t^T = Khat^T V,
-// so each chunk's k is scaled by its decay to the piece end (chunks visited
-// last to first, the decay of the visited chunks carried per channel) and
-// its product accumulates in TMEM: no per-chunk state step.  The reverse pass
-// likewise accumulates scale q exp(prefix of g from the piece start) times do.
-// Pieces that end their document have nothing to contribute and exit.
-template <int MODE>
 __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs &a, unsigned bx) {
-  constexpr bool STATE_ONLY = MODE != FWD_MAIN;
-  constexpr bool REV = MODE == REV_STATE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[fsm::NS], empty[fsm::NS], prep_done[fsm::NS], p_full[2], u_full[2],
@@ -327,13 +308,8 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   const int64_t d = un.doc;
   const int64_t s0 = un.start, s1 = un.end;
   const bool last_piece = un.piece == un.npieces - 1;
-  // the forward state pass has nothing to hand on from a document's last
-  // piece, the reverse pass nothing from its first
-  const bool idle = STATE_ONLY && (REV ? un.piece == 0 : last_piece);
-  const int nch = idle ? 0 : (int)((s1 - s0 + C - 1) / C);
-  // chunk visited at iteration j (the forward state pass walks backwards)
-  constexpr bool BACK = MODE == FWD_STATE;
-  auto chunk_tok = [&](int j) -> int64_t { return s0 + (int64_t)(BACK ? nch - 1 - j : j) * C; };
+  const int nch = (int)((s1 - s0 + C - 1) / C);
+  auto chunk_tok = [&](int j) -> int64_t { return s0 + (int64_t)j * C; };
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -387,10 +363,8 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
           const int tp = (int)chunk_tok(jp);
           for (int x = 0; x < KD; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
           if (jp >= fsm::NS) {
-            if (!STATE_ONLY) {
-              tma_prefetch_3d(&maps.q, 0, h, tp);
-              tma_prefetch_3d(&maps.q, 64, h, tp);
-            }
+            tma_prefetch_3d(&maps.q, 0, h, tp);
+            tma_prefetch_3d(&maps.q, 64, h, tp);
             tma_prefetch_3d(&maps.k, 0, h, tp);
             tma_prefetch_3d(&maps.k, 64, h, tp);
             tma_prefetch_3d(&maps.v, vb * 64, h, tp);
@@ -398,9 +372,9 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         }
         // this CTA's half of the q / k channels (the peer writes the other
         // half of the prepared tiles) and its value half of v
-        mbar_expect_tx(&full[s], (STATE_ONLY ? 8192 : 2 * 8192) + 8192);
+        mbar_expect_tx(&full[s], 3 * 8192);
         uint8_t *q = sm + fsm::Q + s * 16384, *k = sm + fsm::K + s * 16384;
-        if (!STATE_ONLY) tma_load_3d(q + vb * 8192, &maps.q, 64 * vb, h, tok, &full[s]);
+        tma_load_3d(q + vb * 8192, &maps.q, 64 * vb, h, tok, &full[s]);
         tma_load_3d(k + vb * 8192, &maps.k, 64 * vb, h, tok, &full[s]);
         tma_load_3d(sm + fsm::V + s * 8192, &maps.v, vb * 64, h, tok, &full[s]);
       }
@@ -422,16 +396,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
           FAIL_AND_BREAK
         }
         ph_prep ^= 1u << st;
-        if (STATE_ONLY) {
-          // one accumulator over the whole piece (U[0])
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tbase + 128, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit_multicast(&empty[st], 3);
-          if (j == nch - 1) mma_commit(&u_full[0]);
-          continue;
-        }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(ka, ks, 64), idP, ks);
@@ -466,7 +430,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     const int c0 = 64 * vb + 2 * lane, t0 = 8 * pw;
     const uint32_t rem = mapa_shared(sbase, peer);  // the peer's tiles
     uint32_t ph_full = 0;
-    float2 dec = make_float2(1.f, 1.f);  // state-only: decay of the channels over the visited chunks
     // gates of chunk j+1 are loaded into registers while chunk j is prepared
     float2 xn[8];
     auto load_x = [&](int jj, float2 (&x)[8]) {
@@ -491,14 +454,10 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       // this CTA's 64-column block of q, k and its gate totals (byte offsets)
       const uint32_t qo = fsm::Q + s * 16384 + vb * 8192, ko = fsm::K + s * 16384 + vb * 8192,
                      go = fsm::GAM + (j & 3) * 512 + vb * 256;
-      const float2 tot = prep_chunk_pair(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
+      prep_chunk_pair(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
                       reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
-                      reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 1024, pw, lane, vb, L, a.scale,
-                      !STATE_ONLY, REV, STATE_ONLY, dec);
-      if (STATE_ONLY) {
-        dec.x *= tot.x;
-        dec.y *= tot.y;
-      }
+                      reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 1024, pw, lane, vb, L, a.scale, true,
+                      false);
       fence_async_smem();
       // copy the prepared blocks into the peer's tiles (bulk copies that
       // complete on the peer's barriers; one arrive there stands for the
@@ -507,21 +466,14 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       if (pw == 0 && lane == 0) {
         const uint32_t pbar = mapa_shared(smem_u32(&prep_done[s]), peer);
         const uint32_t gbar = mapa_shared(smem_u32(&gam_ready[j & 3]), peer);
-        mbar_arrive_expect_tx_cluster(pbar, STATE_ONLY ? 8192u : 16384u);
-        if (!STATE_ONLY) bulk_copy_to_cluster(rem + qo, sbase + qo, 8192, pbar);
+        mbar_arrive_expect_tx_cluster(pbar, 16384u);
+        bulk_copy_to_cluster(rem + qo, sbase + qo, 8192, pbar);
         bulk_copy_to_cluster(rem + ko, sbase + ko, 8192, pbar);
-        if (!STATE_ONLY) {
-          mbar_arrive_expect_tx_cluster(gbar, 256u);
-          bulk_copy_to_cluster(rem + go, sbase + go, 256, gbar);
-        }
+        mbar_arrive_expect_tx_cluster(gbar, 256u);
+        bulk_copy_to_cluster(rem + go, sbase + go, 256, gbar);
       }
       mbar_arrive(&prep_done[s]);
-      if (!STATE_ONLY) mbar_arrive(&gam_ready[j & 3]);
-    }
-    // state-only: the piece's total decay of this CTA's 64 channels
-    if (STATE_ONLY && nch > 0 && pw == 0 && !*abortp) {
-      a.dbuf[(u * a.H + h) * KD + c0] = dec.x;
-      a.dbuf[(u * a.H + h) * KD + c0 + 1] = dec.y;
+      mbar_arrive(&gam_ready[j & 3]);
     }
   } else {
     // ---------------- epilogue warpgroup ----------------
@@ -532,50 +484,23 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     const int64_t H = a.H;
     const int v0 = vb * 64;
     float S[64];
-    if (STATE_ONLY) {
-#pragma unroll
-      for (int n = 0; n < 64; ++n) S[n] = 0.f;
-    } else {
+    {
       // state entering the unit: h0 folded over the document's earlier pieces
       const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
       piece_state_in<64>(S, h0row, a.lbuf, a.dbuf, u - un.piece, un.piece, H, h, c, v0);
     }
-    if (!STATE_ONLY) {
-      mask_tile_init(sm + fsm::P, qw, lane);
-      mask_tile_init(sm + fsm::P + 8192, qw, lane);
-      store_state_bf16(sm + fsm::S + 16384, c, S);
-      fence_async_smem();
-      mbar_arrive(&s_ready[1]);
-    }
+    mask_tile_init(sm + fsm::P, qw, lane);
+    mask_tile_init(sm + fsm::P + 8192, qw, lane);
+    store_state_bf16(sm + fsm::S + 16384, c, S);
+    fence_async_smem();
+    mbar_arrive(&s_ready[1]);
     uint32_t ph_p = 0, ph_u = 0, ph_o = 0;
-    if (STATE_ONLY && nch > 0) {
-      // the piece's accumulated product is its end state
-      if (mbar_wait(&u_full[0], 0, WAIT_CYCLES)) {
-        tc_fence_after();
-#pragma unroll
-        for (int cp = 0; cp < 4; cp += 2) {
-          uint32_t r[16], r2[16];
-          tmem_ld16(tbase + 128 + lane_off + cp * 16, r);
-          tmem_ld16(tbase + 128 + lane_off + cp * 16 + 16, r2);
-          tmem_ld_wait(r);
-          tmem_tie(r2);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            S[cp * 16 + i] = __uint_as_float(r[i]);
-            S[cp * 16 + 16 + i] = __uint_as_float(r2[i]);
-          }
-        }
-      } else {
-        atomicExch(&abort_flag, 1);
-      }
-    }
-    for (int j = 0; j < (STATE_ONLY ? 0 : nch); ++j) {
+    for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
       const int64_t tok0 = chunk_tok(j);
       const int L = (int)min((int64_t)C, s1 - tok0);
       const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
       // S2: P -> causal mask -> bf16 A operand of the intra-chunk product
-      if (!STATE_ONLY) {
       if (!mbar_wait(&p_full[b], (ph_p >> b) & 1, WAIT_CYCLES)) {
         FAIL_AND_BREAK
       }
@@ -585,7 +510,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[b]);
-      }
       // S3a: state update S <- exp(Gam) (S + kt^T V), bf16 copy for the next readout
       if (!mbar_wait(&u_full[b], (ph_u >> b) & 1, WAIT_CYCLES) ||
           !mbar_wait_cluster(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
@@ -642,12 +566,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       }
       tc_fence_before();
     }
-    float *dst = nullptr;
-    if (STATE_ONLY && nch > 0) {
-      dst = a.lbuf + ((u * H + h) * KD + c) * VD + v0;
-    } else if (!STATE_ONLY && a.ht && last_piece) {
-      dst = a.ht + ((d * H + h) * KD + c) * VD + v0;
-    }
+    float *dst = a.ht && last_piece ? a.ht + ((d * H + h) * KD + c) * VD + v0 : nullptr;
     if (dst && !*abortp) {
 #pragma unroll
       for (int n = 0; n < 64; n += 4)
@@ -660,9 +579,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   if (*abortp && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_TIMEOUT);
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
-
-// STATE_ONLY body is also launched by the backward's combined piece pass
-// (tc_gla_bwd.cu), so the kernel body lives in this header.
 
 }  // namespace tc
 }  // namespace glacore
