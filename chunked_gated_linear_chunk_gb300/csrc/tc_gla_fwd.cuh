@@ -71,24 +71,10 @@ constexpr uint32_t V = 98304;     // 3 x 8 KB (64 value columns)
 constexpr uint32_t P = 122880;    // 2 x 8 KB: masked P (bf16, K-major A)
 constexpr uint32_t S = 139264;    // 2 x 16 KB: S (bf16, rows = key channel)
 constexpr uint32_t GAM = 172032;  // 4 x 128 fp32: exp(chunk gate total)
-constexpr uint32_t XCH = 174080;  // 2 x 8 x 128 fp32: eighth-chunk gate products
+constexpr uint32_t XCH = 174080;  // 8 KB: token-group gate products (two buffers per prep group)
 constexpr uint32_t BYTES = 182272;
 }  // namespace fsm
 
-// Shared-memory addresses of the 16 rows t0 .. t0+15 (t0 % 8 == 0) of one
-// 4-byte column pair (c, c+1) of a bf16 128-byte-swizzled tile with 64-row
-// column blocks: the XOR pattern depends only on (row % 8), so eight bases
-// cover all rows and the row offset folds into the instruction immediate.
-struct Rows16 {
-  uint32_t a[8];
-  __device__ __forceinline__ Rows16(const uint8_t *tile, int t0, int c) {
-    const uint32_t base = smem_u32(tile) + (uint32_t)(c >> 6) * 8192u + (uint32_t)t0 * 128u +
-                          (uint32_t)(c & 7) * 2u;
-    const uint32_t cch = (uint32_t)(c & 63) >> 3;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) a[k] = base + ((cch ^ (uint32_t)k) << 4);
-  }
-};
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -96,79 +82,6 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
 }
 __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Prep of one chunk by the 256 prep threads: thread (warp pw in 0..7, lane)
-// owns key channels c0, c0+1 (c0 = 64 * (pw & 1) + 2 * lane) and tokens
-// t0 = 16 * (pw >> 1) .. +15.  `gv` holds its gate values (already loaded).
-// exp(G_t) is the prefix product of exp(g) and exp(Gam - G_t) the suffix
-// product, so each element costs one exponential:
-//   qt = scale q exp(G),  kt = k exp(-Gam) exp(Gam - G).
-// The four token quarters exchange their partial products through `xch`.
-// Rows t >= L (past the document end) are zeroed.  Writes exp(Gam) of its
-// channels to gam (quarter-0 warps).
-__device__ __forceinline__ void prep_chunk(uint8_t *q, uint8_t *k, float2 (&x)[16], float *gam,
-                                           float *xch, int pw, int lane, int L, float scale,
-                                           bool with_q) {
-  const int tq = pw >> 1;
-  const int c0 = 64 * (pw & 1) + 2 * lane;
-  const int t0 = 16 * tq;
-  float p0 = 1.f, p1 = 1.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const bool ok = t0 + i < L;
-    x[i].x = ok ? __expf(x[i].x) : 1.f;
-    x[i].y = ok ? __expf(x[i].y) : 1.f;
-    p0 *= x[i].x;
-    p1 *= x[i].y;
-  }
-  xch[tq * 128 + c0] = p0;
-  xch[tq * 128 + c0 + 1] = p1;
-  named_bar(1, 256);
-  float pre0 = 1.f, pre1 = 1.f, suf0 = 1.f, suf1 = 1.f;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const float e0 = xch[u * 128 + c0], e1 = xch[u * 128 + c0 + 1];
-    if (u < tq) {
-      pre0 *= e0;
-      pre1 *= e1;
-    } else if (u > tq) {
-      suf0 *= e0;
-      suf1 *= e1;
-    }
-  }
-  const float T0 = pre0 * p0 * suf0, T1 = pre1 * p1 * suf1;  // exp(Gam)
-  const float i0 = __frcp_rn(T0), i1 = __frcp_rn(T1);
-  const Rows16 rq(q, t0, c0), rk(k, t0, c0);
-  uint32_t v[16];
-  if (with_q) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = lds_u32(rq.a[i & 7] + i * 128);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      pre0 *= x[i].x;
-      pre1 *= x[i].y;
-      const __nv_bfloat162 qq = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
-      v[i] = (t0 + i < L) ? pack_bf16(scale * __low2float(qq) * pre0, scale * __high2float(qq) * pre1) : 0u;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) sts_u32(rq.a[i & 7] + i * 128, v[i]);
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = lds_u32(rk.a[i & 7] + i * 128);
-#pragma unroll
-  for (int i = 15; i >= 0; --i) {
-    const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162 *>(&v[i]);
-    v[i] = (t0 + i < L) ? pack_bf16(__low2float(kk) * suf0 * i0, __high2float(kk) * suf1 * i1) : 0u;
-    suf0 *= x[i].x;
-    suf1 *= x[i].y;
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) sts_u32(rk.a[i & 7] + i * 128, v[i]);
-  if (tq == 0) {
-    gam[c0] = T0;
-    gam[c0 + 1] = T1;
-  }
 }
 
 // Prep of one chunk by the 256 prep threads of one CTA of a pair.  The two
@@ -201,24 +114,30 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
-__device__ __forceinline__ float2 prep_chunk_pair(uint32_t q, uint32_t k, float2 (&x)[8], float *gam, float *xch,
+// TPT tokens per thread: the 64 tokens of the chunk are 64 / TPT token
+// groups (tg), whose threads (bar_threads of them) meet at named barrier
+// bar_id to exchange their products through xch ([64 / TPT][128] floats).
+template <int TPT = 8>
+__device__ __forceinline__ float2 prep_chunk_pair(uint32_t q, uint32_t k, float2 (&x)[TPT], float *gam, float *xch,
                                                 int pw, int lane, int rank, int L, float scale, bool with_q,
                                                 bool rev, bool accum = false,
-                                                float2 dec = make_float2(1.f, 1.f)) {
+                                                float2 dec = make_float2(1.f, 1.f), int bar_id = 1,
+                                                int bar_threads = 256) {
+  constexpr int NG = 64 / TPT;
   const int c0 = 64 * rank + 2 * lane;
-  const int t0 = 8 * pw;
+  const int t0 = TPT * pw;
   const float2 one = make_float2(1.f, 1.f);
   float2 p = one;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < TPT; ++i) {
     x[i] = (t0 + i < L) ? make_float2(__expf(x[i].x), __expf(x[i].y)) : one;
     p = mul2(p, x[i]);
   }
   *reinterpret_cast<float2 *>(xch + pw * 128 + c0) = p;
-  named_bar(1, 256);
+  named_bar(bar_id, bar_threads);
   float2 pre = one, suf = one;
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
+  for (int u = 0; u < NG; ++u) {
     const float2 e = *reinterpret_cast<const float2 *>(xch + u * 128 + c0);
     if (u < pw)
       pre = mul2(pre, e);
@@ -227,53 +146,53 @@ __device__ __forceinline__ float2 prep_chunk_pair(uint32_t q, uint32_t k, float2
   }
   const float2 T = mul2(mul2(pre, p), suf);  // exp(Gam)
   // byte offsets of rows t0 .. t0+7 of the column pair (c0, c0+1) in a tile
-  uint32_t off[8];
+  uint32_t off[TPT];
   {
     const uint32_t b = (uint32_t)(c0 >> 6) * 8192u + (uint32_t)t0 * 128u + (uint32_t)(c0 & 7) * 2u;
     const uint32_t cch = (uint32_t)(c0 & 63) >> 3;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) off[i] = b + ((cch ^ (uint32_t)i) << 4) + (uint32_t)i * 128u;
+    for (int i = 0; i < TPT; ++i) off[i] = b + ((cch ^ (uint32_t)(i & 7)) << 4) + (uint32_t)i * 128u;
   }
   const float2 sc2 = make_float2(scale, scale);
-  uint32_t v[8];
+  uint32_t v[TPT];
   if (with_q) {
     float2 a = mul2(sc2, pre);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = lds_u32(q + off[i]);
+    for (int i = 0; i < TPT; ++i) v[i] = lds_u32(q + off[i]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < TPT; ++i) {
       a = mul2(a, x[i]);
       const float2 r = mul2(bf2_to_f2(v[i]), a);
       v[i] = (t0 + i < L) ? pack_bf16(r.x, r.y) : 0u;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sts_u32(q + off[i], v[i]);
+    for (int i = 0; i < TPT; ++i) sts_u32(q + off[i], v[i]);
   }
   const float2 rT = accum ? dec : make_float2(__frcp_rn(T.x), __frcp_rn(T.y));
   if (!rev) {
     float2 a = mul2(suf, rT);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
+    for (int i = 0; i < TPT; ++i) v[i] = lds_u32(k + off[i]);
 #pragma unroll
-    for (int i = 7; i >= 0; --i) {
+    for (int i = TPT - 1; i >= 0; --i) {
       const float2 r = mul2(bf2_to_f2(v[i]), a);
       v[i] = (t0 + i < L) ? pack_bf16(r.x, r.y) : 0u;
       a = mul2(a, x[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
+    for (int i = 0; i < TPT; ++i) sts_u32(k + off[i], v[i]);
   } else {
     float2 a = mul2(mul2(sc2, pre), rT);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = lds_u32(k + off[i]);
+    for (int i = 0; i < TPT; ++i) v[i] = lds_u32(k + off[i]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < TPT; ++i) {
       a = mul2(a, x[i]);
       const float2 r = mul2(bf2_to_f2(v[i]), a);
       v[i] = (t0 + i < L) ? pack_bf16(r.x, r.y) : 0u;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sts_u32(k + off[i], v[i]);
+    for (int i = 0; i < TPT; ++i) sts_u32(k + off[i], v[i]);
   }
   if (pw == 0 && !accum) {
     gam[c0] = T.x;
@@ -320,7 +239,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     for (int i = 0; i < fsm::NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 2);        // the MMA commits of both CTAs (multicast)
-      mbar_init(&prep_done[i], 257);  // 256 local prep threads + the peer's
+      mbar_init(&prep_done[i], 129);  // the 128 prep threads of the chunk's group + the peer's
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
@@ -329,7 +248,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       mbar_init(&p_ready[i], 128);
       mbar_init(&s_ready[i], 128);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 257);
+    for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 129);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -425,45 +344,45 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     }
   } else if (warp < 10) {
     // ---------------- prep warps (8) ----------------
-    // this CTA's 64 key channels (c0, c0+1 per lane), tokens 8 pw .. 8 pw + 7
-    const int pw = warp - 2;
-    const int c0 = 64 * vb + 2 * lane, t0 = 8 * pw;
+    // Two groups of four warps take alternate chunks (group g: chunks j with
+    // j % 2 == g), so that two chunks' prep chains are in flight at once.
+    // Thread: this CTA's key channels c0, c0 + 1, tokens 16 tg .. 16 tg + 15.
+    const int pw = warp - 2, grp = pw >> 2, tg = pw & 3;
+    const int c0 = 64 * vb + 2 * lane, t0 = 16 * tg;
     const uint32_t rem = mapa_shared(sbase, peer);  // the peer's tiles
-    uint32_t ph_full = 0;
-    // gates of chunk j+1 are loaded into registers while chunk j is prepared
-    float2 xn[8];
-    auto load_x = [&](int jj, float2 (&x)[8]) {
+    // gates of the group's next chunk are loaded while this one is prepared
+    float2 xn[16];
+    auto load_x = [&](int jj, float2 (&x)[16]) {
       const int64_t tk = chunk_tok(jj);
       const int LL = (int)min((int64_t)C, s1 - tk);
       const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 16; ++i)
         x[i] = (t0 + i < LL) ? ldg_early2(gp + (int64_t)i * a.H * KD) : make_float2(0.f, 0.f);
     };
-    if (nch > 0) load_x(0, xn);
-    for (int j = 0; j < nch; ++j) {
+    if (grp < nch) load_x(grp, xn);
+    for (int j = grp; j < nch; j += 2) {
       const int s = j % fsm::NS;
       const int64_t tok0 = chunk_tok(j);
       const int L = (int)min((int64_t)C, s1 - tok0);
-      float2 x[8];
+      float2 x[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = xn[i];
-      if (j + 1 < nch) load_x(j + 1, xn);
-      if (!mbar_wait(&full[s], (ph_full >> s) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
-      ph_full ^= 1u << s;
+      for (int i = 0; i < 16; ++i) x[i] = xn[i];
+      if (j + 2 < nch) load_x(j + 2, xn);
+      if (!mbar_wait(&full[s], (j / fsm::NS) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
       // this CTA's 64-column block of q, k and its gate totals (byte offsets)
       const uint32_t qo = fsm::Q + s * 16384 + vb * 8192, ko = fsm::K + s * 16384 + vb * 8192,
                      go = fsm::GAM + (j & 3) * 512 + vb * 256;
-      prep_chunk_pair(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
-                      reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
-                      reinterpret_cast<float *>(sm + fsm::XCH) + (j & 1) * 1024, pw, lane, vb, L, a.scale, true,
-                      false);
+      prep_chunk_pair<16>(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
+                          reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
+                          reinterpret_cast<float *>(sm + fsm::XCH) + (2 * grp + ((j >> 1) & 1)) * 512, tg, lane,
+                          vb, L, a.scale, true, false, false, make_float2(1.f, 1.f), 1 + grp, 128);
       fence_async_smem();
       // copy the prepared blocks into the peer's tiles (bulk copies that
       // complete on the peer's barriers; one arrive there stands for the
-      // 256 threads here)
-      named_bar(1, 256);
-      if (pw == 0 && lane == 0) {
+      // 128 threads of the group here)
+      named_bar(1 + grp, 128);
+      if (tg == 0 && lane == 0) {
         const uint32_t pbar = mapa_shared(smem_u32(&prep_done[s]), peer);
         const uint32_t gbar = mapa_shared(smem_u32(&gam_ready[j & 3]), peer);
         mbar_arrive_expect_tx_cluster(pbar, 16384u);
