@@ -59,6 +59,8 @@ struct Units {
   const Unit *table;
   Docs docs;
   int64_t plen;
+  const int32_t *order;  // launch order (longest first) or null (unit index order)
+  __device__ __forceinline__ int64_t at(int64_t r) const { return order ? (int64_t)order[r] : r; }
   __device__ __forceinline__ Unit get(int64_t u) const {
     if (table) return table[u];
     Unit r;

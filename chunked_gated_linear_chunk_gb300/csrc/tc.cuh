@@ -24,6 +24,9 @@ int64_t piece_len(const glacore_problem *p, bool backward);
 int64_t max_units_of(const glacore_problem *p, int64_t plen);
 cudaError_t launch_build_units(const Docs &docs, int64_t plen, Unit *units, int64_t max_units,
                                cudaStream_t st);
+// Units of a packed batch in launch order, longest first (counting sort by
+// chunk count): long documents start in the first wave instead of the last.
+cudaError_t launch_order_units(const Units &us, int64_t n, int32_t *order, cudaStream_t st);
 
 // Scratch layout of the tcgen05 path (byte offsets into the workspace).
 // Piece hand-off buffers (fp32): L [units,H,K,V] end state of each piece
@@ -32,7 +35,8 @@ cudaError_t launch_build_units(const Docs &docs, int64_t plen, Unit *units, int6
 struct TcLayout {
   int64_t plen, max_units, ckpt_slots;
   bool pieces, table;
-  size_t off_units, off_L, off_D, off_Lr, off_Dr, off_dgp, off_bvec, off_ckpt, off_qt, off_kt, off_eng, total;
+  size_t off_units, off_order, off_L, off_D, off_Lr, off_Dr, off_dgp, off_bvec, off_ckpt, off_qt, off_kt, off_eng,
+      total;
 };
 // The backward resets the gate-gradient carry to the exact boundary term
 // (S_end (.) dH_end) 1_V every CKPT_CHUNKS chunks (state written by pass A).
@@ -46,6 +50,7 @@ inline Units units_of(const Docs &docs, const TcLayout &Lo, char *ws) {
   us.docs = docs;
   us.table = (Lo.pieces && Lo.table) ? (const Unit *)(ws + Lo.off_units) : nullptr;
   us.plen = (Lo.pieces && !Lo.table) ? Lo.plen : 0;
+  us.order = docs.start ? (const int32_t *)(ws + Lo.off_order) : nullptr;
   return us;
 }
 

@@ -20,7 +20,9 @@ __global__ void __launch_bounds__(448, 1)
 bool supported(const glacore_problem *p, bool head_gate, bool) {
   if (head_gate) return false;
   return p->dtype == GLACORE_BF16 && p->K == KD && p->V == VD && p->Hqk == p->H &&
-         (p->chunk_size == 0 || p->chunk_size == 64) && p->B * p->T < ((int64_t)1 << 31);
+         (p->chunk_size == 0 || p->chunk_size == 64) && p->B * p->T < ((int64_t)1 << 31) &&
+         // one-dimensional grids of 2 x units x heads CTAs (units <= documents + pieces)
+         4 * p->B * p->T * p->H < ((int64_t)1 << 31);
 }
 int chunk_of(const glacore_problem *) { return C; }
 size_t workspace_bytes(const glacore_problem *p, bool, bool backward) {
@@ -52,11 +54,14 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gla_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
-  const dim3 grid((unsigned)(2 * Lo.max_units), (unsigned)pr.H);
+  const dim3 grid((unsigned)(2 * Lo.max_units * pr.H));
+  if (Lo.pieces && Lo.table &&
+      (e = launch_build_units(docs, Lo.plen, (Unit *)(ws + Lo.off_units), Lo.max_units, st)) != cudaSuccess)
+    return e;
+  if (a.units.order &&
+      (e = launch_order_units(a.units, Lo.max_units, (int32_t *)(ws + Lo.off_order), st)) != cudaSuccess)
+    return e;
   if (Lo.pieces) {
-    if (Lo.table &&
-        (e = launch_build_units(docs, Lo.plen, (Unit *)(ws + Lo.off_units), Lo.max_units, st)) != cudaSuccess)
-      return e;
     a.lbuf = (float *)(ws + Lo.off_L);
     a.dbuf = (float *)(ws + Lo.off_D);
     FwdArgs as = a;

@@ -169,8 +169,9 @@ __global__ void __launch_bounds__(448, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int64_t u = blockIdx.x;
+  // blockIdx.x = r H + h: launch rank r (units in launch order), head h
+  const int h = (int)((int64_t)blockIdx.x % a.H);
+  const int64_t u = a.units.at((int64_t)blockIdx.x / a.H);
   const int64_t H = a.H;
   const Unit un = a.units.get(u);
   const int64_t d = un.doc;
@@ -673,8 +674,9 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int64_t u = bx;
+  // bx = r H + h: launch rank r (units in launch order), head h
+  const int h = (int)((int64_t)bx % a.H);
+  const int64_t u = a.units.at((int64_t)bx / a.H);
   const int64_t H = a.H;
   const Unit un = a.units.get(u);
   const int64_t d = un.doc;
@@ -1166,16 +1168,19 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   a.eng = (float *)(ws + Lo.off_eng);
   a.kt = (__nv_bfloat16 *)(ws + Lo.off_kt);
   a.err = pr.err;
-  const dim3 grid((unsigned)Lo.max_units, (unsigned)pr.H);
+  const dim3 grid((unsigned)(Lo.max_units * pr.H));
   const int smA = asm_::BYTES + 1024, smB = bsm::BYTES + 1024;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gla_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smA)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(gla_bwd_rev_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
     return e;
+  if (Lo.pieces && Lo.table &&
+      (e = launch_build_units(docs, Lo.plen, (Unit *)(ws + Lo.off_units), Lo.max_units, st)) != cudaSuccess)
+    return e;
+  if (a.units.order &&
+      (e = launch_order_units(a.units, Lo.max_units, (int32_t *)(ws + Lo.off_order), st)) != cudaSuccess)
+    return e;
   if (Lo.pieces) {
-    if (Lo.table &&
-        (e = launch_build_units(docs, Lo.plen, (Unit *)(ws + Lo.off_units), Lo.max_units, st)) != cudaSuccess)
-      return e;
     a.lf = (const float *)(ws + Lo.off_L);
     a.df = (const float *)(ws + Lo.off_D);
     a.lr = (const float *)(ws + Lo.off_Lr);

@@ -220,9 +220,10 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the two value halves of a (unit, head) are a cluster of two CTAs that
   // share the q / k prep (rank = value half)
-  const int vb = bx & 1, h = blockIdx.y;
+  // bx = 2 (r H + h) + vb: launch rank r (units in launch order), head h
+  const int vb = bx & 1, h = (int)((int64_t)(bx >> 1) % a.H);
   const uint32_t peer = (uint32_t)(vb ^ 1);
-  const int64_t u = bx >> 1;
+  const int64_t u = a.units.at((int64_t)(bx >> 1) / a.H);
   const Unit un = a.units.get(u);
   const int64_t d = un.doc;
   const int64_t s0 = un.start, s1 = un.end;

@@ -296,6 +296,38 @@ cudaError_t launch_piece_states(const FwdMaps &fm, const FwdArgs &fa, const FwdM
   return cudaGetLastError();
 }
 
+// One CTA: counting sort of the units by chunk count, longest first (ties in
+// any order; results do not depend on the launch order).
+__global__ void __launch_bounds__(1024) order_units_kernel(Units us, int64_t n, int32_t *order) {
+  __shared__ int cnt[1024];
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  auto bucket = [&](int64_t u) -> int {
+    const Unit un = us.get(u);
+    return (int)min((int64_t)1023, (un.end - un.start + C - 1) / C);
+  };
+  for (int64_t u = threadIdx.x; u < n; u += blockDim.x) atomicAdd(&cnt[bucket(u)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {  // cnt[b] <- first position of bucket b (longer buckets first)
+    int run = 0;
+    for (int b = 1023; b >= 0; --b) {
+      const int c = cnt[b];
+      cnt[b] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int64_t u = threadIdx.x; u < n; u += blockDim.x) order[atomicAdd(&cnt[bucket(u)], 1)] = (int32_t)u;
+}
+
+cudaError_t launch_order_units(const Units &us, int64_t n, int32_t *order, cudaStream_t st) {
+  Units plain = us;
+  plain.order = nullptr;
+  order_units_kernel<<<1, 1024, 0, st>>>(plain, n, order);
+  mark_launch("order_units", st);
+  return cudaGetLastError();
+}
+
 // Piece length: split documents only when (documents x heads x CTAs per
 // unit) leaves most of the GPU's SMs idle, and then into about as many
 // pieces as make one wave.
@@ -331,12 +363,16 @@ TcLayout tc_layout(const glacore_problem *p, bool backward) {
   const size_t mu = (size_t)L.max_units, H = (size_t)p->H;
   const size_t state = (size_t)KD * VD * sizeof(float);
   size_t off = 0;
-  L.off_units = L.off_L = L.off_D = L.off_Lr = L.off_Dr = L.off_dgp = L.off_bvec = L.off_ckpt = 0;
+  L.off_units = L.off_order = L.off_L = L.off_D = L.off_Lr = L.off_Dr = L.off_dgp = L.off_bvec = L.off_ckpt = 0;
   L.off_qt = L.off_kt = L.off_eng = 0;
   // chunks of all documents (upper bound) -> checkpoint slots
   const int64_t chunks = p->segment_ids ? (p->B * p->T + C - 1) / C + p->n_seqs
                                         : p->B * ((p->T + C - 1) / C);
   L.ckpt_slots = chunks / CKPT_CHUNKS + 1;
+  if (p->segment_ids) {  // launch order of the units of a packed batch
+    L.off_order = off;
+    off = al256(off + mu * sizeof(int32_t));
+  }
   if (L.pieces) {
     if (L.table) {
       L.off_units = off;
