@@ -1015,7 +1015,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     mask_tile_init(sm + bsm::P, qw, lane);
     mask_tile_init(sm + bsm::DP, qw, lane);
     // dH = state gradient leaving the unit: dht folded over the document's
-    // later pieces (0 in dH-only mode)
+    // later pieces
     {
       const float *dhtrow = a.dht ? a.dht + ((d * H + h) * KD + c) * VD : nullptr;
 #pragma unroll 1

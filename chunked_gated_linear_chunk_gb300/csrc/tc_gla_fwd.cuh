@@ -84,16 +84,16 @@ __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// Prep of one chunk by the 256 prep threads of one CTA of a pair.  The two
-// CTAs (value halves) of a (unit, head) share the q / k tiles: CTA `rank`
+// Prep of one chunk by the prep threads of one CTA of a pair.  The two CTAs
+// (value halves) of a (unit, head) share the q / k tiles: CTA `rank`
 // prepares key channels 64 rank .. 64 rank + 63 (one 64-column block of
 // each tile) in place; the block is then copied to the peer.
-// Thread (warp pw in 0..7, lane) owns channels c0, c0+1 (c0 = 64 rank +
-// 2 lane) and tokens t0 = 8 pw .. t0 + 7; x holds their gates.  As in
-// prep_chunk: exp(G_t) by prefix products, exp(Gam - G_t) by suffix
-// products, one exponential per element; the eight token groups exchange
-// their products through xch.
-// accum (the state-only piece passes): the k-slot tile is scaled for a
+// Thread (token group pw, lane) owns channels c0, c0+1 (c0 = 64 rank +
+// 2 lane) and tokens t0 = TPT pw .. t0 + TPT - 1; x holds their gates.
+// exp(G_t) comes by prefix products and exp(Gam - G_t) by suffix products,
+// one exponential per element; the token groups exchange their products
+// through xch.
+// accum (the piece passes of piece_state_kernel): the k-slot tile is scaled for a
 // product accumulated over the whole piece instead of a per-chunk state
 // step: with dec = (dec0, dec1) the decay of the channels over the chunks
 // already visited, it becomes k exp(Gam - G) dec (forward pass, chunks

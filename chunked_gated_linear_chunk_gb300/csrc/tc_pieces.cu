@@ -13,8 +13,8 @@
 //   dH_end[last] = dht,   dH_end[p] = diag(D_{p+1}) dH_end[p+1] + Lr_{p+1}.
 // The consumers fold these recurrences over the earlier (later) pieces of
 // their document when they start (piece_state_in / piece_grad_out in
-// tc.cuh); the local states come from state-only modes of the forward and
-// reverse kernels.  This file builds the unit table of packed documents and
+// tc.cuh); the local states come from piece_state_kernel below.  This file
+// also builds the unit table and the launch order of packed documents and
 // sizes the workspace.
 #include "tc_gla_fwd.cuh"
 
