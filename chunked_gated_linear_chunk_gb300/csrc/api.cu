@@ -51,14 +51,34 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t *seg, int64_t 
                                                     int64_t *cbase, int *err) {
   __shared__ int64_t wbuf[32];
   const int64_t BT = B * T;
+  constexpr int TPT = 16;  // consecutive tokens per thread and pass
   int64_t off = 0;
-  for (int64_t base = 0; base < BT; base += blockDim.x) {
-    const int64_t pos = base + threadIdx.x;
-    int64_t flag = 0;
-    if (pos < BT) flag = (pos % T == 0) || (seg[pos] != seg[pos - 1]);
+  for (int64_t base = 0; base < BT; base += (int64_t)blockDim.x * TPT) {
+    const int64_t p0 = base + (int64_t)threadIdx.x * TPT;
+    uint32_t flags = 0;
+    int64_t cnt = 0;
+    int64_t col = p0 % T;
+    int32_t prev = (p0 > 0 && p0 < BT) ? seg[p0 - 1] : 0;
+#pragma unroll
+    for (int i = 0; i < TPT; ++i) {
+      const int64_t pos = p0 + i;
+      if (pos < BT) {
+        const int32_t cur = seg[pos];
+        const bool f = col == 0 || cur != prev;
+        flags |= (uint32_t)f << i;
+        cnt += f;
+        prev = cur;
+      }
+      if (++col == T) col = 0;
+    }
     int64_t tot;
-    const int64_t idx = off + block_excl_scan(flag, wbuf, tot);
-    if (flag && idx < n_seqs) start[idx] = pos;
+    int64_t idx = off + block_excl_scan(cnt, wbuf, tot);
+#pragma unroll
+    for (int i = 0; i < TPT; ++i)
+      if ((flags >> i) & 1u) {
+        if (idx < n_seqs) start[idx] = p0 + i;
+        ++idx;
+      }
     off += tot;
   }
   const int64_t count = off;

@@ -308,13 +308,12 @@ __global__ void __launch_bounds__(1024) order_units_kernel(Units us, int64_t n, 
   };
   for (int64_t u = threadIdx.x; u < n; u += blockDim.x) atomicAdd(&cnt[bucket(u)], 1);
   __syncthreads();
-  if (threadIdx.x == 0) {  // cnt[b] <- first position of bucket b (longer buckets first)
-    int run = 0;
-    for (int b = 1023; b >= 0; --b) {
-      const int c = cnt[b];
-      cnt[b] = run;
-      run += c;
-    }
+  {  // cnt[b] <- first position of bucket b (longer buckets first): thread t scans bucket 1023 - t
+    __shared__ int64_t wbuf[32];
+    const int b = 1023 - (int)threadIdx.x;
+    int64_t tot;
+    const int64_t pos = block_excl_scan((int64_t)cnt[b], wbuf, tot);
+    cnt[b] = (int)pos;
   }
   __syncthreads();
   for (int64_t u = threadIdx.x; u < n; u += blockDim.x) order[atomicAdd(&cnt[bucket(u)], 1)] = (int32_t)u;
