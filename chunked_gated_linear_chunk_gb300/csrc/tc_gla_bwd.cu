@@ -51,7 +51,7 @@ struct BwdArgs {
   const float *lf, *df;  // forward piece hand-off: [units,H,K,V] end states from zero, [units,H,K] decays
   const float *lr, *dr;  // reverse piece hand-off: [units,H,K,V] state gradients at the piece
                          // starts from zero at their ends, [units,H,K] decays
-  float *ckpt;   // [slots,H,K,V] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
+  float *ckpt;   // [slots, H, V/4, K, 4] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
   __nv_bfloat16 *qt, *kt;  // scratch [BT, H, K]: gated q and k (pass A -> pass B)
   float *eng;    // scratch [chunk slots, H, C/4, K, 4] fp32: exp(-G) (pass A -> pass B)
   int *err;
@@ -596,8 +596,11 @@ __global__ void __launch_bounds__(448, 1)
         if (*abortp) break;
         tmem_st_wait();
         const int64_t slot = ckpt_slot(gc0, doc_c0, j, nch);
-        if (slot >= 0) {  // exact boundary state for pass B's gate-gradient carry
-          float *dst = a.ckpt + ((slot * H + h) * KD + c) * VD;
+        if (slot >= 0) {
+          // exact boundary state for pass B's gate-gradient carry, as
+          // [value quad][channel] x 4 columns: each warp store covers 512
+          // contiguous bytes
+          float *dst = a.ckpt + (slot * H + h) * (int64_t)(KD * VD) + 4 * c;
 #pragma unroll
           for (int cb = 0; cb < 4; ++cb) {
             uint32_t r[32];
@@ -605,7 +608,7 @@ __global__ void __launch_bounds__(448, 1)
             tmem_ld_wait32(r);
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4 *>(dst + 32 * cb + e) =
+              *reinterpret_cast<float4 *>(dst + (8 * cb + e / 4) * (4 * KD)) =
                   make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
                               __uint_as_float(r[e + 3]));
           }
@@ -1057,17 +1060,35 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         mbar_arrive(&eg_free[b]);
         uint8_t *Dt = sm + bsm::DH;
         const int64_t slot = ckpt_slot(gc0, doc_c0, j, nch);
-        const float *ck = slot >= 0 ? a.ckpt + ((slot * H + h) * KD + c) * VD : nullptr;
+        // checkpoint rows of channel c ([value quad][channel] x 4 layout)
+        const float *ck = slot >= 0 ? a.ckpt + (slot * H + h) * (int64_t)(KD * VD) + 4 * c : nullptr;
+        if (j >= 1) {
+          // the next chunk's checkpoint (64 KB) into L2, one line per thread and quarter
+          const int64_t ns = ckpt_slot(gc0, doc_c0, j - 1, nch);
+          if (ns >= 0) {
+            const char *nb = reinterpret_cast<const char *>(a.ckpt + ns * H * (int64_t)(KD * VD) +
+                                                            h * (int64_t)(KD * VD));
+#pragma unroll
+            for (int x = 0; x < 4; ++x) prefetch_l2(nb + (x * 128 + c) * 128);
+          }
+        }
         float bnd = 0.f;
         bool waited = i == 0;
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t r[32];
+          float4 cv[8];
+          if (ck) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cv[e] = ldg_early4(ck + (8 * cb + e) * (4 * KD));
+          }
           tmem_ld32(tDH + lane_off + 32 * cb, r);
           tmem_ld_wait32(r);
           if (ck) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) bnd += ck[32 * cb + e] * __uint_as_float(r[e]);
+            for (int e = 0; e < 8; ++e)
+              bnd += cv[e].x * __uint_as_float(r[4 * e]) + cv[e].y * __uint_as_float(r[4 * e + 1]) +
+                     cv[e].z * __uint_as_float(r[4 * e + 2]) + cv[e].w * __uint_as_float(r[4 * e + 3]);
           }
 #pragma unroll
           for (int w = 0; w < 32; ++w) r[w] = __float_as_uint(eGam * __uint_as_float(r[w]));
