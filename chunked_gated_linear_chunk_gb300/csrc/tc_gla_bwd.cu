@@ -1035,17 +1035,9 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     uint32_t ph_egr = 0;
     for (int i = 0; i < nch; ++i) {
       const int j = nch - 1 - i, b = i & 1;
-      // (1) masked P and dP -> bf16 operands (dk/dv of chunk i-1, their last
-      //     readers, are complete: pdp_full(i) is committed after them)
-      if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-      tc_fence_after();
-      mask_tile_to_smem(tP, lane_off, qw, lane, sm + bsm::P);
-      mask_tile_to_smem(tDP, lane_off, qw, lane, sm + bsm::DP);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&pdp_ready);
-      // (2) dHh = exp(Gam) dH in TMEM; its bf16 copy replaces chunk i-1's
-      //     once dk/dv of chunk i-1 have read that
+      // (1) dHh = exp(Gam) dH in TMEM; its bf16 copy replaces chunk i-1's
+      //     once dk/dv of chunk i-1 have read that.  This step does not need
+      //     chunk i's P and dP, so it runs while their products complete.
       if (!mbar_wait(&eg_ready[b], (ph_egr >> b) & 1, WAIT_CYCLES) ||
           (i >= 1 && !mbar_wait(&dh_full, (i - 1) & 1, WAIT_CYCLES)))
         BW_FAIL_AND_BREAK
@@ -1117,6 +1109,15 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&dh_ready);
+      // (2) masked P and dP -> bf16 operands (dk/dv of chunk i-1, their last
+      //     readers, are complete: pdp_full(i) is committed after them)
+      if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      tc_fence_after();
+      mask_tile_to_smem(tP, lane_off, qw, lane, sm + bsm::P);
+      mask_tile_to_smem(tDP, lane_off, qw, lane, sm + bsm::DP);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&pdp_ready);
     }
     // the last dH update
     if (nch > 0 && !*abortp && !mbar_wait(&dh_full, (nch - 1) & 1, WAIT_CYCLES)) atomicExch(&abort_flag, 1);
