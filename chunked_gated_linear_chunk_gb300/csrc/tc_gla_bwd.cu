@@ -143,11 +143,11 @@ constexpr uint32_t K = 32768;      // 2 x 16 KB k, then kt in place
 constexpr uint32_t V = 65536;      // 2 x 16 KB
 constexpr uint32_t DO = 98304;     // 2 x 16 KB
 constexpr uint32_t DP = 131072;    // 8 KB masked dP (bf16 [t][s])
-constexpr uint32_t GT = 139264;    // 32 KB gate tile g [t][c] (fp32, TMA box 32 x 64)
-constexpr uint32_t QT = 172032;    // 16 KB qt = scale q exp(G) (bf16, store source for pass B)
-constexpr uint32_t XCH = 188416;   // 2 x 2 x 128 fp32 gate products
-constexpr uint32_t XQ = 190464;    // 2 x 128 fp32: token-half totals of q (.) dq
-constexpr uint32_t BYTES = 191488;
+constexpr uint32_t GT = 139264;    // 2 x 32 KB gate tiles g [t][c] (fp32, TMA box 32 x 64)
+constexpr uint32_t QT = 204800;    // 16 KB qt = scale q exp(G) (bf16, store source for pass B)
+constexpr uint32_t XCH = 221184;   // 2 x 2 x 128 fp32 gate products
+constexpr uint32_t XQ = 223232;    // 2 x 128 fp32: token-half totals of q (.) dq
+constexpr uint32_t BYTES = 224256;
 }  // namespace asm_
 
 // Thread roles: warp 0 lane 0 TMA loads of k, v, do; lane 1 TMA loads of
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(448, 1)
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[asm_::NS], empty[asm_::NS], qfull[asm_::NS], qempty[asm_::NS],
       prep_done[asm_::NS], dp_full, dp_ready, dq_full[2], dq_free[2], u_full, s_ready, eg_ready[2],
-      eg_free[2], out_ready, stg_free, g_full, g_free, kt_read[asm_::NS];
+      eg_free[2], out_ready, stg_free, g_full[2], g_free[2], kt_read[asm_::NS];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -204,8 +204,10 @@ __global__ void __launch_bounds__(448, 1)
     mbar_init(&s_ready, 128);
     mbar_init(&out_ready, 256);
     mbar_init(&stg_free, 1);
-    mbar_init(&g_full, 1);
-    mbar_init(&g_free, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&g_full[i], 1);
+      mbar_init(&g_free[i], 256);
+    }
     fence_mbar_init();
   }
   tc_fence_before();
@@ -283,13 +285,16 @@ __global__ void __launch_bounds__(448, 1)
       }
       bulk_wait_all();
     } else if (lane == 3) {
-      // gate tile of each chunk (single buffer: refilled once the prep has read it)
+      // gate tile of each chunk (two buffers: chunk j's tile is loaded once
+      // the prep has read chunk j-2's)
       for (int j = 0; j < nch; ++j) {
-        if (j >= 1 && !mbar_wait(&g_free, (j - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        const int gb = j & 1;
+        if (j >= 2 && !mbar_wait(&g_free[gb], ((j >> 1) - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
-        mbar_expect_tx(&g_full, 32768);
-        for (int x = 0; x < 4; ++x) tma_load_3d(sm + asm_::GT + x * 8192, &maps.g, 32 * x, h, tok, &g_full);
+        mbar_expect_tx(&g_full[gb], 32768);
+        for (int x = 0; x < 4; ++x)
+          tma_load_3d(sm + asm_::GT + gb * 32768 + x * 8192, &maps.g, 32 * x, h, tok, &g_full[gb]);
       }
     } else if (lane == 4) {
       // kt of each full chunk to the workspace once the prep has written it
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     const int64_t gc0 = unit_chunk0(a.units, un);
     uint32_t ph_full = 0, ph_free = 0, ph_dqf = 0;
-    const ColF32 gcol(sbase + asm_::GT, 32 * th, c);
+    const ColF32 gcol(sbase + asm_::GT, 32 * th, c);  // buffer 0; buffer 1 is 32 KB on
     // iteration j: gate work and kt of chunk j, then the epilogue of chunk j-1
     for (int j = 0; j <= nch; ++j) {
       if (j < nch) {
@@ -368,10 +373,10 @@ __global__ void __launch_bounds__(448, 1)
         const int64_t tok0 = s0 + (int64_t)j * C;
         const int L = (int)min((int64_t)C, s1 - tok0);
         ChanGate cg;
-        if (!mbar_wait(&g_full, j & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if (!mbar_wait(&g_full[b], (j >> 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
 #pragma unroll
-        for (int i = 0; i < 32; ++i) cg.x[i] = 32 * th + i < L ? lds_f32(gcol.at(i)) : 0.f;
-        mbar_arrive(&g_free);
+        for (int i = 0; i < 32; ++i) cg.x[i] = 32 * th + i < L ? lds_f32(gcol.at(i) + b * 32768) : 0.f;
+        mbar_arrive(&g_free[b]);
         if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_full ^= 1u << st;
         exchange_gates(cg, reinterpret_cast<float *>(sm + asm_::XCH) + b * 256, c, th, L);
