@@ -148,8 +148,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 //   ColF32:  fp32 tile of 32-column blocks, 64 rows each (TMA box 32 x 64)
 struct ColBf16 {
   uint32_t a[8];
-  __device__ __forceinline__ ColBf16(uint32_t tile, int r0, int c) {
-    const uint32_t b = tile + (uint32_t)(c >> 6) * 8192u + (uint32_t)r0 * 128u + (uint32_t)(c & 7) * 2u;
+  // blk: distance between the tile's two 64-column blocks
+  __device__ __forceinline__ ColBf16(uint32_t tile, int r0, int c, uint32_t blk = 8192u) {
+    const uint32_t b = tile + (uint32_t)(c >> 6) * blk + (uint32_t)r0 * 128u + (uint32_t)(c & 7) * 2u;
     const uint32_t cc = (uint32_t)(c >> 3) & 7u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) a[k] = b + ((cc ^ (uint32_t)k) << 4);
@@ -292,6 +293,34 @@ __device__ __forceinline__ void mask_tile_init(uint8_t *tile, int qw, int lane) 
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb)
         st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), 0u, 0u, 0u, 0u);
+  }
+}
+// The same tile from an M = 128 accumulator (row r in lane r): the warp of
+// one TMEM lane quarter writes rows r0 .. r0 + 31 (r0 = 0 or 32; t_acc
+// addresses the tile's first column in that quarter).  mask_rows_init writes
+// each row's zero blocks above the diagonal once; mask_rows_to_smem loads
+// the blocks up to the warp's last diagonal block and writes, per row, the
+// blocks at or below its diagonal (diagonal block masked).
+__device__ __forceinline__ void mask_rows_init(uint8_t *tile, int r0, int lane) {
+  const int row = r0 + lane;
+  for (int cb = (row >> 4) + 1; cb < 4; ++cb)
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb)
+      st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), 0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void mask_rows_to_smem(uint32_t t_acc, int r0, int lane, uint8_t *tile) {
+  const int row = r0 + lane, rb = row >> 4;
+#pragma unroll
+  for (int cp = 0; cp < 4; cp += 2) {
+    if (cp <= (r0 >> 4) + 1) {
+      uint32_t a0[16], a1[16];
+      tmem_ld16(t_acc + cp * 16, a0);
+      tmem_ld16(t_acc + cp * 16 + 16, a1);
+      tmem_ld_wait(a0);
+      tmem_tie(a1);
+      if (cp <= rb) mask_block_store(tile, row, cp, a0, cp == rb, row & 15);
+      if (cp + 1 <= rb) mask_block_store(tile, row, cp + 1, a1, cp + 1 == rb, row & 15);
+    }
   }
 }
 // Called by a whole warp of the epilogue warpgroup (warp quarter qw).

@@ -654,10 +654,12 @@ __global__ void __launch_bounds__(448, 1)
 namespace bsm {  // shared-memory carve-up (bytes)
 constexpr int NS = 2;               // stages of the qt / do ring
 constexpr int NK = 3;               // stages of the kt / v ring (held until dk / dv are stored)
-constexpr uint32_t Q = 0;          // 2 x 16 KB qt (gated by pass A)
-constexpr uint32_t DO = 32768;     // 2 x 16 KB
-constexpr uint32_t K = 65536;      // 3 x 16 KB kt (gated by pass A), then dk (store source)
-constexpr uint32_t V = 114688;     // 3 x 16 KB v, then dv (store source)
+// qt and do share a 32 KB stage, kt and v another: [qt; do] and [kt; v] are
+// the 128-row operands of the stacked P / dP product.  Within a stage the
+// 64-column blocks go qt (kt) block 0, do (v) block 0, qt (kt) block 1, do (v)
+// block 1, 8 KB each, so either tile alone has its blocks 16 KB apart.
+constexpr uint32_t QD = 0;         // 2 x 32 KB qt (gated by pass A) and do
+constexpr uint32_t KV = 65536;     // 3 x 32 KB kt (gated by pass A) and v, then dk and dv (store sources)
 constexpr uint32_t P = 163840;     // 8 KB masked P  (bf16 [t][s])
 constexpr uint32_t DP = 172032;    // 8 KB masked dP (bf16 [t][s])
 constexpr uint32_t DH = 180224;    // 32 KB dHh (bf16 [c][v])
@@ -726,7 +728,9 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
   const uint32_t tbase = tmem_base;
   const uint32_t sbase = smem_u32(sm);
   volatile int *abortp = &abort_flag;
-  const uint32_t tDH = tbase, tP = tbase + 128, tDP = tbase + 192, tDK = tbase + 256,
+  // tPP: the stacked product, P in lanes 0..63 of its first 64 columns,
+  // dP in lanes 64..127 of the next 64
+  const uint32_t tDH = tbase, tPP = tbase + 128, tDK = tbase + 256,
                  tDV = tbase + 320, tEG = tbase + 384;
   const int64_t gc0 = unit_chunk0(a.units, un), doc_c0 = a.units.docs.chunk_base(un.doc);
 
@@ -754,8 +758,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         }
         mbar_expect_tx(&full[st], 2 * 16384);
         for (int x = 0; x < 2; ++x) {
-          tma_load_3d(sm + bsm::Q + st * 16384 + x * 8192, &maps.qt, 64 * x, h, tok, &full[st]);
-          tma_load_3d(sm + bsm::DO + st * 16384 + x * 8192, &maps.dO, 64 * x, h, tok, &full[st]);
+          tma_load_3d(sm + bsm::QD + st * 32768 + x * 16384, &maps.qt, 64 * x, h, tok, &full[st]);
+          tma_load_3d(sm + bsm::QD + st * 32768 + x * 16384 + 8192, &maps.dO, 64 * x, h, tok, &full[st]);
         }
       }
     } else if (lane == 1) {
@@ -770,8 +774,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         const int tok = (int)(s0 + (int64_t)j * C);
         mbar_expect_tx(&kfull[st], 2 * 16384);
         for (int x = 0; x < 2; ++x) {
-          tma_load_3d(sm + bsm::K + st * 16384 + x * 8192, &maps.kt, 64 * x, h, tok, &kfull[st]);
-          tma_load_3d(sm + bsm::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &kfull[st]);
+          tma_load_3d(sm + bsm::KV + st * 32768 + x * 16384, &maps.kt, 64 * x, h, tok, &kfull[st]);
+          tma_load_3d(sm + bsm::KV + st * 32768 + x * 16384 + 8192, &maps.v, 64 * x, h, tok, &kfull[st]);
         }
       }
     } else if (lane == 2) {
@@ -785,8 +789,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         if (!mbar_wait(&out_ready[st], (i / bsm::NK) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         if (s1 - tok0 >= C) {
           for (int x = 0; x < 2; ++x) {
-            tma_store_3d(&maps.dk, sm + bsm::K + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
-            tma_store_3d(&maps.dv, sm + bsm::V + st * 16384 + x * 8192, 64 * x, h, (int)tok0);
+            tma_store_3d(&maps.dk, sm + bsm::KV + st * 32768 + x * 16384, 64 * x, h, (int)tok0);
+            tma_store_3d(&maps.dv, sm + bsm::KV + st * 32768 + x * 16384 + 8192, 64 * x, h, (int)tok0);
           }
           bulk_commit();
           bulk_wait_read_all();
@@ -797,7 +801,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idCC = idesc_bf16(64, 64, false, false);
+      constexpr uint32_t idPP = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idMM = idesc_bf16(128, 64, true, true);   // MN-major A and B
       constexpr uint32_t idKK = idesc_bf16(128, 64, false, false); // K-major A and B
       constexpr uint32_t idMK = idesc_bf16(128, 64, true, false);  // MN-major A, K-major B
@@ -806,24 +810,23 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
       const uint32_t pa = sbase + bsm::P, dpa = sbase + bsm::DP, dha = sbase + bsm::DH;
       for (int i = 0; i < nch; ++i) {
         const int st = i % bsm::NS, sk = i % bsm::NK;
-        const uint32_t qa = sbase + bsm::Q + st * 16384, kta = sbase + bsm::K + sk * 16384;
-        const uint32_t va = sbase + bsm::V + sk * 16384, doa = sbase + bsm::DO + st * 16384;
+        const uint32_t qa = sbase + bsm::QD + st * 32768, kta = sbase + bsm::KV + sk * 32768;
+        const uint32_t va = kta + 8192, doa = qa + 8192;
         if (!mbar_wait(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES) ||
             !mbar_wait(&full[st], (i / bsm::NS) & 1, WAIT_CYCLES) ||
             !mbar_wait(&kfull[sk], (i / bsm::NK) & 1, WAIT_CYCLES))
           BW_FAIL_AND_BREAK
         ph_prep ^= 1u << st;
         tc_fence_after();
+        // [P, .; ., dP] = [qt; dO] [kt; v]^T  (one M = 128, N = 128 product)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(kta, ks, 64), idCC, ks);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDP, kdesc(doa, ks, 64), kdesc(va, ks, 64), idCC, ks);
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tPP, kdesc(qa, ks, 128), kdesc(kta, ks, 128), idPP, ks);
         mma_commit(&pdp_full);
         // dH (TMEM, = dHh after the state step) += qt^T dO
         if (!mbar_wait(&dh_ready, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDH, mdesc(qa, ks, 8192), mdesc(doa, ks, 8192), idH, 1);
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDH, mdesc(qa, ks, 16384), mdesc(doa, ks, 16384), idH, 1);
         mma_commit(&dh_full);
         // dk/dv accumulators are free once the epilogue of chunk i-1 has read them
         if (!mbar_wait(&pdp_ready, i & 1, WAIT_CYCLES) ||
@@ -832,14 +835,14 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         tc_fence_after();
         // dk^T = qt^T dP + dHh V^T
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDK, mdesc(qa, ks, 8192), mdesc(dpa, ks, 8192), idMM, ks);
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDK, mdesc(qa, ks, 16384), mdesc(dpa, ks, 8192), idMM, ks);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDK, kdesc(dha, ks, 128), kdesc(va, ks, 64), idKK, 1);
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDK, kdesc(dha, ks, 128), kdesc(va, ks, 128), idKK, 1);
         // dv^T = dO^T P + dHh^T kt^T
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDV, mdesc(doa, ks, 8192), mdesc(pa, ks, 8192), idMM, ks);
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tDV, mdesc(doa, ks, 16384), mdesc(pa, ks, 8192), idMM, ks);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDV, mdesc(dha, ks, 16384), kdesc(kta, ks, 64), idMK, 1);
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tDV, mdesc(dha, ks, 16384), kdesc(kta, ks, 128), idMK, 1);
         mma_commit(&kv_full);
         mma_commit(&empty[st]);
       }
@@ -899,8 +902,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           if (!mbar_wait(&full[st], (i / bsm::NS) & 1, WAIT_CYCLES) ||
               !mbar_wait(&kfull[sk], (i / bsm::NK) & 1, WAIT_CYCLES))
             BW_FAIL_AND_BREAK
-          const ColBf16 qc(sbase + bsm::Q + st * 16384, 32 * th, c);
-          const ColBf16 kc(sbase + bsm::K + sk * 16384, 32 * th, c);
+          const ColBf16 qc(sbase + bsm::QD + st * 32768, 32 * th, c, 16384);
+          const ColBf16 kc(sbase + bsm::KV + sk * 32768, 32 * th, c, 16384);
 #pragma unroll
           for (int w = 0; w < 32; ++w)
             if (32 * th + w >= L) {
@@ -938,8 +941,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         const float cin = ckpt_slot(gc0, doc_c0, jj, nch) >= 0
                               ? reinterpret_cast<const float *>(sm + bsm::BND)[bb * 128 + c]
                               : carry;
-        const ColBf16 kc(sbase + bsm::K + stt * 16384, 32 * th, c);
-        const ColBf16 vc(sbase + bsm::V + stt * 16384, 32 * th, c);
+        const ColBf16 kc(sbase + bsm::KV + stt * 32768, 32 * th, c, 16384);
+        const ColBf16 vc(sbase + bsm::KV + stt * 32768 + 8192, 32 * th, c, 16384);
         float dgv[32];
         float sk = 0.f;
 #pragma unroll
@@ -1020,8 +1023,11 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    mask_tile_init(sm + bsm::P, qw, lane);
-    mask_tile_init(sm + bsm::DP, qw, lane);
+    // lane quarters 0, 1 hold rows 0..31, 32..63 of P; quarters 2, 3 those of dP
+    uint8_t *const mtile = sm + (qw < 2 ? bsm::P : bsm::DP);
+    const int mr0 = 32 * (qw & 1);
+    const uint32_t tM = tPP + lane_off + (qw < 2 ? 0u : 64u);
+    mask_rows_init(mtile, mr0, lane);
     // dH = state gradient leaving the unit: dht folded over the document's
     // later pieces
     {
@@ -1118,8 +1124,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
       //     readers, are complete: pdp_full(i) is committed after them)
       if (!mbar_wait(&pdp_full, i & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
       tc_fence_after();
-      mask_tile_to_smem(tP, lane_off, qw, lane, sm + bsm::P);
-      mask_tile_to_smem(tDP, lane_off, qw, lane, sm + bsm::DP);
+      mask_rows_to_smem(tM, mr0, lane, mtile);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&pdp_ready);
