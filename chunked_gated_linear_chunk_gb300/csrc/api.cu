@@ -129,7 +129,7 @@ struct Layout {
   size_t off_start, off_cbase;  // doc tables (segments only)
   size_t off_states, off_final, off_acc_q, off_acc_k, off_tc;
   // ssdx: the GLA problem's tensors ([B*T, H, 128]) and states ([n, H, 128, 128])
-  size_t off_xq, off_xk, off_xv, off_xg, off_xh0, off_xo, off_xht, off_xdo, off_xdht, off_xdq, off_xdk,
+  size_t off_xv, off_xh0, off_xo, off_xht, off_xdo, off_xdht, off_xdq, off_xdk,
       off_xdv, off_xdg, off_xdh0;
   size_t total;
 };
@@ -164,8 +164,10 @@ glacore_status check_problem(const glacore_problem *p, bool head_gate) {
 
 bool simt_supported(const glacore_problem *p) { return p->K <= 128 && p->V <= 128; }
 
-// The GLA problem an SSD problem is run as (ssd_gla.cu): every head its own
-// q / k, the gate on every key channel, V padded to 128.
+// The shape of the GLA problem an SSD problem is run as (ssd_gla.cu): K and
+// V of 128 (V zero-padded).  It is checked and laid out as if every head had
+// its own q / k; the kernels then read the grouped q / k and the per-head
+// gate in place.
 glacore_problem ssd_as_gla(const glacore_problem *p) {
   glacore_problem e = *p;
   e.Hqk = p->H;
@@ -200,10 +202,7 @@ Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
       o = off;
       off = align256(off + bytes);
     };
-    take(L.off_xq, bf);
-    take(L.off_xk, bf);
     take(L.off_xv, bf);
-    take(L.off_xg, f32);
     if (p->initial_state) take(L.off_xh0, st);
     if (!backward) {
       take(L.off_xo, bf);
@@ -303,18 +302,17 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
   const Docs docs = make_docs(p, L, ws);
   if (L.ssdx) {
     const int64_t rows = BT * p->H, mats = p->n_seqs * p->H;
+    // q, k of the head groups and the per-head gate are read in place
     glacore_problem e = ssd_as_gla(p);
-    e.q = ws + L.off_xq;
-    e.k = ws + L.off_xk;
+    e.Hqk = p->Hqk;
     e.v = ws + L.off_xv;
-    e.g = (const float *)(ws + L.off_xg);
     e.initial_state = p->initial_state ? (const float *)(ws + L.off_xh0) : nullptr;
-    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, nullptr, ws + L.off_xq,
-                                 ws + L.off_xk, ws + L.off_xv, (float *)(ws + L.off_xg), nullptr, st);
+    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, nullptr, nullptr, nullptr,
+                                 ws + L.off_xv, nullptr, nullptr, st);
     if (c == cudaSuccess && p->initial_state)
       c = ssdx::pad_states(mats, p->V, p->initial_state, (float *)(ws + L.off_xh0), st);
     if (c == cudaSuccess)
-      c = tc::fwd(make_prob(&e, false), docs, &e, ws + L.off_xo, ht ? (float *)(ws + L.off_xht) : nullptr,
+      c = tc::fwd(make_prob(&e, true), docs, &e, ws + L.off_xo, ht ? (float *)(ws + L.off_xht) : nullptr,
                   ws + L.off_tc, st);
     if (c == cudaSuccess) c = ssdx::cut_rows(rows, p->V, ws + L.off_xo, o, st);
     if (c == cudaSuccess && ht) c = ssdx::cut_states(mats, p->V, (const float *)(ws + L.off_xht), ht, st);
@@ -351,19 +349,18 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
   const Docs docs = make_docs(p, L, ws);
   if (L.ssdx) {
     const int64_t rows = BT * p->H, mats = p->n_seqs * p->H;
+    // q, k of the head groups and the per-head gate are read in place
     glacore_problem e = ssd_as_gla(p);
-    e.q = ws + L.off_xq;
-    e.k = ws + L.off_xk;
+    e.Hqk = p->Hqk;
     e.v = ws + L.off_xv;
-    e.g = (const float *)(ws + L.off_xg);
     e.initial_state = p->initial_state ? (const float *)(ws + L.off_xh0) : nullptr;
-    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, dO, ws + L.off_xq, ws + L.off_xk,
-                                 ws + L.off_xv, (float *)(ws + L.off_xg), ws + L.off_xdo, st);
+    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, dO, nullptr, nullptr,
+                                 ws + L.off_xv, nullptr, ws + L.off_xdo, st);
     if (c == cudaSuccess && p->initial_state)
       c = ssdx::pad_states(mats, p->V, p->initial_state, (float *)(ws + L.off_xh0), st);
     if (c == cudaSuccess && dht) c = ssdx::pad_states(mats, p->V, dht, (float *)(ws + L.off_xdht), st);
     if (c == cudaSuccess)
-      c = tc::bwd(make_prob(&e, false), docs, &e, ws + L.off_xdo, dht ? (const float *)(ws + L.off_xdht) : nullptr,
+      c = tc::bwd(make_prob(&e, true), docs, &e, ws + L.off_xdo, dht ? (const float *)(ws + L.off_xdht) : nullptr,
                   ws + L.off_xdq, ws + L.off_xdk, ws + L.off_xdv, (float *)(ws + L.off_xdg),
                   dh0 ? (float *)(ws + L.off_xdh0) : nullptr, ws + L.off_tc, st);
     if (c == cudaSuccess) c = ssdx::reduce_heads(BT, p->H, p->Hqk, ws + L.off_xdq, dq, st);

@@ -6,12 +6,12 @@
 // scalar special case of the per-channel decay): with g_gla[t,h,c] =
 // g_ssd[t,h] for all c the recurrences coincide,
 //   S_t = exp(g_t) S_{t-1} + k_t v_t^T,   o_t = scale S_t^T q_t.
-// These kernels build that GLA problem in the workspace -- q and k broadcast
-// to every head of their group, the gate broadcast over the K channels, v,
-// do, h0 and dht zero-padded to V = 128 -- and map the GLA gradients back:
-// dq and dk summed over the heads that share q and k, dg summed over K
-// (the gradient of a gate shared by K channels), dv / dh0 / o / final
-// state cut to V columns.
+// The tensor-core kernels read q and k of a head's group and the per-head
+// gate in place (their grouped-head and per-head-gate modes).  These kernels
+// only zero-pad v, do, h0 and dht to V = 128, and map the GLA gradients
+// back: dq and dk summed over the heads that share q and k, dg summed over K
+// (the gradient of a gate shared by K channels), dv / dh0 / o / final state
+// cut to V columns.
 #include "internal.cuh"
 
 namespace glacore {
@@ -19,9 +19,9 @@ namespace ssdx {
 
 constexpr int KX = 128, VX = 128;
 
-// One warp per (token, head), 16-byte chunks (V % 8 == 0).  Writes xq, xk
-// (q, k of the head's group), xv (v padded), xg (gate broadcast) and xdo
-// (do padded; skipped when null).
+// One warp per (token, head), 16-byte chunks (V % 8 == 0).  Writes xv (v
+// padded) and, where not null, xq, xk (q, k of the head's group), xg (gate
+// broadcast over K) and xdo (do padded).
 __global__ void expand_kernel(int64_t rows, int64_t H, int64_t Hqk, int64_t V, const uint4 *q, const uint4 *k,
                               const uint4 *v, const float *g, const uint4 *dO, uint4 *xq, uint4 *xk, uint4 *xv,
                               float4 *xg, uint4 *xdo) {
@@ -33,15 +33,17 @@ __global__ void expand_kernel(int64_t rows, int64_t H, int64_t Hqk, int64_t V, c
   const int64_t nv = V / 8;                       // chunks of a v / do row
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   if (lane < 16) {
-    xq[row * (KX / 8) + lane] = q[src + lane];
+    if (xq) xq[row * (KX / 8) + lane] = q[src + lane];
     xv[row * (VX / 8) + lane] = lane < nv ? v[row * nv + lane] : zero;
   } else {
     const int l = lane - 16;
-    xk[row * (KX / 8) + l] = k[src + l];
+    if (xk) xk[row * (KX / 8) + l] = k[src + l];
     if (xdo) xdo[row * (VX / 8) + l] = l < nv ? dO[row * nv + l] : zero;
   }
-  const float gv = g[row];
-  xg[row * (KX / 4) + lane] = make_float4(gv, gv, gv, gv);
+  if (xg) {
+    const float gv = g[row];
+    xg[row * (KX / 4) + lane] = make_float4(gv, gv, gv, gv);
+  }
 }
 
 // states [n*H, K, V] <-> [n*H, K, 128] (pad with zeros / cut)

@@ -8,9 +8,11 @@
 namespace glacore {
 namespace tc {
 
+// HG: one gate per head (SSD); otherwise one per key channel
+template <bool HG>
 __global__ void __launch_bounds__(448, 1)
     gla_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
-  gla_fwd_body(maps, a, blockIdx.x);
+  gla_fwd_body<HG>(maps, a, blockIdx.x);
 }
 
 // =========================================================================
@@ -35,15 +37,18 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   const TcLayout Lo = tc_layout(p, false);
   FwdMaps maps;
   const int64_t BT = pr.BT;
+  memset(&maps, 0, sizeof(maps));
   if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
-      !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32))
+      (!pr.gate_head && !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32)))
     return cudaErrorInvalidValue;
   FwdArgs a;
   memset(&a, 0, sizeof(a));
   a.units = units_of(docs, Lo, ws);
   a.H = pr.H;
+  a.hq_div = (int32_t)(pr.H / pr.Hqk);
+  a.gate_head = pr.gate_head;
   a.scale = pr.scale;
   a.g = pr.g;
   a.h0 = pr.h0;
@@ -52,7 +57,8 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   a.err = pr.err;
   const int smem = fsm::BYTES + 1024;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gla_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+  auto *kernel = a.gate_head ? gla_fwd_kernel<true> : gla_fwd_kernel<false>;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const dim3 grid((unsigned)(2 * Lo.max_units * pr.H));
   if (Lo.pieces && Lo.table &&
@@ -68,7 +74,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
     as.ht = nullptr;
     if ((e = launch_piece_states(maps, as, nullptr, nullptr, Lo.max_units, pr.H, st)) != cudaSuccess) return e;
   }
-  if ((e = launch_pairs(gla_fwd_kernel, grid, smem, st, maps, a)) != cudaSuccess) return e;
+  if ((e = launch_pairs(kernel, grid, smem, st, maps, a)) != cudaSuccess) return e;
   mark_launch("gla_fwd_kernel", st);
   return cudaSuccess;
 }

@@ -40,6 +40,8 @@ struct BwdMaps {
 struct BwdArgs {
   Units units;
   int64_t H;
+  int32_t hq_div;     // heads per q / k head (q, k are [BT, H / hq_div, K]); 0 or 1: one each
+  int32_t gate_head;  // 1: g is [BT, H], one log-decay per head for all key channels
   float scale;
   const float *g;
   const float *h0;     // [n_docs,H,K,V] or null
@@ -158,6 +160,9 @@ constexpr uint32_t BYTES = 224256;
 // warp's TMEM quarter, token half th): gate work and kt for chunk j, then
 // the dq / q (.) dq epilogue of chunk j-1 for their half, written to shared
 // memory for the TMA stores.  Warps 10..13 mask dP and scale the state.
+// HG: one gate per head (g is [BT, H]); the per-channel instance has none of
+// its branches.
+template <bool HG>
 __global__ void __launch_bounds__(448, 1)
     gla_bwd_dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -177,6 +182,7 @@ __global__ void __launch_bounds__(448, 1)
   const int64_t d = un.doc;
   const int64_t s0 = un.start, s1 = un.end;
   const int nch = (int)((s1 - s0 + C - 1) / C);
+  const int hq = (HG && a.hq_div > 1) ? h / a.hq_div : h;  // head of q and k
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(448, 1)
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.dO);
-      tma_prefetch_desc(&maps.g);
+      if (!HG) tma_prefetch_desc(&maps.g);
       for (int j = 0; j < nch; ++j) {
         const int st = j % asm_::NS;
         if (j >= asm_::NS && (!mbar_wait(&empty[st], ((j / asm_::NS) - 1) & 1, WAIT_CYCLES) ||
@@ -235,15 +241,16 @@ __global__ void __launch_bounds__(448, 1)
         if (j + 2 < nch) {
           const int tp = tok + 2 * C;
           for (int x = 0; x < 128; x += 64) {
-            tma_prefetch_3d(&maps.k, x, h, tp);
+            tma_prefetch_3d(&maps.k, x, hq, tp);
             tma_prefetch_3d(&maps.v, x, h, tp);
             tma_prefetch_3d(&maps.dO, x, h, tp);
           }
-          for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
+          if (!HG)
+            for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
         }
         mbar_expect_tx(&full[st], 3 * 16384);
         for (int x = 0; x < 2; ++x) {
-          tma_load_3d(sm + asm_::K + st * 16384 + x * 8192, &maps.k, 64 * x, h, tok, &full[st]);
+          tma_load_3d(sm + asm_::K + st * 16384 + x * 8192, &maps.k, 64 * x, hq, tok, &full[st]);
           tma_load_3d(sm + asm_::V + st * 16384 + x * 8192, &maps.v, 64 * x, h, tok, &full[st]);
           tma_load_3d(sm + asm_::DO + st * 16384 + x * 8192, &maps.dO, 64 * x, h, tok, &full[st]);
         }
@@ -257,12 +264,12 @@ __global__ void __launch_bounds__(448, 1)
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
         if (j + 2 < nch) {
-          tma_prefetch_3d(&maps.q, 0, h, tok + 2 * C);
-          tma_prefetch_3d(&maps.q, 64, h, tok + 2 * C);
+          tma_prefetch_3d(&maps.q, 0, hq, tok + 2 * C);
+          tma_prefetch_3d(&maps.q, 64, hq, tok + 2 * C);
         }
         mbar_expect_tx(&qfull[st], 16384);
         for (int x = 0; x < 2; ++x)
-          tma_load_3d(sm + asm_::Q + st * 16384 + x * 8192, &maps.q, 64 * x, h, tok, &qfull[st]);
+          tma_load_3d(sm + asm_::Q + st * 16384 + x * 8192, &maps.q, 64 * x, hq, tok, &qfull[st]);
       }
     } else if (lane == 2) {
       // stores of full chunks (a ragged chunk is stored by its epilogue threads)
@@ -284,7 +291,7 @@ __global__ void __launch_bounds__(448, 1)
         mbar_arrive(&stg_free);
       }
       bulk_wait_all();
-    } else if (lane == 3) {
+    } else if (lane == 3 && !HG) {
       // gate tile of each chunk (two buffers: chunk j's tile is loaded once
       // the prep has read chunk j-2's)
       for (int j = 0; j < nch; ++j) {
@@ -366,6 +373,20 @@ __global__ void __launch_bounds__(448, 1)
     const int64_t gc0 = unit_chunk0(a.units, un);
     uint32_t ph_full = 0, ph_free = 0, ph_dqf = 0;
     const ColF32 gcol(sbase + asm_::GT, 32 * th, c);  // buffer 0; buffer 1 is 32 KB on
+    // one gate per head: thread (th = 0, c < 64) fetches token c's gate two
+    // chunks ahead and stages it in the gate buffer of its chunk before the
+    // exchange barrier of the chunk before (gate of token t at byte 4 t)
+    const bool stager = HG && th == 0 && c < C;
+    auto gate_of = [&](int jj) -> float {
+      const int64_t t0 = s0 + (int64_t)jj * C;
+      return (jj < nch && t0 + c < s1) ? ldg_early(a.g + (t0 + c) * H + h) : 0.f;
+    };
+    float gnext = 0.f;
+    if (stager) {
+      reinterpret_cast<float *>(sm + asm_::GT)[c] = gate_of(0);
+      gnext = gate_of(1);
+    }
+    if (HG) named_bar(1, 256);
     // iteration j: gate work and kt of chunk j, then the epilogue of chunk j-1
     for (int j = 0; j <= nch; ++j) {
       if (j < nch) {
@@ -373,10 +394,23 @@ __global__ void __launch_bounds__(448, 1)
         const int64_t tok0 = s0 + (int64_t)j * C;
         const int L = (int)min((int64_t)C, s1 - tok0);
         ChanGate cg;
-        if (!mbar_wait(&g_full[b], (j >> 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+        if constexpr (HG) {
+          // the gates of chunk j (the same for every channel), staged two chunks
+          // ago; the next chunk's go to the other buffer before this chunk's
+          // exchange barrier, and the one after next is fetched
+          const uint32_t gs = sbase + asm_::GT + b * 32768 + 128 * th;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) cg.x[i] = 32 * th + i < L ? lds_f32(gcol.at(i) + b * 32768) : 0.f;
-        mbar_arrive(&g_free[b]);
+          for (int i = 0; i < 32; ++i) cg.x[i] = lds_f32(gs + 4 * i);
+          if (stager) {
+            reinterpret_cast<float *>(sm + asm_::GT + (b ^ 1) * 32768)[c] = gnext;
+            gnext = gate_of(j + 2);
+          }
+        } else {
+          if (!mbar_wait(&g_full[b], (j >> 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cg.x[i] = 32 * th + i < L ? lds_f32(gcol.at(i) + b * 32768) : 0.f;
+          mbar_arrive(&g_free[b]);
+        }
         if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_full ^= 1u << st;
         exchange_gates(cg, reinterpret_cast<float *>(sm + asm_::XCH) + b * 256, c, th, L);
@@ -1167,6 +1201,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   if (docs.n == 0) return cudaSuccess;
   const TcLayout Lo = tc_layout(p, true);
   BwdMaps maps;
+  memset(&maps, 0, sizeof(maps));
   const int64_t BT = pr.BT;
   float *dgp = (float *)(ws + Lo.off_dgp);
   if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
@@ -1174,7 +1209,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
       !make_map(&maps.dO, dO, true, VD, pr.H, BT, 64) ||
       !make_map(&maps.dq, dq, true, KD, pr.H, BT, 64) ||
-      !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32) ||
+      (!pr.gate_head && !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32)) ||
       !make_map(&maps.dk, dk, true, KD, pr.H, BT, 64) ||
       !make_map(&maps.dv, dv, true, VD, pr.H, BT, 64) ||
       !make_map(&maps.qt, ws + Lo.off_qt, true, KD, pr.H, BT, 64) ||
@@ -1184,6 +1219,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   memset(&a, 0, sizeof(a));
   a.units = units_of(docs, Lo, ws);
   a.H = pr.H;
+  a.hq_div = (int32_t)(pr.H / pr.Hqk);
+  a.gate_head = pr.gate_head;
   a.scale = pr.scale;
   a.g = pr.g;
   a.h0 = pr.h0;
@@ -1203,7 +1240,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   const dim3 grid((unsigned)(Lo.max_units * pr.H));
   const int smA = asm_::BYTES + 1024, smB = bsm::BYTES + 1024;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gla_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smA)) != cudaSuccess ||
+  auto *dq_kernel = a.gate_head ? gla_bwd_dq_kernel<true> : gla_bwd_dq_kernel<false>;
+  if ((e = cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smA)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(gla_bwd_rev_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smB)) != cudaSuccess)
     return e;
   if (Lo.pieces && Lo.table &&
@@ -1220,8 +1258,10 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     // local end states of the pieces (forward) and local state gradients at
     // their starts (reverse), in one launch; the consumers fold them
     FwdMaps fm, rm;
+    memset(&fm, 0, sizeof(fm));
     if (!make_map(&fm.q, pr.q, true, KD, pr.Hqk, BT, 64) || !make_map(&fm.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
-        !make_map(&fm.v, pr.v, true, VD, pr.H, BT, 64) || !make_map(&fm.g, pr.g, false, KD, pr.H, BT, 32))
+        !make_map(&fm.v, pr.v, true, VD, pr.H, BT, 64) ||
+        (!pr.gate_head && !make_map(&fm.g, pr.g, false, KD, pr.H, BT, 32)))
       return cudaErrorInvalidValue;
     rm = fm;
     rm.k = fm.q;   // the reverse pass runs q through the k slot ...
@@ -1230,6 +1270,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     memset(&fa, 0, sizeof(fa));
     fa.units = a.units;
     fa.H = pr.H;
+    fa.hq_div = a.hq_div;
+    fa.gate_head = a.gate_head;
     fa.scale = pr.scale;
     fa.g = pr.g;
     fa.err = pr.err;
@@ -1240,7 +1282,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     ra.dbuf = (float *)(ws + Lo.off_Dr);
     if ((e = launch_piece_states(fm, fa, &rm, &ra, Lo.max_units, pr.H, st)) != cudaSuccess) return e;
   }
-  gla_bwd_dq_kernel<<<grid, 448, smA, st>>>(maps, a);
+  dq_kernel<<<grid, 448, smA, st>>>(maps, a);
   mark_launch("gla_bwd_dq_kernel", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gla_bwd_rev_kernel<<<grid, 448, smB, st>>>(maps, a);

@@ -53,6 +53,8 @@ struct FwdMaps {
 struct FwdArgs {
   Units units;
   int64_t H;
+  int32_t hq_div;     // heads per q / k head (q, k are [BT, H / hq_div, K]); 0 or 1: one each
+  int32_t gate_head;  // 1: g is [BT, H], one log-decay per head for all key channels
   float scale;
   const float *g;
   const float *h0;    // [n_docs,H,K,V] state entering the document, or null
@@ -209,6 +211,9 @@ __device__ __forceinline__ void store_state_bf16(uint8_t *St, int c, const float
                  pack_bf16(S[n + 6], S[n + 7]));
 }
 
+// HG: one gate per head (g is [BT, H]); the per-channel instance has none of
+// its branches.
+template <bool HG>
 __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs &a, unsigned bx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -222,6 +227,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   // share the q / k prep (rank = value half)
   // bx = 2 (r H + h) + vb: launch rank r (units in launch order), head h
   const int vb = bx & 1, h = (int)((int64_t)(bx >> 1) % a.H);
+  const int hq = (HG && a.hq_div > 1) ? h / a.hq_div : h;  // head of q and k
   const uint32_t peer = (uint32_t)(vb ^ 1);
   const int64_t u = a.units.at((int64_t)(bx >> 1) / a.H);
   const Unit un = a.units.get(u);
@@ -271,7 +277,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
-      tma_prefetch_desc(&maps.g);
+      if (!HG) tma_prefetch_desc(&maps.g);
       for (int j = 0; j < nch; ++j) {
         const int s = j % fsm::NS;
         if (j >= fsm::NS && !mbar_wait(&empty[s], ((j / fsm::NS) - 1) & 1, WAIT_CYCLES))
@@ -281,12 +287,13 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
           // gates for the prep warps (read from L2); q/k/v ahead of the ring
           const int tp = (int)chunk_tok(jp);
-          for (int x = 0; x < KD; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
+          if (!HG)
+            for (int x = 0; x < KD; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
           if (jp >= fsm::NS) {
-            tma_prefetch_3d(&maps.q, 0, h, tp);
-            tma_prefetch_3d(&maps.q, 64, h, tp);
-            tma_prefetch_3d(&maps.k, 0, h, tp);
-            tma_prefetch_3d(&maps.k, 64, h, tp);
+            tma_prefetch_3d(&maps.q, 0, hq, tp);
+            tma_prefetch_3d(&maps.q, 64, hq, tp);
+            tma_prefetch_3d(&maps.k, 0, hq, tp);
+            tma_prefetch_3d(&maps.k, 64, hq, tp);
             tma_prefetch_3d(&maps.v, vb * 64, h, tp);
           }
         }
@@ -294,8 +301,8 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         // half of the prepared tiles) and its value half of v
         mbar_expect_tx(&full[s], 3 * 8192);
         uint8_t *q = sm + fsm::Q + s * 16384, *k = sm + fsm::K + s * 16384;
-        tma_load_3d(q + vb * 8192, &maps.q, 64 * vb, h, tok, &full[s]);
-        tma_load_3d(k + vb * 8192, &maps.k, 64 * vb, h, tok, &full[s]);
+        tma_load_3d(q + vb * 8192, &maps.q, 64 * vb, hq, tok, &full[s]);
+        tma_load_3d(k + vb * 8192, &maps.k, 64 * vb, hq, tok, &full[s]);
         tma_load_3d(sm + fsm::V + s * 8192, &maps.v, vb * 64, h, tok, &full[s]);
       }
     }
@@ -356,10 +363,19 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     auto load_x = [&](int jj, float2 (&x)[16]) {
       const int64_t tk = chunk_tok(jj);
       const int LL = (int)min((int64_t)C, s1 - tk);
-      const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
+      if constexpr (HG) {  // one gate per head: the same for both channels
+        const float *gp = a.g + (tk + t0) * a.H + h;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        x[i] = (t0 + i < LL) ? ldg_early2(gp + (int64_t)i * a.H * KD) : make_float2(0.f, 0.f);
+        for (int i = 0; i < 16; ++i) {
+          const float gv = (t0 + i < LL) ? ldg_early(gp + (int64_t)i * a.H) : 0.f;
+          x[i] = make_float2(gv, gv);
+        }
+      } else {
+        const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          x[i] = (t0 + i < LL) ? ldg_early2(gp + (int64_t)i * a.H * KD) : make_float2(0.f, 0.f);
+      }
     };
     if (grp < nch) load_x(grp, xn);
     for (int j = grp; j < nch; j += 2) {

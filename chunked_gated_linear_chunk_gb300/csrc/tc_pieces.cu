@@ -151,21 +151,23 @@ __device__ __forceinline__ void piece_state_body(const FwdMaps &maps, const FwdA
 
   if (warp == 0) {
     if (lane == 0) {
+      const int hq = a.hq_div > 1 ? h / a.hq_div : h;  // head of the k slot's tensor (k or q)
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
-      tma_prefetch_desc(&maps.g);
+      if (!a.gate_head) tma_prefetch_desc(&maps.g);
       for (int j = 0; j < nch; ++j) {
         const int s = j % psm::NS;
         if (j >= psm::NS && !mbar_wait(&empty[s], ((j / psm::NS) - 1) & 1, WAIT_CYCLES)) PS_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)chunk_tok(j);
-        for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
-          const int tp = (int)chunk_tok(jp);
-          tma_prefetch_3d(&maps.g, 64 * kb, h, tp);
-          tma_prefetch_3d(&maps.g, 64 * kb + 32, h, tp);
-        }
+        if (!a.gate_head)
+          for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
+            const int tp = (int)chunk_tok(jp);
+            tma_prefetch_3d(&maps.g, 64 * kb, h, tp);
+            tma_prefetch_3d(&maps.g, 64 * kb + 32, h, tp);
+          }
         mbar_expect_tx(&full[s], 8192 + 16384);
-        tma_load_3d(sm + psm::K + s * 8192, &maps.k, 64 * kb, h, tok, &full[s]);
+        tma_load_3d(sm + psm::K + s * 8192, &maps.k, 64 * kb, hq, tok, &full[s]);
         tma_load_3d(sm + psm::V + s * 16384, &maps.v, 0, h, tok, &full[s]);
         tma_load_3d(sm + psm::V + s * 16384 + 8192, &maps.v, 64, h, tok, &full[s]);
       }
@@ -200,10 +202,19 @@ __device__ __forceinline__ void piece_state_body(const FwdMaps &maps, const FwdA
     auto load_x = [&](int jj, float2 (&x)[8]) {
       const int64_t tk = chunk_tok(jj);
       const int LL = (int)min((int64_t)C, s1 - tk);
-      const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
+      if (a.gate_head) {  // one gate per head: the same for both channels
+        const float *gp = a.g + (tk + t0) * a.H + h;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        x[i] = (t0 + i < LL) ? ldg_early2(gp + (int64_t)i * a.H * KD) : make_float2(0.f, 0.f);
+        for (int i = 0; i < 8; ++i) {
+          const float gv = (t0 + i < LL) ? ldg_early(gp + (int64_t)i * a.H) : 0.f;
+          x[i] = make_float2(gv, gv);
+        }
+      } else {
+        const float *gp = a.g + ((tk + t0) * a.H + h) * KD + c0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          x[i] = (t0 + i < LL) ? ldg_early2(gp + (int64_t)i * a.H * KD) : make_float2(0.f, 0.f);
+      }
     };
     load_x(0, xn);
     for (int j = 0; j < nch; ++j) {
