@@ -124,13 +124,12 @@ namespace {
 
 struct Layout {
   bool tc;             // tensor-core path
-  bool ssdx;           // SSD through the GLA tensor-core kernels (expanded problem in the workspace)
+  bool ssdx;           // SSD through the GLA tensor-core kernels (states padded in the workspace)
   int chunk;           // chunk length of the state workspace / doc table
   size_t off_start, off_cbase;  // doc tables (segments only)
   size_t off_states, off_final, off_acc_q, off_acc_k, off_tc;
   // ssdx: the GLA problem's tensors ([B*T, H, 128]) and states ([n, H, 128, 128])
-  size_t off_xv, off_xh0, off_xo, off_xht, off_xdo, off_xdht, off_xdq, off_xdk,
-      off_xdv, off_xdg, off_xdh0;
+  size_t off_xh0, off_xht, off_xdht, off_xdq, off_xdk, off_xdg, off_xdh0;
   size_t total;
 };
 
@@ -165,9 +164,9 @@ glacore_status check_problem(const glacore_problem *p, bool head_gate) {
 bool simt_supported(const glacore_problem *p) { return p->K <= 128 && p->V <= 128; }
 
 // The shape of the GLA problem an SSD problem is run as (ssd_gla.cu): K and
-// V of 128 (V zero-padded).  It is checked and laid out as if every head had
-// its own q / k; the kernels then read the grouped q / k and the per-head
-// gate in place.
+// V of 128, every head its own q / k.  It is checked and laid out so; the
+// kernels then read the grouped q / k, the per-head gate and the V-column v
+// and do in place (the columns past V as zeros).
 glacore_problem ssd_as_gla(const glacore_problem *p) {
   glacore_problem e = *p;
   e.Hqk = p->H;
@@ -176,7 +175,9 @@ glacore_problem ssd_as_gla(const glacore_problem *p) {
   return e;
 }
 bool ssdx_supported(const glacore_problem *p, bool head_gate, bool backward) {
-  if (!head_gate || p->dtype != GLACORE_BF16 || p->K != 128 || p->V > 128 || p->V % 8) return false;
+  // V of 64 or 128: the kernels read v and do as 128 columns, the missing 64
+  // zero-filled by TMA, and store o and dv per 64-column half
+  if (!head_gate || p->dtype != GLACORE_BF16 || p->K != 128 || (p->V != 64 && p->V != 128)) return false;
   const glacore_problem e = ssd_as_gla(p);
   return tc::supported(&e, false, backward);
 }
@@ -202,17 +203,13 @@ Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
       o = off;
       off = align256(off + bytes);
     };
-    take(L.off_xv, bf);
     if (p->initial_state) take(L.off_xh0, st);
     if (!backward) {
-      take(L.off_xo, bf);
       take(L.off_xht, st);
     } else {
-      take(L.off_xdo, bf);
       take(L.off_xdht, st);
       take(L.off_xdq, bf);
       take(L.off_xdk, bf);
-      take(L.off_xdv, bf);
       take(L.off_xdg, f32);
       if (p->initial_state) take(L.off_xdh0, st);
     }
@@ -301,20 +298,17 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
   }
   const Docs docs = make_docs(p, L, ws);
   if (L.ssdx) {
-    const int64_t rows = BT * p->H, mats = p->n_seqs * p->H;
-    // q, k of the head groups and the per-head gate are read in place
+    const int64_t mats = p->n_seqs * p->H;
+    // q, k of the head groups, the per-head gate and the V-column v are read
+    // in place; only the states are padded to V = 128
     glacore_problem e = ssd_as_gla(p);
     e.Hqk = p->Hqk;
-    e.v = ws + L.off_xv;
+    e.V = p->V;
     e.initial_state = p->initial_state ? (const float *)(ws + L.off_xh0) : nullptr;
-    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, nullptr, nullptr, nullptr,
-                                 ws + L.off_xv, nullptr, nullptr, st);
-    if (c == cudaSuccess && p->initial_state)
-      c = ssdx::pad_states(mats, p->V, p->initial_state, (float *)(ws + L.off_xh0), st);
+    cudaError_t c = cudaSuccess;
+    if (p->initial_state) c = ssdx::pad_states(mats, p->V, p->initial_state, (float *)(ws + L.off_xh0), st);
     if (c == cudaSuccess)
-      c = tc::fwd(make_prob(&e, true), docs, &e, ws + L.off_xo, ht ? (float *)(ws + L.off_xht) : nullptr,
-                  ws + L.off_tc, st);
-    if (c == cudaSuccess) c = ssdx::cut_rows(rows, p->V, ws + L.off_xo, o, st);
+      c = tc::fwd(make_prob(&e, true), docs, &e, o, ht ? (float *)(ws + L.off_xht) : nullptr, ws + L.off_tc, st);
     if (c == cudaSuccess && ht) c = ssdx::cut_states(mats, p->V, (const float *)(ws + L.off_xht), ht, st);
     return cuda_status(c);
   }
@@ -349,23 +343,22 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
   const Docs docs = make_docs(p, L, ws);
   if (L.ssdx) {
     const int64_t rows = BT * p->H, mats = p->n_seqs * p->H;
-    // q, k of the head groups and the per-head gate are read in place
+    // q, k of the head groups, the per-head gate, the V-column v and do are
+    // read in place, dv written in place; only the states are padded to V = 128
     glacore_problem e = ssd_as_gla(p);
     e.Hqk = p->Hqk;
-    e.v = ws + L.off_xv;
+    e.V = p->V;
     e.initial_state = p->initial_state ? (const float *)(ws + L.off_xh0) : nullptr;
-    cudaError_t c = ssdx::expand(BT, p->H, p->Hqk, p->V, p->q, p->k, p->v, p->g, dO, nullptr, nullptr,
-                                 ws + L.off_xv, nullptr, ws + L.off_xdo, st);
-    if (c == cudaSuccess && p->initial_state)
+    cudaError_t c = cudaSuccess;
+    if (p->initial_state)
       c = ssdx::pad_states(mats, p->V, p->initial_state, (float *)(ws + L.off_xh0), st);
     if (c == cudaSuccess && dht) c = ssdx::pad_states(mats, p->V, dht, (float *)(ws + L.off_xdht), st);
     if (c == cudaSuccess)
-      c = tc::bwd(make_prob(&e, true), docs, &e, ws + L.off_xdo, dht ? (const float *)(ws + L.off_xdht) : nullptr,
-                  ws + L.off_xdq, ws + L.off_xdk, ws + L.off_xdv, (float *)(ws + L.off_xdg),
+      c = tc::bwd(make_prob(&e, true), docs, &e, dO, dht ? (const float *)(ws + L.off_xdht) : nullptr,
+                  ws + L.off_xdq, ws + L.off_xdk, dv, (float *)(ws + L.off_xdg),
                   dh0 ? (float *)(ws + L.off_xdh0) : nullptr, ws + L.off_tc, st);
     if (c == cudaSuccess) c = ssdx::reduce_heads(BT, p->H, p->Hqk, ws + L.off_xdq, dq, st);
     if (c == cudaSuccess) c = ssdx::reduce_heads(BT, p->H, p->Hqk, ws + L.off_xdk, dk, st);
-    if (c == cudaSuccess) c = ssdx::cut_rows(rows, p->V, ws + L.off_xdv, dv, st);
     if (c == cudaSuccess) c = ssdx::sum_channels(rows, (const float *)(ws + L.off_xdg), dg, st);
     if (c == cudaSuccess && dh0) c = ssdx::cut_states(mats, p->V, (const float *)(ws + L.off_xdh0), dh0, st);
     return cuda_status(c);

@@ -150,16 +150,12 @@ size_t fwd_smem(int64_t K);
 size_t bwd_smem(int64_t K, int64_t V);
 }  // namespace simt
 
-// SSD through the GLA tensor-core kernels (ssd_gla.cu): layout changes
-// between the SSD problem and the equivalent GLA problem (K = V = 128,
-// q / k per head, gate per channel).
+// SSD through the GLA tensor-core kernels (ssd_gla.cu): the states padded
+// to V = 128 and back, the per-head dq / dk summed over each q / k group,
+// dg summed over K.
 namespace ssdx {
-cudaError_t expand(int64_t BT, int64_t H, int64_t Hqk, int64_t V, const void *q, const void *k, const void *v,
-                   const float *g, const void *dO, void *xq, void *xk, void *xv, float *xg, void *xdo,
-                   cudaStream_t st);
 cudaError_t pad_states(int64_t mats, int64_t V, const float *src, float *dst, cudaStream_t st);
 cudaError_t cut_states(int64_t mats, int64_t V, const float *src, float *dst, cudaStream_t st);
-cudaError_t cut_rows(int64_t rows, int64_t V, const void *src, void *dst, cudaStream_t st);
 cudaError_t reduce_heads(int64_t BT, int64_t H, int64_t Hqk, const void *x, void *out, cudaStream_t st);
 cudaError_t sum_channels(int64_t rows, const float *x, float *dg, cudaStream_t st);
 }  // namespace ssdx

@@ -6,45 +6,19 @@
 // scalar special case of the per-channel decay): with g_gla[t,h,c] =
 // g_ssd[t,h] for all c the recurrences coincide,
 //   S_t = exp(g_t) S_{t-1} + k_t v_t^T,   o_t = scale S_t^T q_t.
-// The tensor-core kernels read q and k of a head's group and the per-head
-// gate in place (their grouped-head and per-head-gate modes).  These kernels
-// only zero-pad v, do, h0 and dht to V = 128, and map the GLA gradients
-// back: dq and dk summed over the heads that share q and k, dg summed over K
-// (the gradient of a gate shared by K channels), dv / dh0 / o / final state
-// cut to V columns.
+// The tensor-core kernels read q and k of a head's group, the per-head gate
+// and the V-column v and do in place (their grouped-head and per-head-gate
+// modes; v's and do's columns past V read as zeros), and write o and dv in
+// place.  These kernels pad h0 and dht to V = 128 and cut the final state and
+// dh0 back, and map the GLA gradients back: dq and dk summed over the heads
+// that share q and k, dg summed over K (the gradient of a gate shared by K
+// channels).
 #include "internal.cuh"
 
 namespace glacore {
 namespace ssdx {
 
 constexpr int KX = 128, VX = 128;
-
-// One warp per (token, head), 16-byte chunks (V % 8 == 0).  Writes xv (v
-// padded) and, where not null, xq, xk (q, k of the head's group), xg (gate
-// broadcast over K) and xdo (do padded).
-__global__ void expand_kernel(int64_t rows, int64_t H, int64_t Hqk, int64_t V, const uint4 *q, const uint4 *k,
-                              const uint4 *v, const float *g, const uint4 *dO, uint4 *xq, uint4 *xk, uint4 *xv,
-                              float4 *xg, uint4 *xdo) {
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;  // = t * H + h
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const int64_t t = row / H, h = row - t * H, hq = h / (H / Hqk);
-  const int64_t src = (t * Hqk + hq) * (KX / 8);  // 16 chunks of 8 bf16 per row
-  const int64_t nv = V / 8;                       // chunks of a v / do row
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  if (lane < 16) {
-    if (xq) xq[row * (KX / 8) + lane] = q[src + lane];
-    xv[row * (VX / 8) + lane] = lane < nv ? v[row * nv + lane] : zero;
-  } else {
-    const int l = lane - 16;
-    if (xk) xk[row * (KX / 8) + l] = k[src + l];
-    if (xdo) xdo[row * (VX / 8) + l] = l < nv ? dO[row * nv + l] : zero;
-  }
-  if (xg) {
-    const float gv = g[row];
-    xg[row * (KX / 4) + lane] = make_float4(gv, gv, gv, gv);
-  }
-}
 
 // states [n*H, K, V] <-> [n*H, K, 128] (pad with zeros / cut)
 __global__ void pad_state_kernel(int64_t mats, int64_t V, const float *src, float *dst) {
@@ -58,14 +32,6 @@ __global__ void cut_state_kernel(int64_t mats, int64_t V, const float *src, floa
   if (i >= mats * KX * V) return;
   const int64_t c = i % V, rowk = i / V;
   dst[i] = src[rowk * VX + c];
-}
-// [rows, 128] bf16 -> [rows, V] bf16, 16-byte chunks
-__global__ void cut_rows_kernel(int64_t rows, int64_t V, const uint4 *src, uint4 *dst) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t nv = V / 8;
-  if (i >= rows * nv) return;
-  const int64_t r = i / nv, c = i - r * nv;
-  dst[i] = src[r * (VX / 8) + c];
 }
 // dq / dk: sum over the G = H / Hqk heads of a group, fp32, rounded once.
 // One thread per (token, group, 8 channels).
@@ -106,16 +72,6 @@ __global__ void sum_channels_kernel(int64_t rows, const float4 *x, float *dg) {
 
 static unsigned blocks_of(int64_t n, int per) { return (unsigned)((n + per - 1) / per); }
 
-cudaError_t expand(int64_t BT, int64_t H, int64_t Hqk, int64_t V, const void *q, const void *k, const void *v,
-                   const float *g, const void *dO, void *xq, void *xk, void *xv, float *xg, void *xdo,
-                   cudaStream_t st) {
-  const int64_t rows = BT * H;
-  expand_kernel<<<blocks_of(rows, 8), 256, 0, st>>>(rows, H, Hqk, V, (const uint4 *)q, (const uint4 *)k,
-                                                   (const uint4 *)v, g, (const uint4 *)dO, (uint4 *)xq,
-                                                   (uint4 *)xk, (uint4 *)xv, (float4 *)xg, (uint4 *)xdo);
-  mark_launch("ssd_expand", st);
-  return cudaGetLastError();
-}
 cudaError_t pad_states(int64_t mats, int64_t V, const float *src, float *dst, cudaStream_t st) {
   pad_state_kernel<<<blocks_of(mats * KX * VX, 256), 256, 0, st>>>(mats, V, src, dst);
   mark_launch("ssd_pad_state", st);
@@ -124,11 +80,6 @@ cudaError_t pad_states(int64_t mats, int64_t V, const float *src, float *dst, cu
 cudaError_t cut_states(int64_t mats, int64_t V, const float *src, float *dst, cudaStream_t st) {
   cut_state_kernel<<<blocks_of(mats * KX * V, 256), 256, 0, st>>>(mats, V, src, dst);
   mark_launch("ssd_cut_state", st);
-  return cudaGetLastError();
-}
-cudaError_t cut_rows(int64_t rows, int64_t V, const void *src, void *dst, cudaStream_t st) {
-  cut_rows_kernel<<<blocks_of(rows * (V / 8), 256), 256, 0, st>>>(rows, V, (const uint4 *)src, (uint4 *)dst);
-  mark_launch("ssd_cut_rows", st);
   return cudaGetLastError();
 }
 cudaError_t reduce_heads(int64_t BT, int64_t H, int64_t Hqk, const void *x, void *out, cudaStream_t st) {

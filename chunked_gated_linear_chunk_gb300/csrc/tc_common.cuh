@@ -240,12 +240,13 @@ __device__ __forceinline__ void store_block_f32(float *row0, int64_t stride, con
           make_float4(v[4 * s], v[4 * s + 1], v[4 * s + 2], v[4 * s + 3]);
   }
 }
+// cmax: the block's columns at or past cmax are skipped.
 __device__ __forceinline__ void store_block_bf16(__nv_bfloat16 *row0, int64_t stride, const float (&v)[16],
-                                                 int lane, int t_in_chunk0, int L) {
+                                                 int lane, int t_in_chunk0, int L, int cmax = 32) {
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int t = 4 * s + (lane & 3);
-    if (t_in_chunk0 + t < L) {
+    if (t_in_chunk0 + t < L && 4 * (lane >> 2) < cmax) {
       uint2 w;
       w.x = pack_bf16(v[4 * s], v[4 * s + 1]);
       w.y = pack_bf16(v[4 * s + 2], v[4 * s + 3]);

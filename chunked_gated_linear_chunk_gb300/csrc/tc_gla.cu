@@ -40,7 +40,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   memset(&maps, 0, sizeof(maps));
   if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
-      !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
+      !make_map(&maps.v, pr.v, true, pr.V, pr.H, BT, 64) ||
       (!pr.gate_head && !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32)))
     return cudaErrorInvalidValue;
   FwdArgs a;
@@ -49,6 +49,7 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   a.H = pr.H;
   a.hq_div = (int32_t)(pr.H / pr.Hqk);
   a.gate_head = pr.gate_head;
+  a.vd = (int32_t)pr.V;
   a.scale = pr.scale;
   a.g = pr.g;
   a.h0 = pr.h0;

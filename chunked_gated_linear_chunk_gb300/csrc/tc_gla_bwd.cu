@@ -42,6 +42,8 @@ struct BwdArgs {
   int64_t H;
   int32_t hq_div;     // heads per q / k head (q, k are [BT, H / hq_div, K]); 0 or 1: one each
   int32_t gate_head;  // 1: g is [BT, H], one log-decay per head for all key channels
+  int32_t vd;         // value columns of v, do and dv (64 or 128); the kernels compute
+                      // 128, reading the missing columns as zeros
   float scale;
   const float *g;
   const float *h0;     // [n_docs,H,K,V] or null
@@ -242,8 +244,10 @@ __global__ void __launch_bounds__(448, 1)
           const int tp = tok + 2 * C;
           for (int x = 0; x < 128; x += 64) {
             tma_prefetch_3d(&maps.k, x, hq, tp);
-            tma_prefetch_3d(&maps.v, x, h, tp);
-            tma_prefetch_3d(&maps.dO, x, h, tp);
+            if (x < a.vd) {  // v and do have vd columns
+              tma_prefetch_3d(&maps.v, x, h, tp);
+              tma_prefetch_3d(&maps.dO, x, h, tp);
+            }
           }
           if (!HG)
             for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
@@ -785,9 +789,9 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           const int tp = tok - 2 * C;
           for (int x = 0; x < 128; x += 64) {
             tma_prefetch_3d(&maps.qt, x, h, tp);
-            tma_prefetch_3d(&maps.dO, x, h, tp);
+            if (x < a.vd) tma_prefetch_3d(&maps.dO, x, h, tp);  // v and do have vd columns
             tma_prefetch_3d(&maps.kt, x, h, tp);
-            tma_prefetch_3d(&maps.v, x, h, tp);
+            if (x < a.vd) tma_prefetch_3d(&maps.v, x, h, tp);
           }
         }
         mbar_expect_tx(&full[st], 2 * 16384);
@@ -824,7 +828,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         if (s1 - tok0 >= C) {
           for (int x = 0; x < 2; ++x) {
             tma_store_3d(&maps.dk, sm + bsm::KV + st * 32768 + x * 16384, 64 * x, h, (int)tok0);
-            tma_store_3d(&maps.dv, sm + bsm::KV + st * 32768 + x * 16384 + 8192, 64 * x, h, (int)tok0);
+            if (64 * x < a.vd)  // dv has vd columns
+              tma_store_3d(&maps.dv, sm + bsm::KV + st * 32768 + x * 16384 + 8192, 64 * x, h, (int)tok0);
           }
           bulk_commit();
           bulk_wait_read_all();
@@ -1028,7 +1033,8 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
             for (int w = 0; w < 16; ++w) sts_u16(vc.at(16 * blk + w), f32_to_bf16_bits(dvv[w]));
           } else {
             transpose_4x4_blocks(dvv, lane);
-            store_block_bf16(a.dv + ((tok0 + tb) * H + h) * VD + 32 * qw, H * VD, dvv, lane, tb, L);
+            store_block_bf16(a.dv + ((tok0 + tb) * H + h) * a.vd + 32 * qw, H * a.vd, dvv, lane, tb, L,
+                             a.vd - 32 * qw);
           }
         }
         tc_fence_before();
@@ -1206,12 +1212,12 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   float *dgp = (float *)(ws + Lo.off_dgp);
   if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
       !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
-      !make_map(&maps.v, pr.v, true, VD, pr.H, BT, 64) ||
-      !make_map(&maps.dO, dO, true, VD, pr.H, BT, 64) ||
+      !make_map(&maps.v, pr.v, true, pr.V, pr.H, BT, 64) ||
+      !make_map(&maps.dO, dO, true, pr.V, pr.H, BT, 64) ||
       !make_map(&maps.dq, dq, true, KD, pr.H, BT, 64) ||
       (!pr.gate_head && !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32)) ||
       !make_map(&maps.dk, dk, true, KD, pr.H, BT, 64) ||
-      !make_map(&maps.dv, dv, true, VD, pr.H, BT, 64) ||
+      !make_map(&maps.dv, dv, true, pr.V, pr.H, BT, 64) ||
       !make_map(&maps.qt, ws + Lo.off_qt, true, KD, pr.H, BT, 64) ||
       !make_map(&maps.kt, ws + Lo.off_kt, true, KD, pr.H, BT, 64))
     return cudaErrorInvalidValue;
@@ -1221,6 +1227,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   a.H = pr.H;
   a.hq_div = (int32_t)(pr.H / pr.Hqk);
   a.gate_head = pr.gate_head;
+  a.vd = (int32_t)pr.V;
   a.scale = pr.scale;
   a.g = pr.g;
   a.h0 = pr.h0;
@@ -1260,7 +1267,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     FwdMaps fm, rm;
     memset(&fm, 0, sizeof(fm));
     if (!make_map(&fm.q, pr.q, true, KD, pr.Hqk, BT, 64) || !make_map(&fm.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
-        !make_map(&fm.v, pr.v, true, VD, pr.H, BT, 64) ||
+        !make_map(&fm.v, pr.v, true, pr.V, pr.H, BT, 64) ||
         (!pr.gate_head && !make_map(&fm.g, pr.g, false, KD, pr.H, BT, 32)))
       return cudaErrorInvalidValue;
     rm = fm;
@@ -1272,6 +1279,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     fa.H = pr.H;
     fa.hq_div = a.hq_div;
     fa.gate_head = a.gate_head;
+    fa.vd = a.vd;
     fa.scale = pr.scale;
     fa.g = pr.g;
     fa.err = pr.err;

@@ -55,13 +55,15 @@ struct FwdArgs {
   int64_t H;
   int32_t hq_div;     // heads per q / k head (q, k are [BT, H / hq_div, K]); 0 or 1: one each
   int32_t gate_head;  // 1: g is [BT, H], one log-decay per head for all key channels
+  int32_t vd;         // value columns of v and o (64 or 128); the kernels compute 128,
+                      // reading v's missing columns as zeros (TMA fill)
   float scale;
   const float *g;
   const float *h0;    // [n_docs,H,K,V] state entering the document, or null
   float *ht;          // [n_docs,H,K,V] final state (written by the last piece)
   float *lbuf;        // [units,H,K,V] piece end state from zero (written by the piece pass)
   float *dbuf;        // [units,H,K] exp(sum of g over the piece) (written by the piece pass)
-  __nv_bfloat16 *o;
+  __nv_bfloat16 *o;   // [BT, H, vd]
   int *err;
 };
 
@@ -294,7 +296,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
             tma_prefetch_3d(&maps.q, 64, hq, tp);
             tma_prefetch_3d(&maps.k, 0, hq, tp);
             tma_prefetch_3d(&maps.k, 64, hq, tp);
-            tma_prefetch_3d(&maps.v, vb * 64, h, tp);
+            if (vb * 64 < a.vd) tma_prefetch_3d(&maps.v, vb * 64, h, tp);
           }
         }
         // this CTA's half of the q / k channels (the peer writes the other
@@ -484,10 +486,13 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         tmem_ld16(tO + lane_off + cp * 16 + 16, r[1]);
         tmem_ld_wait(r[0]);
         tmem_tie(r[1]);
-        if (lane < 16 && prow < L) {
+        // o has 128 columns, or in the per-head-gate instance a.vd (64 or
+        // 128): a value half at or past them stores nothing
+        const int Lo = (!HG || (int)(blockIdx.x & 1) * 64 < a.vd) ? L : 0;
+        if (lane < 16 && prow < Lo) {
 #pragma unroll
           for (int hc = 0; hc < 2; ++hc) {
-            __nv_bfloat16 *dst = a.o + ((tok0 + prow) * H + h) * VD + v0 + (cp + hc) * 16;
+            __nv_bfloat16 *dst = a.o + ((tok0 + prow) * H + h) * (HG ? (int64_t)a.vd : (int64_t)VD) + v0 + (cp + hc) * 16;
             const uint32_t *x = r[hc];
             st_global_v4(dst, pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
                          pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
