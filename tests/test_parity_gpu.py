@@ -87,6 +87,13 @@ SMALL = {
     "gla_bf16_pieces_T1000_nostate": lambda: case(2, 14, B=1, T=1000, H=1, Hqk=1),
     "gla_bf16_pieces_packed": lambda: case(4, 15, B=1, T=3000, H=1, Hqk=1, doc_mean=700),
     "gla_bf16_pieces_B2_H2": lambda: case(5, 16, B=2, T=1500, H=2, Hqk=2),
+    # SSD split into pieces (the piece passes in their grouped-head and
+    # per-head-gate modes), two heads on one B / C group
+    "ssd_bf16_pieces_T2000": lambda: case(3, 17, B=1, T=2000, H=2),
+    # SSD with V = 128 (both value halves stored) and two B / C groups
+    "ssd_bf16_V128_groups2": lambda: case(3, 18, B=1, T=200, H=4, Hqk=2, V=128),
+    # SSD with V < 64: the fp32 CUDA-core kernels
+    "ssd_bf16_V32": lambda: case(3, 19, B=1, T=130, H=2, V=32),
 }
 
 
