@@ -26,7 +26,9 @@
 // reads row c of TMEM and owns channel c for the suffix sums.  Thread roles
 // as in the forward: warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 prep
 // (thread = one key channel x 32 tokens; it stages exp(+-G) into its own
-// TMEM lane), warps 10..13 epilogue.
+// TMEM lane), warps 10..13 epilogue.  SSD runs the same kernels with one
+// gate per head, q / k shared by a group of heads and V = 64 read as 128
+// columns (BwdArgs: gate_head, hq_div, vd).
 #include <string.h>
 
 #include "tc_gla_fwd.cuh"
@@ -155,9 +157,10 @@ constexpr uint32_t BYTES = 224256;
 }  // namespace asm_
 
 // Thread roles: warp 0 lane 0 TMA loads of k, v, do; lane 1 TMA loads of
-// raw q; lane 2 TMA stores of dq and qt; lane 3
-// TMA loads of the gate tile; lane 4 TMA stores of kt.  Pass B takes the
-// gated operands qt, kt from here instead of gating q and k again.  Warp 1
+// raw q; lane 2 TMA stores of dq and qt; lane 3 TMA loads of the gate tile
+// (per-channel gates; a per-head gate is staged by 64 of the per-channel
+// threads instead); lane 4 TMA stores of kt.  Pass B takes the gated
+// operands qt, kt from here instead of gating q and k again.  Warp 1
 // MMA + TMEM.  Warps 2..9 per-channel warps (key channel c = lane of the
 // warp's TMEM quarter, token half th): gate work and kt for chunk j, then
 // the dq / q (.) dq epilogue of chunk j-1 for their half, written to shared
@@ -706,12 +709,12 @@ constexpr uint32_t BND = 217088;   // 2 x 128 fp32: exact gate-gradient carry at
 constexpr uint32_t BYTES = 218112;
 }  // namespace bsm
 
-// Thread roles: warp 0 lane 0 TMA loads of q, do; lane 1 TMA loads of k, v;
-// lane 2 TMA loads of the gate-gradient partials and TMA stores of dk, dv,
-// dg.  Warp 1 MMA + TMEM.  Warps 2..9 per-channel warps (key channel /
-// value column c, token half th): qt, kt and exp(-G) of chunk i, then the
-// dk / dg / dv epilogue of chunk i-1, written over kt, v and the partials.
-// Warps 10..13 mask P and dP and scale the state gradient.
+// Thread roles: warp 0 lane 0 TMA loads of qt, do; lane 1 TMA loads of kt,
+// v; lane 2 TMA stores of dk, dv.  Warp 1 MMA + TMEM.  Warps 2..9
+// per-channel warps (key channel / value column c, token half th): exp(-G)
+// of chunk i (written by pass A) into TMEM, then the dk / dg / dv epilogue
+// of chunk i-1, dk and dv written over kt and v for the TMA stores.  Warps
+// 10..13 scale the state gradient and mask P and dP.
 __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdArgs &a, unsigned bx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);

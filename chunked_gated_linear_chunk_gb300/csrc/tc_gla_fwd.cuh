@@ -33,11 +33,15 @@ namespace glacore {
 namespace tc {
 
 // =========================================================================
-// Forward: grid (2 * n_docs, H), 448 threads (x = 2 * doc + value half),
-// clusters of two CTAs along x.  One CTA owns one document, one head and
-// 64 value columns and walks the document's chunks in order; the two CTAs
-// of a cluster (the value halves) split the gate / q / k prep by key channel
-// and exchange the prepared tiles through distributed shared memory.
+// Forward: a one-dimensional grid of 2 x units x H CTAs (a unit is a
+// document or a piece of one; x = 2 (rank H + head) + value half, units in
+// launch order), 448 threads, clusters of two CTAs along x.  One CTA owns
+// one unit, one head and 64 value columns and walks the unit's chunks in
+// order; the two CTAs of a cluster (the value halves) split the gate / q / k
+// prep by key channel and exchange the prepared tiles through distributed
+// shared memory.  SSD runs the same kernel with one gate per head, q / k
+// shared by a group of heads and V = 64 read as 128 columns (FwdArgs:
+// gate_head, hq_div, vd).
 //   warp 0      TMA producer (3-stage ring of q, k, v tiles; L2 prefetch of
 //               gates and of the tiles two chunks ahead)
 //   warp 1      TMEM owner and MMA issuer
