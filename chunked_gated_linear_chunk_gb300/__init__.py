@@ -27,13 +27,13 @@ import torch
 
 __all__ = [
     "GlacoreError", "load", "gla_fwd", "gla_bwd", "ssd_fwd", "ssd_bwd", "count_docs",
-    "get_device_error", "workspace_size", "Problem",
+    "get_device_error", "workspace_size", "Problem", "selftest_wait",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libglacore.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_DOCS = range(7)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_DOCS, ERR_RANGE = range(8)
 F32, BF16 = 0, 1
 
 EXPORTS = (
@@ -41,6 +41,7 @@ EXPORTS = (
     "ssd_fwd_workspace_size", "ssd_bwd_workspace_size", "glacore_count_docs",
     "glacore_get_device_error", "glacore_status_string", "glacore_version",
     "glacore_set_timing_events", "glacore_timing_count", "glacore_timing_label", "gla_bwd_noalloc",
+    "glacore_selftest_wait",
 )
 
 
@@ -112,6 +113,8 @@ def load(path: str | None = None):
         lib.glacore_timing_count.argtypes = []
         lib.glacore_timing_label.restype = ctypes.c_char_p
         lib.glacore_timing_label.argtypes = [ctypes.c_int]
+        lib.glacore_selftest_wait.restype = ctypes.c_int
+        lib.glacore_selftest_wait.argtypes = [ctypes.c_int64, P]
         if path is None:
             _lib = lib
         return lib
@@ -202,6 +205,14 @@ def get_device_error():
     _check(load().glacore_get_device_error(_stream(torch.cuda.current_device())), "device")
 
 
+def selftest_wait(cycles: int, device=None):
+    """Runs the library's bounded-wait self-test on the current stream: a
+    wait that can never complete, with a limit of ``cycles`` SM clocks.  The
+    timeout lands in the device error word (read it with get_device_error)."""
+    dev = torch.cuda.current_device() if device is None else device
+    _check(load().glacore_selftest_wait(int(cycles), _stream(dev)), "selftest_wait")
+
+
 def _problem(q, k, v, g, scale, segment_ids, initial_state, chunk_size, n_seqs, head_gate):
     q, k, v = _contig(q), _contig(k), _contig(v)
     g = _contig(g, torch.float32)
@@ -252,7 +263,7 @@ def _workspace(p, kind, device, workspace):
 
 
 def _fwd(kind, q, k, v, g, scale=None, segment_ids=None, initial_state=None,
-         output_final_state=False, chunk_size=64, n_seqs=None, out=None, final_out=None,
+         output_final_state=False, chunk_size=0, n_seqs=None, out=None, final_out=None,
          workspace=None, poison=False):
     head_gate = kind == "ssd"
     p, keep = _problem(q, k, v, g, scale, segment_ids, initial_state, chunk_size, n_seqs, head_gate)
@@ -270,7 +281,7 @@ def _fwd(kind, q, k, v, g, scale=None, segment_ids=None, initial_state=None,
 
 
 def _bwd(kind, q, k, v, g, do, scale=None, segment_ids=None, initial_state=None, dht=None,
-         chunk_size=64, n_seqs=None, outs=None, workspace=None, poison=False):
+         chunk_size=0, n_seqs=None, outs=None, workspace=None, poison=False):
     head_gate = kind == "ssd"
     p, keep = _problem(q, k, v, g, scale, segment_ids, initial_state, chunk_size, n_seqs, head_gate)
     dev = keep[0].device
@@ -297,26 +308,26 @@ def _bwd(kind, q, k, v, g, do, scale=None, segment_ids=None, initial_state=None,
 
 
 def gla_fwd(q, k, v, g, scale=None, segment_ids=None, initial_state=None, output_final_state=False,
-            chunk_size=64, n_seqs=None, **kw):
+            chunk_size=0, n_seqs=None, **kw):
     """GLA forward.  Returns (o, final_state or None)."""
     return _fwd("gla", q, k, v, g, scale, segment_ids, initial_state, output_final_state, chunk_size,
                 n_seqs, **kw)
 
 
-def gla_bwd(q, k, v, g, do, scale=None, segment_ids=None, initial_state=None, dht=None, chunk_size=64,
+def gla_bwd(q, k, v, g, do, scale=None, segment_ids=None, initial_state=None, dht=None, chunk_size=0,
             n_seqs=None, **kw):
     """GLA backward.  Returns (dq, dk, dv, dg, dh0 or None)."""
     return _bwd("gla", q, k, v, g, do, scale, segment_ids, initial_state, dht, chunk_size, n_seqs, **kw)
 
 
 def ssd_fwd(q, k, v, g, scale=1.0, segment_ids=None, initial_state=None, output_final_state=False,
-            chunk_size=64, n_seqs=None, **kw):
+            chunk_size=0, n_seqs=None, **kw):
     """Mamba-2 SSD forward (g is the per-head log decay [B,T,H])."""
     return _fwd("ssd", q, k, v, g, scale, segment_ids, initial_state, output_final_state, chunk_size,
                 n_seqs, **kw)
 
 
-def ssd_bwd(q, k, v, g, do, scale=1.0, segment_ids=None, initial_state=None, dht=None, chunk_size=64,
+def ssd_bwd(q, k, v, g, do, scale=1.0, segment_ids=None, initial_state=None, dht=None, chunk_size=0,
             n_seqs=None, **kw):
     """Mamba-2 SSD backward.  Returns (dq, dk, dv, dg, dh0 or None)."""
     return _bwd("ssd", q, k, v, g, do, scale, segment_ids, initial_state, dht, chunk_size, n_seqs, **kw)

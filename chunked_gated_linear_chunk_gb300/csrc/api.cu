@@ -4,8 +4,11 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.cuh"
 #include "tc.cuh"
+#include "tc_ptx.cuh"
 
 namespace glacore {
 
@@ -27,17 +30,21 @@ void mark_launch(const char *label, cudaStream_t st) {
 }
 
 // Device address of g_device_error for the current device (looked up once
-// per device; kernels receive it as an argument).
+// per device; kernels receive it as an argument).  The cache entries are
+// atomics: host threads may look the address up concurrently (they store
+// the same value).
 static int *device_error_ptr() {
-  static int *cache[128] = {nullptr};
+  static std::atomic<int *> cache[128];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-  if (!cache[dev]) {
+  int *p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
-    cache[dev] = (int *)ptr;
+    p = (int *)ptr;
+    cache[dev].store(p, std::memory_order_release);
   }
-  return cache[dev];
+  return p;
 }
 
 // ---- segment preparation (one CTA; documents numbered row-major) ------
@@ -118,6 +125,22 @@ cudaError_t launch_prep(const int32_t *seg, int64_t B, int64_t T, int64_t n_seqs
   return cudaGetLastError();
 }
 
+// ---- self-test of the bounded waits -------------------------------------
+//
+// One thread waits, through the kernels' own bounded wait (ptx::mbar_wait),
+// on a shared-memory mbarrier that nothing ever arrives on: phase 0 never
+// completes, the limit runs out and the timeout is recorded exactly as a
+// kernel records it.  No copy, MMA or tensor memory is in flight.
+__global__ void wait_selftest_kernel(long long cycles, int *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, cycles)) set_device_error(err, GLACORE_ERR_TIMEOUT);
+}
+
 // ---- argument checks ----------------------------------------------------
 
 namespace {
@@ -145,7 +168,7 @@ glacore_status check_problem(const glacore_problem *p, bool head_gate) {
   if (p->dtype != GLACORE_F32 && p->dtype != GLACORE_BF16) return GLACORE_ERR_INVALID_ARG;
   if (p->reserved0 != 0) return GLACORE_ERR_INVALID_ARG;
   if (p->chunk_size < 0) return GLACORE_ERR_INVALID_ARG;
-  if (p->chunk_size != 0 && p->chunk_size != 64 && p->chunk_size != 128)
+  if (p->chunk_size != 0 && p->chunk_size != 16 && p->chunk_size != 32 && p->chunk_size != 64)
     return GLACORE_ERR_UNSUPPORTED;
   if (p->B > (int64_t)1 << 31 || p->T > (int64_t)1 << 31 || p->H > 65535)
     return GLACORE_ERR_INVALID_ARG;
@@ -161,7 +184,12 @@ glacore_status check_problem(const glacore_problem *p, bool head_gate) {
   return GLACORE_OK;
 }
 
-bool simt_supported(const glacore_problem *p) { return p->K <= 128 && p->V <= 128; }
+// The CUDA-core kernels take any K, V up to 128 at chunk 16 (chunk_size 0
+// or 16), and chunks of 32 or 64 where their shared memory fits.
+int simt_chunk(const glacore_problem *p) { return p->chunk_size ? p->chunk_size : simt::SC_DEFAULT; }
+bool simt_supported(const glacore_problem *p) {
+  return p->K <= 128 && p->V <= 128 && simt::chunk_fits(p->K, p->V, simt_chunk(p));
+}
 
 // The shape of the GLA problem an SSD problem is run as (ssd_gla.cu): K and
 // V of 128, every head its own q / k.  It is checked and laid out so; the
@@ -187,7 +215,7 @@ Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
   memset(&L, 0, sizeof(L));
   L.tc = tc::supported(p, head_gate, backward);
   L.ssdx = !L.tc && ssdx_supported(p, head_gate, backward);
-  L.chunk = (L.tc || L.ssdx) ? tc::C : simt::SC;
+  L.chunk = (L.tc || L.ssdx) ? tc::C : simt_chunk(p);
   const int64_t BT = p->B * p->T, n = p->n_seqs;
   size_t off = 0;
   if (p->segment_ids) {
@@ -314,7 +342,7 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
   }
   const Prob pr = make_prob(p, head_gate);
   if (L.tc) return cuda_status(tc::fwd(pr, docs, p, o, ht, ws + L.off_tc, st));
-  return cuda_status(simt::launch_fwd(pr, docs, p->dtype, o, ht, nullptr, st));
+  return cuda_status(simt::launch_fwd(pr, docs, p->dtype, L.chunk, o, ht, nullptr, st));
 }
 
 glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
@@ -368,7 +396,7 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
     return cuda_status(tc::bwd(pr, docs, p, dO, dht, dq, dk, dv, dg, dh0, ws + L.off_tc, st));
   float *states = (float *)(ws + L.off_states);
   float *fin = (float *)(ws + L.off_final);
-  cudaError_t e = simt::launch_fwd(pr, docs, p->dtype, nullptr, fin, states, st);
+  cudaError_t e = simt::launch_fwd(pr, docs, p->dtype, L.chunk, nullptr, fin, states, st);
   if (e != cudaSuccess) return GLACORE_ERR_CUDA;
   float *accq = nullptr, *acck = nullptr;
   if (p->Hqk != p->H) {
@@ -378,7 +406,7 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
     if (cudaMemsetAsync(accq, 0, nb, st) != cudaSuccess) return GLACORE_ERR_CUDA;
     if (cudaMemsetAsync(acck, 0, nb, st) != cudaSuccess) return GLACORE_ERR_CUDA;
   }
-  e = simt::launch_bwd(pr, docs, p->dtype, dO, dht, states, fin, dq, dk, accq, acck, dv, dg,
+  e = simt::launch_bwd(pr, docs, p->dtype, L.chunk, dO, dht, states, fin, dq, dk, accq, acck, dv, dg,
                        dh0, st);
   if (e != cudaSuccess) return GLACORE_ERR_CUDA;
   if (accq) {
@@ -451,6 +479,14 @@ glacore_status glacore_get_device_error(glacore_stream_t stream) {
   return (glacore_status)h;
 }
 
+glacore_status glacore_selftest_wait(int64_t cycles, glacore_stream_t stream) {
+  if (cycles < 1 || cycles > ((int64_t)1 << 40)) return GLACORE_ERR_INVALID_ARG;
+  int *err = device_error_ptr();
+  if (!err) return GLACORE_ERR_CUDA;
+  wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)cycles, err);
+  return cuda_status(cudaGetLastError());
+}
+
 const char *glacore_status_string(glacore_status s) {
   switch (s) {
     case GLACORE_OK: return "ok";
@@ -460,6 +496,9 @@ const char *glacore_status_string(glacore_status s) {
     case GLACORE_ERR_TIMEOUT: return "bounded device wait ran out";
     case GLACORE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case GLACORE_ERR_DOCS: return "segment_ids holds a different number of documents than n_seqs";
+    case GLACORE_ERR_RANGE:
+      return "a chunk's summed log-decay is below the kernels' range (-80 per chunk; chunk_size 16 "
+             "covers stronger decay)";
   }
   return "unknown status";
 }

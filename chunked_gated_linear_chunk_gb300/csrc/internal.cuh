@@ -129,25 +129,28 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(x);
 }
 
-// ---- SIMT path (fp32 arithmetic; any K, V with K * V <= 16384) ----------
+// ---- SIMT path (fp32 arithmetic; chunk of 16, 32 or 64 tokens) ---------
 namespace simt {
-constexpr int SC = 16;  // chunk length used by the SIMT kernels
-constexpr int SV = 32;  // value columns per forward CTA
+constexpr int SC_DEFAULT = 16;  // chunk length of the SIMT kernels unless the caller asks for another
+constexpr int SV = 32;          // value columns per forward CTA
+constexpr size_t kMaxSmem = 227 * 1024;  // dynamic shared memory per CTA
 
-// Forward / state pass.  o may be null (state pass).  ws_states: if non-null,
-// the fp32 state entering every chunk is written to
-// ws_states[(cbase + j) * H + h][K][V].  ht: final state or null.
-cudaError_t launch_fwd(const Prob &p, const Docs &docs, int dtype, void *o, float *ht,
+// Forward / state pass with chunks of sc (16, 32 or 64) tokens.  o may be null
+// (state pass).  ws_states: if non-null, the fp32 state entering every chunk
+// is written to ws_states[(cbase + j) * H + h][K][V].  ht: final state or null.
+cudaError_t launch_fwd(const Prob &p, const Docs &docs, int dtype, int sc, void *o, float *ht,
                        float *ws_states, cudaStream_t st);
 // Backward gradient pass over chunks in reverse (reads ws_states and the
 // final states written by the state pass).
-cudaError_t launch_bwd(const Prob &p, const Docs &docs, int dtype, const void *dO,
+cudaError_t launch_bwd(const Prob &p, const Docs &docs, int dtype, int sc, const void *dO,
                        const float *dht, const float *ws_states, const float *ws_final,
                        void *dq, void *dk, float *dq_acc, float *dk_acc, void *dv, float *dg,
                        float *dh0, cudaStream_t st);
 cudaError_t launch_convert(const float *src, void *dst, int dtype, int64_t n, cudaStream_t st);
-size_t fwd_smem(int64_t K);
-size_t bwd_smem(int64_t K, int64_t V);
+size_t fwd_smem(int64_t K, int sc);
+size_t bwd_smem(int64_t K, int64_t V, int sc);
+// True when both kernels' shared memory fits for chunks of sc tokens.
+bool chunk_fits(int64_t K, int64_t V, int sc);
 }  // namespace simt
 
 // SSD through the GLA tensor-core kernels (ssd_gla.cu): the states padded

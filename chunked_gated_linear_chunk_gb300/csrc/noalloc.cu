@@ -13,6 +13,8 @@
 // host code its name is only a host-side stand-in, so its device address is
 // looked up once per device with cudaGetSymbolAddress (with that device
 // current) and passed on like any workspace pointer.
+#include <atomic>
+
 #include "internal.cuh"
 
 namespace glacore {
@@ -24,16 +26,18 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 // Device address of g_noalloc_scratch on the current device; the first call
 // on each device does the lookup.
+// The cache entries are atomics: host threads may race on the first lookup
+// (they store the same address).
 static glacore_status noalloc_scratch(void **out) {
-  static void *cache[128] = {nullptr};
+  static std::atomic<void *> cache[128];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return GLACORE_ERR_CUDA;
-  if (!cache[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return GLACORE_ERR_CUDA;
-    cache[dev] = ptr;
+  void *p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GLACORE_ERR_CUDA;
+    cache[dev].store(p, std::memory_order_release);
   }
-  *out = cache[dev];
+  *out = p;
   return GLACORE_OK;
 }
 

@@ -2,9 +2,14 @@
 //
 // This is the instance used for fp32 inputs (where tensor-core bf16/tf32
 // rounding would exceed a 1e-4 relative error) and for head sizes the
-// tensor-core kernels do not cover.  It evaluates the same chunk formulas
-// as the tensor-core path, with a short chunk (SC = 16 tokens) so that the
-// per-chunk decay factors stay well inside the fp32 exponent range:
+// tensor-core kernels do not cover, and for any problem whose caller asks
+// for chunk_size 16 or 32.  It evaluates the same chunk formulas as the
+// tensor-core path with chunks of SC = 16, 32 or 64 tokens (a template
+// parameter; 16 unless the caller asks otherwise): the short chunk keeps
+// the per-chunk decay factors inside the fp32 exponent range for much
+// stronger decay.  A chunk whose summed log-decay in some channel is below
+// -80 sets GLACORE_ERR_RANGE (exp(-G) would approach the fp32 limit of
+// about exp(88)).
 //
 //   FLAT blog, "Linear Attention / Forward Recurrence" (chunkwise form) and
 //   "Gated Linear Attention" (decay ratios as exponentiated chunk-local
@@ -35,12 +40,16 @@ __device__ __forceinline__ float gate_at(const Prob &p, int64_t tok, int64_t h, 
   return p.gate_head ? p.g[tok * p.H + h] : p.g[(tok * p.H + h) * p.K + c];
 }
 
-size_t fwd_smem(int64_t K) {
+size_t fwd_smem(int64_t K, int SC) {
   return sizeof(float) * (size_t)(K * SV + 2 * SC * K + SC * SV + SC * SC + K);
 }
 
+// Lowest summed log-decay of one chunk in one channel that the chunk
+// formulas keep inside the fp32 exponent range.
+constexpr float kMinChunkLogDecay = -80.f;
+
 // grid (n_docs, H, ceil(V / SV)), 256 threads.
-template <typename T>
+template <typename T, int SC>
 __global__ void __launch_bounds__(256) fwd_kernel(Prob p, Docs docs, T *o, float *ht, float *ws) {
   const int64_t d = blockIdx.x, h = blockIdx.y, v0 = (int64_t)blockIdx.z * SV;
   const int64_t K = p.K, V = p.V;
@@ -89,6 +98,7 @@ __global__ void __launch_bounds__(256) fwd_kernel(Prob p, Docs docs, T *o, float
         }
       }
       gam[c] = G;
+      if (!(G >= kMinChunkLogDecay)) set_device_error(p.err, GLACORE_ERR_RANGE);
     }
     for (int i = tid; i < SC * SV; i += nt) {
       const int t = i / SV, j = i % SV;
@@ -133,13 +143,13 @@ __global__ void __launch_bounds__(256) fwd_kernel(Prob p, Docs docs, T *o, float
   }
 }
 
-size_t bwd_smem(int64_t K, int64_t V) {
+size_t bwd_smem(int64_t K, int64_t V, int SC) {
   return sizeof(float) * (size_t)(2 * K * V + 8 * SC * K + 2 * SC * V + 2 * SC * SC + 2 * K + SC);
 }
 
 // grid (n_docs, H), 256 threads.  Reads the fp32 chunk-entry states
 // (ws) and the final states (wsfin) written by the state pass.
-template <typename T>
+template <typename T, int SC>
 __global__ void __launch_bounds__(256)
     bwd_kernel(Prob p, Docs docs, const T *dO, const float *dht, const float *ws,
                const float *wsfin, T *dq, T *dk, float *dq_acc, float *dk_acc, T *dv, float *dg,
@@ -205,6 +215,7 @@ __global__ void __launch_bounds__(256)
         }
       }
       gam[c] = G;
+      if (!(G >= kMinChunkLogDecay)) set_device_error(p.err, GLACORE_ERR_RANGE);
     }
     for (int64_t i = tid; i < SC * V; i += nt) {
       const int t = (int)(i / V);
@@ -299,48 +310,67 @@ __global__ void convert_kernel(const float *src, T *dst, int64_t n) {
     dst[i] = from_f32<T>(src[i]);
 }
 
-cudaError_t launch_fwd(const Prob &p, const Docs &docs, int dtype, void *o, float *ht,
-                       float *ws_states, cudaStream_t st) {
-  if (docs.n == 0) return cudaSuccess;
+template <typename T, int SC>
+static cudaError_t fwd_as(const Prob &p, const Docs &docs, void *o, float *ht, float *ws_states,
+                          cudaStream_t st) {
   dim3 grid((unsigned)docs.n, (unsigned)p.H, (unsigned)((p.V + SV - 1) / SV));
-  const size_t smem = fwd_smem(p.K);
-  if (dtype == GLACORE_BF16) {
-    auto k = fwd_kernel<__nv_bfloat16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, 256, smem, st>>>(p, docs, (__nv_bfloat16 *)o, ht, ws_states);
-    mark_launch(o ? "simt_fwd" : "simt_state_pass", st);
-  } else {
-    auto k = fwd_kernel<float>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, 256, smem, st>>>(p, docs, (float *)o, ht, ws_states);
-    mark_launch(o ? "simt_fwd" : "simt_state_pass", st);
-  }
+  const size_t smem = fwd_smem(p.K, SC);
+  auto k = fwd_kernel<T, SC>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, 256, smem, st>>>(p, docs, (T *)o, ht, ws_states);
+  mark_launch(o ? "simt_fwd" : "simt_state_pass", st);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const Prob &p, const Docs &docs, int dtype, const void *dO,
+bool chunk_fits(int64_t K, int64_t V, int sc) {
+  return (sc == 16 || sc == 32 || sc == 64) && fwd_smem(K, sc) <= kMaxSmem && bwd_smem(K, V, sc) <= kMaxSmem;
+}
+
+cudaError_t launch_fwd(const Prob &p, const Docs &docs, int dtype, int sc, void *o, float *ht,
+                       float *ws_states, cudaStream_t st) {
+  if (docs.n == 0) return cudaSuccess;
+  if (dtype == GLACORE_BF16) {
+    using T = __nv_bfloat16;
+    return sc == 64   ? fwd_as<T, 64>(p, docs, o, ht, ws_states, st)
+           : sc == 32 ? fwd_as<T, 32>(p, docs, o, ht, ws_states, st)
+                      : fwd_as<T, 16>(p, docs, o, ht, ws_states, st);
+  }
+  using T = float;
+  return sc == 64   ? fwd_as<T, 64>(p, docs, o, ht, ws_states, st)
+         : sc == 32 ? fwd_as<T, 32>(p, docs, o, ht, ws_states, st)
+                    : fwd_as<T, 16>(p, docs, o, ht, ws_states, st);
+}
+
+template <typename T, int SC>
+static cudaError_t bwd_as(const Prob &p, const Docs &docs, const void *dO, const float *dht,
+                          const float *ws_states, const float *ws_final, void *dq, void *dk,
+                          float *dq_acc, float *dk_acc, void *dv, float *dg, float *dh0, cudaStream_t st) {
+  dim3 grid((unsigned)docs.n, (unsigned)p.H);
+  const size_t smem = bwd_smem(p.K, p.V, SC);
+  auto k = bwd_kernel<T, SC>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, 256, smem, st>>>(p, docs, (const T *)dO, dht, ws_states, ws_final, (T *)dq, (T *)dk, dq_acc,
+                             dk_acc, (T *)dv, dg, dh0);
+  mark_launch("simt_bwd", st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const Prob &p, const Docs &docs, int dtype, int sc, const void *dO,
                        const float *dht, const float *ws_states, const float *ws_final, void *dq,
                        void *dk, float *dq_acc, float *dk_acc, void *dv, float *dg, float *dh0,
                        cudaStream_t st) {
   if (docs.n == 0) return cudaSuccess;
-  dim3 grid((unsigned)docs.n, (unsigned)p.H);
-  const size_t smem = bwd_smem(p.K, p.V);
+#define GLACORE_SIMT_BWD(T, SCV) \
+  bwd_as<T, SCV>(p, docs, dO, dht, ws_states, ws_final, dq, dk, dq_acc, dk_acc, dv, dg, dh0, st)
   if (dtype == GLACORE_BF16) {
     using T = __nv_bfloat16;
-    auto k = bwd_kernel<T>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, 256, smem, st>>>(p, docs, (const T *)dO, dht, ws_states, ws_final, (T *)dq,
-                               (T *)dk, dq_acc, dk_acc, (T *)dv, dg, dh0);
-    mark_launch("simt_bwd", st);
-  } else {
-    using T = float;
-    auto k = bwd_kernel<T>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, 256, smem, st>>>(p, docs, (const T *)dO, dht, ws_states, ws_final, (T *)dq,
-                               (T *)dk, dq_acc, dk_acc, (T *)dv, dg, dh0);
-    mark_launch("simt_bwd", st);
+    return sc == 64 ? GLACORE_SIMT_BWD(T, 64) : sc == 32 ? GLACORE_SIMT_BWD(T, 32) : GLACORE_SIMT_BWD(T, 16);
   }
-  return cudaGetLastError();
+  using T = float;
+  return sc == 64 ? GLACORE_SIMT_BWD(T, 64) : sc == 32 ? GLACORE_SIMT_BWD(T, 32) : GLACORE_SIMT_BWD(T, 16);
+#undef GLACORE_SIMT_BWD
 }
 
 cudaError_t launch_convert(const float *src, void *dst, int dtype, int64_t n, cudaStream_t st) {

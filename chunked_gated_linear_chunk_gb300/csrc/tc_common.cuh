@@ -13,6 +13,12 @@ using namespace ptx;
 
 constexpr long long WAIT_CYCLES = 4000000000LL;  // ~2 s: bounded waits
 
+// Smallest total decay exp(sum of g over a chunk) of one channel that the
+// chunk-local factorisation exp(G_t) * exp(-G_s) keeps inside the fp32 /
+// bf16 exponent range: exp(-80).  A chunk below it makes the kernel record
+// GLACORE_ERR_RANGE (its outputs are then not valid).
+constexpr float kMinChunkDecay = 1.8048513e-35f;
+
 typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -321,6 +327,46 @@ __device__ __forceinline__ void mask_rows_to_smem(uint32_t t_acc, int r0, int la
       tmem_tie(a1);
       if (cp <= rb) mask_block_store(tile, row, cp, a0, cp == rb, row & 15);
       if (cp + 1 <= rb) mask_block_store(tile, row, cp + 1, a1, cp + 1 == rb, row & 15);
+    }
+  }
+}
+// The rounding residue of a masked tile: lo = bf16(x - bf16(x)) for the
+// blocks at or below the diagonal (the masked entries are 0).  With the
+// tile written by mask_tile_to_smem (hi = bf16(x)), hi + lo carries about
+// 16 bits of the fp32 value, so a product with both (two accumulating MMAs)
+// removes the bf16 rounding of the tile itself.  Same TMEM layout, warp
+// roles and zero-initialised blocks as mask_tile_to_smem.
+__device__ __forceinline__ void mask_block_store_lo(uint8_t *tile, int row, int cb, const uint32_t (&r)[16],
+                                                    bool diag, int lane) {
+#pragma unroll
+  for (int hb = 0; hb < 2; ++hb) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i0 = hb * 8 + 2 * e;
+      const float x0 = (!diag || i0 <= lane) ? __uint_as_float(r[i0]) : 0.f;
+      const float x1 = (!diag || i0 + 1 <= lane) ? __uint_as_float(r[i0 + 1]) : 0.f;
+      const uint32_t hi = pack_bf16(x0, x1);
+      w[e] = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+    }
+    st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), w[0], w[1], w[2], w[3]);
+  }
+}
+__device__ __forceinline__ void mask_tile_lo_to_smem(uint32_t t_acc, uint32_t lane_off, int qw, int lane,
+                                                     uint8_t *tile) {
+  const int row = qw * 16 + lane;
+#pragma unroll
+  for (int cp = 0; cp < 4; cp += 2) {
+    if (cp <= qw) {
+      uint32_t r0[16], r1[16];
+      tmem_ld16(t_acc + lane_off + cp * 16, r0);
+      tmem_ld16(t_acc + lane_off + cp * 16 + 16, r1);
+      tmem_ld_wait(r0);
+      tmem_tie(r1);
+      if (lane < 16) {
+        mask_block_store_lo(tile, row, cp, r0, cp == qw, lane);
+        if (cp + 1 <= qw) mask_block_store_lo(tile, row, cp + 1, r1, cp + 1 == qw, lane);
+      }
     }
   }
 }

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(448, 1)
       prep_done[asm_::NS], dp_full, dp_ready, dq_full[2], dq_free[2], u_full, s_ready, eg_ready[2],
       eg_free[2], out_ready, stg_free, g_full[2], g_free[2], kt_read[asm_::NS];
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
+  __shared__ int abort_flag, range_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // blockIdx.x = r H + h: launch rank r (units in launch order), head h
@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(448, 1)
   }
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    range_flag = 0;
     for (int i = 0; i < asm_::NS; ++i) {
       mbar_init(&full[i], 1);    // k, v, do (released by the MMA commit)
       mbar_init(&empty[i], 1);
@@ -421,6 +422,8 @@ __global__ void __launch_bounds__(448, 1)
         if (!mbar_wait(&full[st], (ph_full >> st) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
         ph_full ^= 1u << st;
         exchange_gates(cg, reinterpret_cast<float *>(sm + asm_::XCH) + b * 256, c, th, L);
+        // decay outside the range of the chunk-local factorisation (NaN too)
+        if (th == 0 && !(cg.total >= kMinChunkDecay)) range_flag = 1;
         // exp(G_t) -> TMEM (dq scaling; column 63 = exp(Gam) for the state step)
         if (j >= 2) {
           if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
@@ -686,6 +689,7 @@ __global__ void __launch_bounds__(448, 1)
   tc_fence_before();
   __syncthreads();
   if (*abortp && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_TIMEOUT);
+  if (range_flag && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_RANGE);
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 

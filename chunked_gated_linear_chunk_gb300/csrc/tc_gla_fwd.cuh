@@ -12,6 +12,12 @@
 //   P   = (qt kt^T) masked to s <= t
 //   O   = qt S + P V          S <- diag(exp(Gam)) (S + kt^T V)
 //
+// The masked P enters P V as two bf16 tiles, hi = bf16(P) and
+// lo = bf16(P - hi), so that its own rounding does not add to the error of
+// o (which is rounded to bf16 once more when it is stored).  The lo half is
+// built after the state step and its product issued after the next chunk's
+// readout, so it stays off the chunk-to-chunk chain.
+//
 // The fp32 state S never leaves the SM between chunks (FLAT's "keep the
 // state on-chip"; FLA instead writes every chunk state to HBM).  All
 // matrix products run on tcgen05 (bf16 operands from shared memory,
@@ -76,11 +82,11 @@ constexpr int NS = 3;             // q/k/v pipeline stages
 constexpr uint32_t Q = 0;         // 3 x 16 KB: q, then qt in place
 constexpr uint32_t K = 49152;     // 3 x 16 KB: k, then kt in place
 constexpr uint32_t V = 98304;     // 3 x 8 KB (64 value columns)
-constexpr uint32_t P = 122880;    // 2 x 8 KB: masked P (bf16, K-major A)
-constexpr uint32_t S = 139264;    // 2 x 16 KB: S (bf16, rows = key channel)
-constexpr uint32_t GAM = 172032;  // 4 x 128 fp32: exp(chunk gate total)
-constexpr uint32_t XCH = 174080;  // 8 KB: token-group gate products (two buffers per prep group)
-constexpr uint32_t BYTES = 182272;
+constexpr uint32_t P = 122880;    // 2 x 16 KB: masked P as bf16 hi (+0) and lo (+8 KB) tiles (K-major A)
+constexpr uint32_t S = 155648;    // 2 x 16 KB: S (bf16, rows = key channel)
+constexpr uint32_t GAM = 188416;  // 4 x 128 fp32: exp(chunk gate total)
+constexpr uint32_t XCH = 190464;  // 8 KB: token-group gate products (two buffers per prep group)
+constexpr uint32_t BYTES = 198656;
 }  // namespace fsm
 
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
@@ -224,9 +230,9 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[fsm::NS], empty[fsm::NS], prep_done[fsm::NS], p_full[2], u_full[2],
-      o_full[2], p_ready[2], s_ready[2], gam_ready[4];
+      o_full[2], p_ready[2], p_lo_ready[2], s_ready[2], gam_ready[4];
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
+  __shared__ int abort_flag, range_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the two value halves of a (unit, head) are a cluster of two CTAs that
@@ -249,6 +255,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   }
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    range_flag = 0;
     for (int i = 0; i < fsm::NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 2);        // the MMA commits of both CTAs (multicast)
@@ -259,6 +266,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       mbar_init(&u_full[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&p_ready[i], 128);
+      mbar_init(&p_lo_ready[i], 128);
       mbar_init(&s_ready[i], 128);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 129);
@@ -318,12 +326,29 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       constexpr uint32_t idP = idesc_bf16(64, 64, false, false);
       constexpr uint32_t idO = idesc_bf16(64, 64, false, true);
       constexpr uint32_t idU = idesc_bf16(128, 64, true, true);
-      uint32_t ph_prep = 0, ph_pr = 0, ph_sr = 0;  // one parity bit per buffer
+      uint32_t ph_prep = 0, ph_pr = 0, ph_sr = 0, ph_lo = 0;  // one parity bit per buffer
+      // the second half of chunk j's P V (the P_lo tile) is issued after
+      // chunk j+1's readout, so that the lo tile is built while the tensor
+      // core runs other work; its commit releases the output tile and the
+      // q / k / v stage of chunk j
+      auto finish = [&](int jj) -> bool {
+        const int bb = jj & 1, sst = jj % fsm::NS;
+        if (!mbar_wait(&p_lo_ready[bb], (ph_lo >> bb) & 1, WAIT_CYCLES)) return false;
+        ph_lo ^= 1u << bb;
+        tc_fence_after();
+        const uint32_t Plo = sbase + fsm::P + bb * 16384 + 8192, vaa = sbase + fsm::V + sst * 8192;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tbase + 256 + 64 * bb, kdesc(Plo, ks, 64), mdesc(vaa, ks, 8192), idO, 1);
+        mma_commit(&o_full[bb]);
+        mma_commit_multicast(&empty[sst], 3);
+        return true;
+      };
       for (int j = 0; j < nch; ++j) {
         const int b = j & 1, st = j % fsm::NS;
         const uint32_t qa = sbase + fsm::Q + st * 16384, ka = sbase + fsm::K + st * 16384;
         const uint32_t va = sbase + fsm::V + st * 8192;
-        const uint32_t Pa = sbase + fsm::P + b * 8192, Sa = sbase + fsm::S + (b ^ 1) * 16384;
+        const uint32_t Pa = sbase + fsm::P + b * 16384, Sa = sbase + fsm::S + (b ^ 1) * 16384;
         const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
         if (!mbar_wait_cluster(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) {
           FAIL_AND_BREAK
@@ -345,11 +370,13 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(qa, ks, 64), mdesc(Sa, ks, 16384), idO, ks);
+        // P V as (P_hi + P_lo) V: the hi half now, the lo half after the
+        // next chunk's readout
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tO, kdesc(Pa, ks, 64), mdesc(va, ks, 8192), idO, 1);
-        mma_commit(&o_full[b]);
-        mma_commit_multicast(&empty[st], 3);
+        if (j >= 1 && !finish(j - 1)) FAIL_AND_BREAK
       }
+      if (nch > 0 && !*abortp && !finish(nch - 1)) atomicExch(&abort_flag, 1);
       // every commit that targets this CTA's stage barriers has landed
       // before the CTAs leave (the peer's arrive on our barriers and ours on
       // its): wait for the last phase of each stage
@@ -396,10 +423,13 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       // this CTA's 64-column block of q, k and its gate totals (byte offsets)
       const uint32_t qo = fsm::Q + s * 16384 + vb * 8192, ko = fsm::K + s * 16384 + vb * 8192,
                      go = fsm::GAM + (j & 3) * 512 + vb * 256;
-      prep_chunk_pair<16>(sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
-                          reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
-                          reinterpret_cast<float *>(sm + fsm::XCH) + (2 * grp + ((j >> 1) & 1)) * 512, tg, lane,
-                          vb, L, a.scale, true, false, false, make_float2(1.f, 1.f), 1 + grp, 128);
+      const float2 gam = prep_chunk_pair<16>(
+          sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
+          reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
+          reinterpret_cast<float *>(sm + fsm::XCH) + (2 * grp + ((j >> 1) & 1)) * 512, tg, lane, vb, L, a.scale,
+          true, false, false, make_float2(1.f, 1.f), 1 + grp, 128);
+      // decay outside the range of the chunk-local factorisation (NaN too)
+      if (tg == 0 && !(fminf(gam.x, gam.y) >= kMinChunkDecay)) range_flag = 1;
       fence_async_smem();
       // copy the prepared blocks into the peer's tiles (bulk copies that
       // complete on the peer's barriers; one arrive there stands for the
@@ -431,57 +461,20 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
       piece_state_in<64>(S, h0row, a.lbuf, a.dbuf, u - un.piece, un.piece, H, h, c, v0);
     }
-    mask_tile_init(sm + fsm::P, qw, lane);
-    mask_tile_init(sm + fsm::P + 8192, qw, lane);
+    for (int t = 0; t < 4; ++t) mask_tile_init(sm + fsm::P + t * 8192, qw, lane);
     store_state_bf16(sm + fsm::S + 16384, c, S);
     fence_async_smem();
     mbar_arrive(&s_ready[1]);
     uint32_t ph_p = 0, ph_u = 0, ph_o = 0;
-    for (int j = 0; j < nch; ++j) {
-      const int b = j & 1;
-      const int64_t tok0 = chunk_tok(j);
+    // S3b: output tile O = qt S_prev + P V of chunk jj, stored one chunk
+    // late (its P_lo half is issued after the next chunk's readout)
+    auto store_o = [&](int jj) -> bool {
+      const int bb = jj & 1;
+      const int64_t tok0 = chunk_tok(jj);
       const int L = (int)min((int64_t)C, s1 - tok0);
-      const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
-      // S2: P -> causal mask -> bf16 A operand of the intra-chunk product
-      if (!mbar_wait(&p_full[b], (ph_p >> b) & 1, WAIT_CYCLES)) {
-        FAIL_AND_BREAK
-      }
-      ph_p ^= 1u << b;
-      tc_fence_after();
-      mask_tile_to_smem(tP, lane_off, qw, lane, sm + fsm::P + b * 8192);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_ready[b]);
-      // S3a: state update S <- exp(Gam) (S + kt^T V), bf16 copy for the next readout
-      if (!mbar_wait(&u_full[b], (ph_u >> b) & 1, WAIT_CYCLES) ||
-          !mbar_wait_cluster(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
-        FAIL_AND_BREAK
-      }
-      ph_u ^= 1u << b;
-      tc_fence_after();
-      const float eG = reinterpret_cast<const float *>(sm + fsm::GAM)[(j & 3) * 128 + c];
-#pragma unroll
-      for (int cp = 0; cp < 4; cp += 2) {
-        uint32_t r[16], r2[16];
-        tmem_ld16(tU + lane_off + cp * 16, r);
-        tmem_ld16(tU + lane_off + cp * 16 + 16, r2);
-        tmem_ld_wait(r);
-        tmem_tie(r2);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          S[cp * 16 + i] = eG * (S[cp * 16 + i] + __uint_as_float(r[i]));
-          S[cp * 16 + 16 + i] = eG * (S[cp * 16 + 16 + i] + __uint_as_float(r2[i]));
-        }
-      }
-      store_state_bf16(sm + fsm::S + b * 16384, c, S);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&s_ready[b]);
-      // S3b: output tile O = qt S_prev + P V
-      if (!mbar_wait(&o_full[b], (ph_o >> b) & 1, WAIT_CYCLES)) {
-        FAIL_AND_BREAK
-      }
-      ph_o ^= 1u << b;
+      const uint32_t tO = tbase + 256 + 64 * bb;
+      if (!mbar_wait(&o_full[bb], (ph_o >> bb) & 1, WAIT_CYCLES)) return false;
+      ph_o ^= 1u << bb;
       tc_fence_after();
 #pragma unroll
       for (int cp = 0; cp < 4; cp += 2) {
@@ -510,7 +503,54 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         }
       }
       tc_fence_before();
+      return true;
+    };
+    for (int j = 0; j < nch; ++j) {
+      const int b = j & 1;
+      const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b;
+      // S2: P -> causal mask -> bf16 A operand (hi) of the intra-chunk product
+      if (!mbar_wait(&p_full[b], (ph_p >> b) & 1, WAIT_CYCLES)) {
+        FAIL_AND_BREAK
+      }
+      ph_p ^= 1u << b;
+      tc_fence_after();
+      mask_tile_to_smem(tP, lane_off, qw, lane, sm + fsm::P + b * 16384);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_ready[b]);
+      // S3a: state update S <- exp(Gam) (S + kt^T V), bf16 copy for the next readout
+      if (!mbar_wait(&u_full[b], (ph_u >> b) & 1, WAIT_CYCLES) ||
+          !mbar_wait_cluster(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
+        FAIL_AND_BREAK
+      }
+      ph_u ^= 1u << b;
+      tc_fence_after();
+      const float eG = reinterpret_cast<const float *>(sm + fsm::GAM)[(j & 3) * 128 + c];
+#pragma unroll
+      for (int cp = 0; cp < 4; cp += 2) {
+        uint32_t r[16], r2[16];
+        tmem_ld16(tU + lane_off + cp * 16, r);
+        tmem_ld16(tU + lane_off + cp * 16 + 16, r2);
+        tmem_ld_wait(r);
+        tmem_tie(r2);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          S[cp * 16 + i] = eG * (S[cp * 16 + i] + __uint_as_float(r[i]));
+          S[cp * 16 + 16 + i] = eG * (S[cp * 16 + 16 + i] + __uint_as_float(r2[i]));
+        }
+      }
+      store_state_bf16(sm + fsm::S + b * 16384, c, S);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s_ready[b]);
+      // the rounding residue of P (lo tile), off the readout's path
+      mask_tile_lo_to_smem(tP, lane_off, qw, lane, sm + fsm::P + b * 16384 + 8192);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_lo_ready[b]);
+      if (j >= 1 && !store_o(j - 1)) FAIL_AND_BREAK
     }
+    if (nch > 0 && !*abortp && !store_o(nch - 1)) atomicExch(&abort_flag, 1);
     float *dst = a.ht && last_piece ? a.ht + ((d * H + h) * KD + c) * VD + v0 : nullptr;
     if (dst && !*abortp) {
 #pragma unroll
@@ -522,6 +562,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   __syncwarp();
   cluster_sync();  // no remote access to this CTA's shared memory after this point
   if (*abortp && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_TIMEOUT);
+  if (range_flag && threadIdx.x == 0) set_device_error(a.err, GLACORE_ERR_RANGE);
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 

@@ -16,6 +16,8 @@
 // tc.cuh); the local states come from piece_state_kernel below.  This file
 // also builds the unit table and the launch order of packed documents and
 // sizes the workspace.
+#include <atomic>
+
 #include "tc_gla_fwd.cuh"
 
 namespace glacore {
@@ -341,8 +343,21 @@ cudaError_t launch_order_units(const Units &us, int64_t n, int32_t *order, cudaS
 // Piece length: split documents only when (documents x heads x CTAs per
 // unit) leaves most of the GPU's SMs idle, and then into about as many
 // pieces as make one wave.
+// SMs of the current device (one CTA of the chunk-walking kernels per SM).
+static int64_t sm_count() {
+  static std::atomic<int> cache[128];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 int64_t piece_len(const glacore_problem *p, bool backward) {
-  const int64_t sms = 148;  // one CTA per SM (GB300: 152 SMs)
+  const int64_t sms = sm_count();
   const int64_t per_unit = backward ? 1 : 2;
   const int64_t units = p->n_seqs * p->H * per_unit;
   const int64_t never = (int64_t)1 << 40;

@@ -40,8 +40,19 @@
  *  - Host-side validation runs before any launch; on failure nothing is
  *    enqueued and an error status is returned.
  *  - Inconsistencies that only the device can see (the number of documents
- *    in segment_ids differs from n_seqs) set a device error word instead of
- *    trapping; read it with glacore_get_device_error.
+ *    in segment_ids differs from n_seqs; a decay outside the kernels'
+ *    range) set a device error word instead of trapping; read it with
+ *    glacore_get_device_error.
+ *  - Decay range.  Inside a chunk the kernels evaluate exp(G_t - G_s) as
+ *    exp(G_t) * exp(-G_s), with G the prefix sum of g from the chunk start
+ *    (FLAT blog, "Gated Linear Attention": decay ratios as exponentiated
+ *    chunk-local prefix sums).  That product stays inside the fp32 / bf16
+ *    exponent range while the summed log-decay of every chunk, in every
+ *    key channel, is at least -80.  A call that meets a chunk below that
+ *    sets GLACORE_ERR_RANGE and its outputs are not valid.  The CUDA-core
+ *    kernels (chunk_size 16) have the same bound per 16 tokens, so they
+ *    cover decays four times stronger: up to an average log-decay of -5
+ *    per token, against -1.25 on the tensor-core path.
  *  - Pointers passed to the tensor-core path must be 16-byte aligned.
  *  - Calls on different streams may run concurrently provided they use
  *    different workspace buffers.
@@ -66,7 +77,8 @@ typedef enum {
   GLACORE_ERR_CUDA = 3,        /* a CUDA runtime call failed */
   GLACORE_ERR_TIMEOUT = 4,     /* a bounded device wait ran out */
   GLACORE_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than *_workspace_size */
-  GLACORE_ERR_DOCS = 6         /* device: document count != n_seqs */
+  GLACORE_ERR_DOCS = 6,        /* device: document count != n_seqs */
+  GLACORE_ERR_RANGE = 7        /* device: a chunk's decay is outside the kernels' range (below) */
 } glacore_status;
 
 typedef enum { GLACORE_F32 = 0, GLACORE_BF16 = 1 } glacore_dtype;
@@ -76,9 +88,17 @@ typedef enum { GLACORE_F32 = 0, GLACORE_BF16 = 1 } glacore_dtype;
  *   H           value heads; Hqk heads of q/k (GLA: Hqk == H; SSD: H % Hqk == 0)
  *   K, V        key and value head dims (1..256)
  *   dtype       element type of q, k, v, o, do, dq, dk, dv
- *   chunk_size  chunk length of the chunk-parallel form: 64 (default) or
- *               128; 0 selects 64.  Results do not depend on it beyond
- *               rounding.
+ *   chunk_size  chunk length of the chunk-parallel form: 0, 16, 32 or 64
+ *               (any other value: GLACORE_ERR_UNSUPPORTED).  The tensor-core
+ *               kernels (bf16; GLA with K = V = 128 and one q/k head per
+ *               value head; SSD with K = 128 and V of 64 or 128) run chunks
+ *               of 64 and take chunk_size 0 or 64.  Every other problem, and
+ *               any problem given chunk_size 16 or 32, runs the CUDA-core
+ *               kernels with chunks of chunk_size tokens (0: 16); those take
+ *               32 and 64 only where their shared memory fits (64: K = V =
+ *               64 or smaller; 32: K * V up to about 8192), and
+ *               GLACORE_ERR_UNSUPPORTED otherwise.  Results do not depend
+ *               on it beyond rounding.
  *   scale       output scale (GLA usually K^-1/2; Mamba-2: 1)
  *   n_seqs      number of documents: B when segment_ids is NULL
  *   initial_state  [n_seqs,H,K,V] fp32 or NULL (zero)
@@ -167,9 +187,19 @@ glacore_status glacore_count_docs(const int32_t *segment_ids, int64_t B,
                                   glacore_stream_t stream);
 
 /* Reads and clears the library's device error word (set by kernels for
- * GLACORE_ERR_DOCS or GLACORE_ERR_TIMEOUT).  Synchronises `stream`.
+ * GLACORE_ERR_DOCS, GLACORE_ERR_RANGE or GLACORE_ERR_TIMEOUT).  Synchronises `stream`.
  * Returns GLACORE_OK if no device error was recorded. */
 glacore_status glacore_get_device_error(glacore_stream_t stream);
+
+/* Self-test of the bounded device waits.  Launches one CTA that waits on
+ * a shared-memory mbarrier nothing ever arrives on, with a limit of
+ * `cycles` SM clock cycles (1 .. 2^40), through the same bounded wait the
+ * kernels use; when the limit runs out it records GLACORE_ERR_TIMEOUT in
+ * the device error word and returns.  No copy, tensor-core work or tensor
+ * memory is in flight.  Asynchronous on `stream`; read the result with
+ * glacore_get_device_error.  The pages have no counterpart: it exists so
+ * that the timeout path of every kernel can be shown to end. */
+glacore_status glacore_selftest_wait(int64_t cycles, glacore_stream_t stream);
 
 /* Static English description of a status code. */
 const char *glacore_status_string(glacore_status s);

@@ -36,8 +36,9 @@ def test_library_exports_every_declared_symbol():
 def test_status_strings_and_version():
     lib = glc.load()
     assert lib.glacore_version() >= 100
-    for s in range(7):
+    for s in range(8):
         assert lib.glacore_status_string(s)
+    assert b"range" in lib.glacore_status_string(glc.ERR_RANGE)
     assert b"unknown" in lib.glacore_status_string(99)
 
 
@@ -68,10 +69,49 @@ def test_invalid_arguments_rejected_before_launch(over):
     assert lib.gla_fwd_workspace_size(ctypes.byref(p)) == 0
 
 
-def test_unsupported_chunk_size():
+# (problem fields, status of gla_bwd without a workspace): chunk lengths a
+# kernel family does not run are UNSUPPORTED; the ones it runs get as far as
+# the workspace check (WORKSPACE), before any launch
+CHUNKS = [
+    (dict(chunk_size=128), glc.ERR_UNSUPPORTED),
+    (dict(chunk_size=48), glc.ERR_UNSUPPORTED),
+    (dict(chunk_size=64), glc.ERR_WORKSPACE),  # tensor-core kernels
+    (dict(chunk_size=0), glc.ERR_WORKSPACE),
+    (dict(chunk_size=16), glc.ERR_WORKSPACE),  # CUDA-core kernels on a bf16 problem
+    (dict(chunk_size=32), glc.ERR_UNSUPPORTED),  # CUDA-core chunk 32 does not fit K = V = 128
+    (dict(dtype=glc.F32, chunk_size=64), glc.ERR_UNSUPPORTED),
+    (dict(dtype=glc.F32, K=64, V=64, chunk_size=64), glc.ERR_WORKSPACE),
+    (dict(dtype=glc.F32, K=64, V=64, chunk_size=32), glc.ERR_WORKSPACE),
+    (dict(dtype=glc.F32, K=64, V=64, chunk_size=16), glc.ERR_WORKSPACE),
+    (dict(dtype=glc.F32, K=128, V=64, chunk_size=64), glc.ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("over,status", CHUNKS)
+def test_chunk_size_contract(over, status):
     lib = glc.load()
-    p = make_problem(chunk_size=32)
-    assert lib.gla_fwd(ctypes.byref(p), ctypes.c_void_p(4096), None, None) == glc.ERR_UNSUPPORTED
+    p = make_problem(**over)
+    o = ctypes.c_void_p(4096)
+    assert lib.gla_bwd(ctypes.byref(p), o, None, o, o, o, o, None, None) == status
+    if status == glc.ERR_WORKSPACE:
+        assert lib.gla_bwd_workspace_size(ctypes.byref(p)) > 0
+
+
+def test_chunk_16_workspace_holds_chunk_states():
+    """chunk_size 16 moves a tensor-core problem to the CUDA-core kernels,
+    whose backward keeps the fp32 state entering every 16-token chunk."""
+    lib = glc.load()
+    p = make_problem(chunk_size=16)
+    B, T, H, K, V = p.B, p.T, p.H, p.K, p.V
+    states = B * ((T + 15) // 16) * H * K * V * 4
+    assert lib.gla_bwd_workspace_size(ctypes.byref(p)) >= states
+
+
+def test_selftest_wait_rejects_bad_limits():
+    lib = glc.load()
+    assert lib.glacore_selftest_wait(0, None) == glc.ERR_INVALID_ARG
+    assert lib.glacore_selftest_wait(-5, None) == glc.ERR_INVALID_ARG
+    assert lib.glacore_selftest_wait((1 << 40) + 1, None) == glc.ERR_INVALID_ARG
 
 
 def test_missing_outputs_rejected():

@@ -29,7 +29,7 @@ def np64(t):
     return None if t is None else t.detach().to("cpu", torch.float64).numpy()
 
 
-def run_gpu(d, chunk=64):
+def run_gpu(d, chunk=0):
     w = d["workload"]
     x = inputs.to_device(d, "cuda")
     fwd = glc.gla_fwd if w.kind == "gla" else glc.ssd_fwd
@@ -105,13 +105,21 @@ def test_small_cases_against_oracle(cuda_ok, name):
     compare(gpu, ref, d["workload"].dtype)
 
 
-def test_chunk_size_does_not_change_results(cuda_ok):
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_chunk_size_does_not_change_results_fp32(cuda_ok, chunk):
+    """One kernel family (the fp32 CUDA-core kernels) at three chunk lengths,
+    each against the oracle at the fp32 tolerance: documents that start
+    mid-chunk, a ragged tail and initial / final states."""
+    d = case(4, 11, B=2, T=150, H=2, Hqk=2, K=64, V=64, dtype="fp32", doc_mean=40)
+    compare(run_gpu(d, chunk=chunk), run_oracle(d), "fp32")
+
+
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_chunk_size_does_not_change_results_bf16(cuda_ok, chunk):
+    """The same bf16 problem at chunk 64 (tensor-core kernels) and chunk 16
+    (CUDA-core kernels), each against the oracle."""
     d = case(5, 11, B=1, T=300, H=2, Hqk=2)
-    a = run_gpu(d, chunk=64)
-    b = run_gpu(d, chunk=128)
-    ref = run_oracle(d)
-    compare(a, ref, "bf16")
-    compare(b, ref, "bf16")
+    compare(run_gpu(d, chunk=chunk), run_oracle(d), "bf16")
 
 
 def test_empty_sequence(cuda_ok):
