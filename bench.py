@@ -144,19 +144,46 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------- CPU oracle ----
-def oracle_sample(d, rows, threads=None):
-    """Times the oracle fwd+bwd on batch rows `rows` (all heads); returns
-    seconds.  Workloads with documents or states run whole (rows = all)."""
+def oracle_sample(d, rows, threads=None, heads=None, tokens=None):
+    """Times the oracle fwd+bwd on batch rows `rows`, value heads `heads`
+    (default all) and the first `tokens` tokens of each row (default all),
+    every document of them; returns (seconds, token count scaled to all
+    heads, threads the oracle used, description).  Heads are independent
+    recurrences except where q / k are shared (SSD: one group), so a head
+    subset of a grouped problem keeps whole groups."""
     import oracle
 
-    whole = d["segment_ids"] is not None or d["h0"] is not None or d["dht"] is not None
-    sl = (lambda t: t) if whole else (lambda t: None if t is None else t[rows[0]:rows[-1] + 1])
+    H = d["v"].shape[2]
+    Hqk = d["q"].shape[2]
+    heads = list(range(H)) if heads is None else list(heads)
+    grp = H // Hqk
+    if grp > 1:  # whole q / k groups
+        ng = max(1, len(heads) // grp)
+        heads = list(range(ng * grp))
+    hq = sorted({h // grp for h in heads})
+    T = d["q"].shape[1] if tokens is None else min(tokens, d["q"].shape[1])
+    r = slice(rows[0], rows[-1] + 1)
+    hs = slice(heads[0], heads[-1] + 1)
+    qs = slice(hq[0], hq[-1] + 1)
+    seg = None
+    n_docs = len(rows)
+    if d["segment_ids"] is not None:
+        seg = d["segment_ids"][r, :T]
+        n_docs = oracle.count_docs(seg, seg.shape[0], T)
+    st = lambda t: None if t is None else t[:n_docs, hs]  # the sample's documents come first
+    if d["segment_ids"] is None:
+        st = lambda t: None if t is None else t[r, hs]
+    q, k = d["q"][r, :T, qs], d["k"][r, :T, qs]
+    v, do = d["v"][r, :T, hs], d["do"][r, :T, hs]
+    g = d["g"][r, :T, hs]
+    used = max(1, min(threads or os.cpu_count() or 1, n_docs * len(hq)))
     t0 = time.perf_counter()
-    oracle.fwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), d["scale"], sl(d["segment_ids"]), d["h0"],
-               threads=threads)
-    oracle.bwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), sl(d["do"]), d["scale"], sl(d["segment_ids"]),
-               d["h0"], d["dht"], threads=threads)
-    return time.perf_counter() - t0
+    oracle.fwd(q, k, v, g, d["scale"], seg, st(d["h0"]), threads=threads)
+    oracle.bwd(q, k, v, g, do, d["scale"], seg, st(d["h0"]), st(d["dht"]), threads=threads)
+    secs = time.perf_counter() - t0
+    ntok = q.shape[0] * q.shape[1]
+    what = f"{q.shape[0]} x {q.shape[1]} tokens, heads {heads[0]}..{heads[-1]} of {H}"
+    return secs, ntok * len(heads) / H, used, what
 
 
 def run_reference(args, w):
@@ -170,7 +197,9 @@ def run_reference(args, w):
     threads = min(cores, w.H)
     for _ in range(args.warmup):
         oracle_sample(d, [0], threads)
-    times = [oracle_sample(d, [0], threads) for _ in range(args.steps)]
+    samples = [oracle_sample(d, [0], threads) for _ in range(args.steps)]
+    times = [smp[0] for smp in samples]
+    threads = samples[0][2]
     ms = 1e3 * statistics.mean(times)
     tokens = w.T  # one batch row, all heads
     value = tokens / (ms / 1e3)
@@ -189,22 +218,17 @@ def run_reference(args, w):
 
 
 # -------------------------------------------------------------- GPU arm ----
-def run_glacore(args, w):
+def measure_device(w, dev, steps, warmup, world=1, rank_sync=False):
+    """Times `steps` fwd+bwd steps of workload w with inputs resident in HBM
+    (L2 flushed by a write of twice its size before each step, outside the
+    event pair).  Returns the per-step and per-kernel CUDA-event times and the
+    roofline figures of the step and of its dominant kernel."""
     import torch
 
     import chunked_gated_linear_chunk_gb300 as glc
     from chunked_gated_linear_chunk_gb300 import inputs
     from chunked_gated_linear_chunk_gb300 import roofline as rf
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    glc.load()
     d = inputs.make(w)
     x = inputs.to_device(d, dev)
     scale, n_seqs = d["scale"], d["n_seqs"]
@@ -233,22 +257,19 @@ def run_glacore(args, w):
         bwd_fn(x["q"], x["k"], x["v"], x["g"], x["do"], scale, x["segment_ids"], x["h0"], x["dht"], w.chunk,
                n_seqs, outs=(dq, dk, dv, dg, dh0), workspace=bws)
 
-    def step():
+    for _ in range(warmup):
+        flush.fill_(1)
         fwd_call()
         bwd_call()
-
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
     torch.cuda.synchronize()
     glc.get_device_error()
 
-    K = args.steps
+    K = steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     tfs = [glc.LaunchTimer(16) for _ in range(K)]
     tbs = [glc.LaunchTimer(16) for _ in range(K)]
-    if world > 1:
+    if rank_sync:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
@@ -261,13 +282,12 @@ def run_glacore(args, w):
                 bwd_call()
             ends[i].record()
         torch.cuda.synchronize()
-    if world > 1:
+    if rank_sync:
         torch.distributed.barrier()
     glc.get_device_error()
     clocks = clk.summary()
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_local = statistics.mean(step_ms)
     # per-kernel durations from the library's launch events
     per_kernel = {}
     launches = 0
@@ -285,22 +305,76 @@ def run_glacore(args, w):
         bwd_ms.append(fprev.elapsed_time(prev))
         launches += len(tfs[i].labels) + len(tbs[i].labels)
 
-    ms, value = job_throughput(ms_local, w.B * w.T, world, dev)
-
     peaks, peak_kind = load_peaks()
     shp = shape_of(w, n_seqs)
     flops = rf.fwd_flops(shp) + rf.bwd_flops(shp)
     nbytes = rf.fwd_bytes(shp) + rf.bwd_bytes(shp)
     t_roof = rf.roofline_time_s(flops, nbytes, peaks["bf16_tflops"], peaks["hbm_gbs"])
-    kern_us = {k: 1e3 * statistics.mean(v) for k, v in per_kernel.items()}
+    # a kernel launched several times per step (the fp32 path's state and
+    # gradient passes are one launch each) is summed per step
+    kern_us = {k: 1e3 * sum(v) / K for k, v in per_kernel.items()}
     dom = max(kern_us, key=kern_us.get)
     dom_bytes = rf.kernel_bytes(shp, dom)
-    achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9
+    achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9 if dom_bytes else None
+    return {
+        "d": d, "n_seqs": n_seqs, "nf": nf, "nb": nb, "fwd_fn": fwd_fn, "bwd_fn": bwd_fn,
+        "ms_local": statistics.mean(step_ms), "step_ms": step_ms, "fwd_ms": statistics.mean(fwd_ms),
+        "bwd_ms": statistics.mean(bwd_ms), "kernels_us": kern_us, "launches": launches, "clocks": clocks,
+        "flops": flops, "bytes": nbytes, "t_roof": t_roof, "peaks": peaks, "peak_kind": peak_kind,
+        "dom": dom, "dom_bytes": dom_bytes, "achieved": achieved,
+    }
+
+
+def roofline_entry(m, traffic=None):
+    peaks = m["peaks"]
+    return {"bound": "hbm", "kernel": m["dom"], "achieved": m["achieved"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": (m["achieved"] / peaks["hbm_gbs"]) if m["achieved"] else None, "traffic": traffic,
+            "algorithmic_bytes_per_launch": m["dom_bytes"], "peak_kind": m["peak_kind"]}
+
+
+def cpu_baseline_of(w, d, sample=(None, None, None)):
+    """The oracle (fp64 token by token, as it stands) on the host cores over a
+    bounded sample of workload w: `sample` = (batch rows, heads, tokens per
+    row), None for all.  Returns the cpu_baseline object."""
+    threads = os.cpu_count() or 1
+    nrows, nheads, ntok = sample
+    rows = list(range(w.B if nrows is None else min(nrows, w.B)))
+    heads = list(range(w.H if nheads is None else min(nheads, w.H)))
+    secs, tokens, used, what = oracle_sample(d, rows, threads, heads, ntok)
+    return {"value": tokens / secs, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"fp64 token-by-token oracle fwd+bwd on {what}, {secs:.1f} s on {used} threads "
+                      f"(tokens/s counted over all {w.H} heads)"}
+
+
+# bounded CPU samples of the workloads: (batch rows, heads, tokens per row) of
+# the oracle run, every document of them (a few seconds each on the host cores)
+CPU_SAMPLE = {1: (None, None, None), 2: (None, None, None), 3: (1, None, 1024), 4: (None, 8, 8192),
+              5: (None, 8, 8192)}
+
+
+def run_glacore(args, w):
+    import torch
+
+    import chunked_gated_linear_chunk_gb300 as glc
+    from chunked_gated_linear_chunk_gb300 import inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    glc.load()
+    m = measure_device(w, dev, args.steps, args.warmup, world, rank_sync=world > 1)
+    d, n_seqs = m["d"], m["n_seqs"]
+    ms, value = job_throughput(m["ms_local"], w.B * w.T, world, dev)
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         try:
-            tinfo = json.load(open(tpath)).get(dom)
+            tinfo = json.load(open(tpath)).get(m["dom"])
             if tinfo and tinfo.get("source_sha") == kernel_source_sha():
                 traffic = tinfo.get("dram_bytes_per_launch")
         except (OSError, ValueError):
@@ -309,7 +383,7 @@ def run_glacore(args, w):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, d, dev, world, fwd_fn, bwd_fn, scale, n_seqs, nf, nb)
+        e2e = run_e2e(args, w, d, dev, world, m["fwd_fn"], m["bwd_fn"], d["scale"], n_seqs, m["nf"], m["nb"])
 
     if rank != 0:
         if world > 1:
@@ -317,32 +391,47 @@ def run_glacore(args, w):
         return 0
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rows = list(range(w.B))
-        threads = os.cpu_count() or 1
-        secs = oracle_sample(d, rows, threads)
-        cpu = {"value": len(rows) * w.T / secs, "unit": UNIT, "cores": min(threads, len(rows) * w.H),
-               "kind": "oracle",
-               "sample": f"fp64 token-by-token oracle fwd+bwd over the whole workload ({w.B}x{w.T} tokens, "
-                         f"{w.H} heads), {secs:.1f} s"}
+        cpu = cpu_baseline_of(w, d, CPU_SAMPLE[w.index])
+    # every workload of the build on this GPU (rank 0, one GPU): the headline
+    # one from the run above, the others timed here with fewer steps
+    workloads = None
+    if world == 1 and not args.no_workloads:
+        workloads = {}
+        for wi, wk in sorted(inputs.WORKLOADS.items()):
+            mk = m if wk.name == w.name else measure_device(wk, dev, min(args.steps, 20), 3)
+            tk = wk.B * wk.T / (mk["ms_local"] * 1e-3)
+            entry = {
+                "ms_per_step": mk["ms_local"], "tokens_per_s": tk, "tflops": mk["flops"] / (mk["ms_local"] * 1e-3) / 1e12,
+                "steps": len(mk["step_ms"]),
+                "step_roofline": {"roofline_us": mk["t_roof"] * 1e6, "measured_us": mk["ms_local"] * 1e3,
+                                  "frac": mk["t_roof"] / (mk["ms_local"] * 1e-3), "peak": mk["peak_kind"]},
+                "fwd_ms": mk["fwd_ms"], "bwd_ms": mk["bwd_ms"], "kernels_us": mk["kernels_us"],
+                "roofline": roofline_entry(mk), "dtype": "bf16" if wk.dtype == "bf16" else "f32",
+            }
+            if not args.no_cpu_baseline:
+                entry["cpu_baseline"] = cpu if wk.name == w.name else cpu_baseline_of(wk, mk["d"], CPU_SAMPLE[wi])
+            workloads[wk.name] = entry
+            if mk is not m:
+                del mk
+                torch.cuda.empty_cache()
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": w.chunk,
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}"},
-        "tflops": flops / (ms * 1e-3) / 1e12,
-        "step_roofline": {"roofline_us": t_roof * 1e6, "measured_us": ms * 1e3, "frac": t_roof / (ms * 1e-3),
-                          "peak": peak_kind},
-        "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms),
-        "kernels_us": kern_us,
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes_per_launch": dom_bytes, "peak_kind": peak_kind},
-        "gpu_launches": launches,
-        "clocks": clocks,
+        "tflops": m["flops"] / (ms * 1e-3) / 1e12,
+        "step_roofline": {"roofline_us": m["t_roof"] * 1e6, "measured_us": ms * 1e3, "frac": m["t_roof"] / (ms * 1e-3),
+                          "peak": m["peak_kind"]},
+        "fwd_ms": m["fwd_ms"], "bwd_ms": m["bwd_ms"],
+        "kernels_us": m["kernels_us"],
+        "roofline": roofline_entry(m, traffic),
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -500,6 +589,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="glacore", choices=["glacore", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload entries (all five workloads, timed after the headline one)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX, choices=[1, 2, 3, 4, 5],
                     help="synthetic workload (default 2: GLA B4 H16 T2048 d128 bf16, the headline)")
     ap.add_argument("--ingest-traffic", metavar="NCU_CSV",
