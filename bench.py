@@ -5,7 +5,9 @@ Workload: GLA, B=4 H=16 T=2048 K=V=128, bf16 q/k/v/do, fp32 gates, chunk 64,
 no initial or final state (seeded synthetic inputs, see
 chunked_gated_linear_chunk_gb300/inputs.py).  One step = gla_fwd + gla_bwd
 over that batch.  Inputs are resident in HBM; L2 is flushed (a write of
-twice the L2 size) before every timed step, outside the timed interval.
+twice the L2 size, then a read of it, so no dirty line of the flush is left
+for the timed kernels to write back) before every timed step, outside the
+timed interval.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl glacore|reference]
 
@@ -218,6 +220,20 @@ def run_reference(args, w):
 
 
 # -------------------------------------------------------------- GPU arm ----
+def flush_l2(buf, i):
+    """Flushes L2 before a timed step: writes `buf` (twice the L2 size), then
+    reads it back, so that the dirty lines of the write are written back to
+    HBM here rather than during the timed kernels.  A short spin on the GPU
+    follows, so that the host has enqueued the step's launches before the
+    start event is reached: the events then time the kernels, not the
+    Python call that launches the first of them."""
+    import torch
+
+    buf.fill_(i & 0xFF)
+    buf.view(torch.int32).max()
+    torch.cuda._sleep(400_000)  # about 0.2 ms at the GB300's 2 GHz SM clock
+
+
 def measure_device(w, dev, steps, warmup, world=1, rank_sync=False):
     """Times `steps` fwd+bwd steps of workload w with inputs resident in HBM
     (L2 flushed by a write of twice its size before each step, outside the
@@ -258,7 +274,7 @@ def measure_device(w, dev, steps, warmup, world=1, rank_sync=False):
                n_seqs, outs=(dq, dk, dv, dg, dh0), workspace=bws)
 
     for _ in range(warmup):
-        flush.fill_(1)
+        flush_l2(flush, 1)
         fwd_call()
         bwd_call()
     torch.cuda.synchronize()
@@ -274,7 +290,7 @@ def measure_device(w, dev, steps, warmup, world=1, rank_sync=False):
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             starts[i].record()
             with tfs[i]:
                 fwd_call()
@@ -352,6 +368,116 @@ CPU_SAMPLE = {1: (None, None, None), 2: (None, None, None), 3: (1, None, 1024), 
               5: (None, 8, 8192)}
 
 
+# the operations around the recurrence, at the sizes of the pages' layer:
+# the output norm and gate on the bench workload's o (B4 T2048 H16 V128),
+# the short convolution at the FLAT blog's benchmark shape (B8 S4096,
+# 2048 channels, 4 taps, bias, SiLU)
+FUSIONS = {
+    "norm_gate_bf16_B4_T2048_H16_V128": dict(kind="norm_gate", shape=(4, 2048, 16, 128)),
+    "short_conv_bf16_B8_T4096_D2048_K4_silu": dict(kind="short_conv", shape=(8, 4096, 2048, 4)),
+}
+
+
+def measure_fusion(name, spec, dev, steps, cpu):
+    """Times the forward and the backward of one fused operation (L2 flushed
+    before each, outside the event pairs) and reports GB/s against the
+    measured copy bandwidth; the oracle (numpy fp64, one host thread) runs a
+    bounded slice of the same inputs."""
+    import torch
+
+    import chunked_gated_linear_chunk_gb300 as glc
+
+    peaks, peak_kind = load_peaks()
+    g = torch.Generator("cpu")
+    g.manual_seed(77)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    if spec["kind"] == "norm_gate":
+        B, T, H, V = spec["shape"]
+        o = torch.randn(B, T, H, V, generator=g).to(torch.bfloat16)
+        z = (2.0 * torch.randn(B, T, H, V, generator=g)).to(torch.bfloat16)
+        dy = torch.randn(B, T, H, V, generator=g).to(torch.bfloat16)
+        wt = 1.0 + 0.5 * torch.randn(V, generator=g)
+        od, zd, dyd, wd = (t.to(dev) for t in (o, z, dy, wt))
+        y = torch.empty_like(od)
+        outs = (torch.empty_like(od), torch.empty_like(od), torch.empty(V, device=dev))
+        ws = torch.empty(max(256, int(glc.load().norm_gate_bwd_workspace_size(B * T * H, V))), dtype=torch.uint8,
+                         device=dev)
+        fwd = lambda: glc.norm_gate_fwd(od, zd, wd, 1e-5, out=y)
+        bwd = lambda: glc.norm_gate_bwd(od, zd, wd, dyd, 1e-5, outs=outs, workspace=ws)
+        n = B * T * H * V
+        fbytes, bbytes = 3 * 2 * n, 5 * 2 * n
+        units = B * T
+
+        def oracle_slice():
+            from oracle import fusions as F
+
+            sl = slice(0, T // 16)
+            F.norm_gate_fwd(o[:, sl], z[:, sl], wt, 1e-5)
+            F.norm_gate_bwd(o[:, sl], z[:, sl], wt, dy[:, sl], 1e-5)
+            return B * (T // 16)
+    else:
+        B, T, D, Kc = spec["shape"]
+        x = torch.randn(B, T, D, generator=g).to(torch.bfloat16)
+        dy = torch.randn(B, T, D, generator=g).to(torch.bfloat16)
+        wt = 0.5 * torch.randn(Kc, D, generator=g)
+        bt = 0.1 * torch.randn(D, generator=g)
+        xd, dyd, wd, bd = (t.to(dev) for t in (x, dy, wt, bt))
+        y = torch.empty_like(xd)
+        outs = (torch.empty_like(xd), torch.empty(Kc, D, device=dev), torch.empty(D, device=dev))
+        ws = torch.empty(max(256, int(glc.load().short_conv_bwd_workspace_size(B, T, D, Kc))), dtype=torch.uint8,
+                         device=dev)
+        fwd = lambda: glc.short_conv_fwd(xd, wd, bd, None, True, out=y)
+        bwd = lambda: glc.short_conv_bwd(xd, wd, bd, dyd, None, True, outs=outs, workspace=ws)
+        n = B * T * D
+        fbytes, bbytes = 2 * 2 * n, 3 * 2 * n
+        units = B * T
+
+        def oracle_slice():
+            from oracle import fusions as F
+
+            sl = slice(0, T // 64)
+            F.short_conv_fwd(x[:1, sl], wt, bt)
+            F.short_conv_bwd(x[:1, sl], wt, bt, dy[:1, sl])
+            return T // 64
+
+    def timed(fn):
+        for _ in range(3):
+            flush_l2(flush, 1)
+            fn()
+        ts = []
+        for i in range(steps):
+            flush_l2(flush, i)
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b_.record()
+            ts.append((a, b_))
+        torch.cuda.synchronize()
+        return statistics.mean(x.elapsed_time(y) for x, y in ts) * 1e3  # us
+
+    fus, bus = timed(fwd), timed(bwd)
+    glc.get_device_error()
+    hbm = peaks["hbm_gbs"]
+    entry = {
+        "fwd_us": fus, "bwd_us": bus, "tokens_per_s": units / ((fus + bus) * 1e-6),
+        "fwd_roofline": {"bound": "hbm", "achieved": fbytes / (fus * 1e-6) / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": fbytes / (fus * 1e-6) / 1e9 / hbm, "algorithmic_bytes_per_launch": fbytes,
+                         "peak_kind": peak_kind},
+        "bwd_roofline": {"bound": "hbm", "achieved": bbytes / (bus * 1e-6) / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": bbytes / (bus * 1e-6) / 1e9 / hbm, "algorithmic_bytes_per_launch": bbytes,
+                         "peak_kind": peak_kind},
+        "dtype": "bf16",
+    }
+    if cpu:
+        t0 = time.perf_counter()
+        tok = oracle_slice()
+        secs = time.perf_counter() - t0
+        entry["cpu_baseline"] = {"value": tok / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": f"numpy fp64 oracle fwd+bwd on {tok} tokens of the shape, {secs:.2f} s"}
+    return entry
+
+
 def run_glacore(args, w):
     import torch
 
@@ -414,13 +540,17 @@ def run_glacore(args, w):
             if mk is not m:
                 del mk
                 torch.cuda.empty_cache()
+    fusions = None
+    if world == 1 and not args.no_workloads:
+        fusions = {name: measure_fusion(name, spec, dev, min(args.steps, 20), not args.no_cpu_baseline)
+                   for name, spec in FUSIONS.items()}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": w.chunk,
-                   "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}"},
+                   "l2": "flushed before every timed step (write of 2x L2, then read back; outside the timed events)", "parallelism": f"replicas x{world}"},
         "tflops": m["flops"] / (ms * 1e-3) / 1e12,
         "step_roofline": {"roofline_us": m["t_roof"] * 1e6, "measured_us": ms * 1e3, "frac": m["t_roof"] / (ms * 1e-3),
                           "peak": m["peak_kind"]},
@@ -432,6 +562,7 @@ def run_glacore(args, w):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "workloads": workloads,
+        "fusions": fusions,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

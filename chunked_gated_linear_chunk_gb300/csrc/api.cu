@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "internal.cuh"
@@ -20,6 +21,13 @@ __device__ int g_device_error = 0;
 static thread_local cudaEvent_t *t_events = nullptr;
 static thread_local int t_nev = 0, t_used = 0;
 static thread_local const char *t_labels[64];
+
+static thread_local cudaError_t t_last_cuda = cudaSuccess;
+glacore_status status_of(cudaError_t e) {
+  if (e == cudaSuccess) return GLACORE_OK;
+  t_last_cuda = e;
+  return GLACORE_ERR_CUDA;
+}
 
 void mark_launch(const char *label, cudaStream_t st) {
   if (t_events && t_used < t_nev) {
@@ -141,6 +149,28 @@ __global__ void wait_selftest_kernel(long long cycles, int *err) {
   if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, cycles)) set_device_error(err, GLACORE_ERR_TIMEOUT);
 }
 
+// ---- exact hand-off of states between sequence pieces ------------------
+//
+// JLA product page ("our split is exact"): the recurrence is linear in the
+// state, so the state entering piece r is the fold of the earlier pieces'
+// local end states L and total decays D, and the state gradient leaving
+// piece r the fold of the later pieces' local start-state gradients and
+// decays.  One thread per state element, the pieces in order.
+__global__ void state_scan_kernel(const float *L, const float *D, int64_t R, int64_t mats, int64_t K, int64_t V,
+                                  const float *seed, int64_t r, int reverse, float *out) {
+  const int64_t n = mats * K * V;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t mk = i / V;  // (matrix, key row)
+    float s = seed ? seed[i] : 0.f;
+    if (!reverse) {
+      for (int64_t q = 0; q < r; ++q) s = D[q * mats * K + mk] * s + L[q * n + i];
+    } else {
+      for (int64_t q = R - 1; q > r; --q) s = D[q * mats * K + mk] * s + L[q * n + i];
+    }
+    out[i] = s;
+  }
+}
+
 // ---- argument checks ----------------------------------------------------
 
 namespace {
@@ -180,6 +210,11 @@ glacore_status check_problem(const glacore_problem *p, bool head_gate) {
   }
   if (BT > 0 && (!p->q || !p->k || !p->v || !p->g)) return GLACORE_ERR_INVALID_ARG;
   if (!(p->scale == p->scale)) return GLACORE_ERR_INVALID_ARG;  // NaN scale
+  // token strides of q, k, v: 0 (contiguous) or at least one token's heads
+  if (p->q_stride < 0 || p->k_stride < 0 || p->v_stride < 0) return GLACORE_ERR_INVALID_ARG;
+  if ((p->q_stride && p->q_stride < p->Hqk * p->K) || (p->k_stride && p->k_stride < p->Hqk * p->K) ||
+      (p->v_stride && p->v_stride < p->H * p->V))
+    return GLACORE_ERR_INVALID_ARG;
   (void)head_gate;
   return GLACORE_OK;
 }
@@ -245,6 +280,15 @@ Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
     L.off_tc = off;
     off = align256(off + tc::workspace_bytes(&e, false, backward));
   } else if (L.tc) {
+    if (backward && p->Hqk != p->H) {
+      // shared q / k heads: dq and dk per value head, then summed over the
+      // heads of each group
+      const size_t bf = (size_t)BT * p->H * 128 * 2;
+      L.off_xdq = off;
+      off = align256(off + bf);
+      L.off_xdk = off;
+      off = align256(off + bf);
+    }
     L.off_tc = off;
     off = align256(off + tc::workspace_bytes(p, head_gate, backward));
   } else if (backward) {
@@ -284,15 +328,16 @@ Prob make_prob(const glacore_problem *p, bool head_gate) {
   q.q = p->q;
   q.k = p->k;
   q.v = p->v;
+  q.qs = p->q_stride ? p->q_stride : p->Hqk * p->K;
+  q.ks = p->k_stride ? p->k_stride : p->Hqk * p->K;
+  q.vs = p->v_stride ? p->v_stride : p->H * p->V;
   q.g = p->g;
   q.h0 = p->initial_state;
   q.err = device_error_ptr();
   return q;
 }
 
-glacore_status cuda_status(cudaError_t e) {
-  return e == cudaSuccess ? GLACORE_OK : GLACORE_ERR_CUDA;
-}
+glacore_status cuda_status(cudaError_t e) { return status_of(e); }
 
 Docs make_docs(const glacore_problem *p, const Layout &L, char *ws) {
   Docs d;
@@ -322,7 +367,7 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
     cudaError_t e = launch_prep(p->segment_ids, p->B, p->T, p->n_seqs, L.chunk,
                                 (int64_t *)(ws + L.off_start), (int64_t *)(ws + L.off_cbase),
                                 device_error_ptr(), st);
-    if (e != cudaSuccess) return GLACORE_ERR_CUDA;
+    if (e != cudaSuccess) return status_of(e);
   }
   const Docs docs = make_docs(p, L, ws);
   if (L.ssdx) {
@@ -366,7 +411,7 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
     cudaError_t e = launch_prep(p->segment_ids, p->B, p->T, p->n_seqs, L.chunk,
                                 (int64_t *)(ws + L.off_start), (int64_t *)(ws + L.off_cbase),
                                 device_error_ptr(), st);
-    if (e != cudaSuccess) return GLACORE_ERR_CUDA;
+    if (e != cudaSuccess) return status_of(e);
   }
   const Docs docs = make_docs(p, L, ws);
   if (L.ssdx) {
@@ -392,6 +437,12 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
     return cuda_status(c);
   }
   const Prob pr = make_prob(p, head_gate);
+  if (L.tc && p->Hqk != p->H) {
+    cudaError_t c = tc::bwd(pr, docs, p, dO, dht, ws + L.off_xdq, ws + L.off_xdk, dv, dg, dh0, ws + L.off_tc, st);
+    if (c == cudaSuccess) c = ssdx::reduce_heads(BT, p->H, p->Hqk, ws + L.off_xdq, dq, st);
+    if (c == cudaSuccess) c = ssdx::reduce_heads(BT, p->H, p->Hqk, ws + L.off_xdk, dk, st);
+    return cuda_status(c);
+  }
   if (L.tc)
     return cuda_status(tc::bwd(pr, docs, p, dO, dht, dq, dk, dv, dg, dh0, ws + L.off_tc, st));
   float *states = (float *)(ws + L.off_states);
@@ -479,12 +530,64 @@ glacore_status glacore_get_device_error(glacore_stream_t stream) {
   return (glacore_status)h;
 }
 
+glacore_status gla_fwd_state(const glacore_problem *p, float *L, float *D, glacore_stream_t stream) {
+  glacore_status s = check_problem(p, false);
+  if (s) return s;
+  if (p->B * p->T > 0 && (!L || !D)) return GLACORE_ERR_INVALID_ARG;
+  if (p->segment_ids || !tc::supported(p, false, false)) return GLACORE_ERR_UNSUPPORTED;
+  if (!(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) && aligned16(L) && aligned16(D)))
+    return GLACORE_ERR_INVALID_ARG;
+  if (p->B * p->T == 0) return GLACORE_OK;
+  t_used = 0;
+  Layout Lo;
+  memset(&Lo, 0, sizeof(Lo));
+  Lo.chunk = tc::C;
+  const Docs docs = make_docs(p, Lo, nullptr);
+  return cuda_status(tc::doc_states(make_prob(p, false), docs, nullptr, L, D, (cudaStream_t)stream));
+}
+
+glacore_status gla_bwd_state(const glacore_problem *p, const void *do_, float *L, float *D,
+                             glacore_stream_t stream) {
+  glacore_status s = check_problem(p, false);
+  if (s) return s;
+  if (p->B * p->T > 0 && (!L || !D || !do_)) return GLACORE_ERR_INVALID_ARG;
+  if (p->segment_ids || !tc::supported(p, false, true)) return GLACORE_ERR_UNSUPPORTED;
+  if (!(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) && aligned16(L) &&
+        aligned16(D) && aligned16(do_)))
+    return GLACORE_ERR_INVALID_ARG;
+  if (p->B * p->T == 0) return GLACORE_OK;
+  t_used = 0;
+  Layout Lo;
+  memset(&Lo, 0, sizeof(Lo));
+  Lo.chunk = tc::C;
+  const Docs docs = make_docs(p, Lo, nullptr);
+  return cuda_status(tc::doc_states(make_prob(p, false), docs, do_, L, D, (cudaStream_t)stream));
+}
+
+glacore_status glacore_state_scan(const float *L, const float *D, int64_t R, int64_t mats, int64_t K, int64_t V,
+                                  const float *seed, int64_t r, int32_t reverse, float *out,
+                                  glacore_stream_t stream) {
+  if (R < 1 || mats < 0 || K < 1 || V < 1 || r < 0 || r >= R || (reverse != 0 && reverse != 1))
+    return GLACORE_ERR_INVALID_ARG;
+  if (mats == 0) return GLACORE_OK;
+  if (!L || !D || !out) return GLACORE_ERR_INVALID_ARG;
+  const int64_t n = mats * K * V;
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  state_scan_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(L, D, R, mats, K, V, seed, r, reverse, out);
+  mark_launch("state_scan", (cudaStream_t)stream);
+  return cuda_status(cudaGetLastError());
+}
+
 glacore_status glacore_selftest_wait(int64_t cycles, glacore_stream_t stream) {
   if (cycles < 1 || cycles > ((int64_t)1 << 40)) return GLACORE_ERR_INVALID_ARG;
   int *err = device_error_ptr();
   if (!err) return GLACORE_ERR_CUDA;
   wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)cycles, err);
   return cuda_status(cudaGetLastError());
+}
+
+const char *glacore_last_cuda_error(void) {
+  return t_last_cuda == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_cuda);
 }
 
 const char *glacore_status_string(glacore_status s) {
@@ -503,7 +606,7 @@ const char *glacore_status_string(glacore_status s) {
   return "unknown status";
 }
 
-int glacore_version(void) { return 100; }
+int glacore_version(void) { return 200; }
 
 void glacore_set_timing_events(void *events, int n_events) {
   t_events = (cudaEvent_t *)events;

@@ -113,6 +113,7 @@ __device__ __forceinline__ int64_t block_excl_scan(int64_t x, int64_t *warp_buf,
 // Problem as the kernels see it (token axis flattened: BT = B * T).
 struct Prob {
   int64_t BT, H, Hqk, K, V;
+  int64_t qs, ks, vs;  // elements between consecutive tokens of q, k, v
   int gate_head;  // 0: g[BT,H,K]; 1: g[BT,H]
   float scale;
   const void *q, *k, *v;
@@ -165,6 +166,9 @@ cudaError_t sum_channels(int64_t rows, const float *x, float *dg, cudaStream_t s
 
 // Records the next caller-provided timing event (if any) after a launch.
 void mark_launch(const char *label, cudaStream_t st);
+// Maps a CUDA result to a status, remembering the CUDA error of this host
+// thread's last failing call (glacore_last_cuda_error).
+glacore_status status_of(cudaError_t e);
 
 // ---- segment prep ------------------------------------------------------
 cudaError_t launch_prep(const int32_t *seg, int64_t B, int64_t T, int64_t n_seqs, int chunk,

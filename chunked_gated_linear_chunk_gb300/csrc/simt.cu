@@ -89,9 +89,9 @@ __global__ void __launch_bounds__(256) fwd_kernel(Prob p, Docs docs, T *o, float
         if (t < L) {
           const int64_t tok = a0 + t;
           G += gate_at(p, tok, h, c);
-          const int64_t qi = (tok * p.Hqk + hk) * K + c;
-          qt[t * K + c] = p.scale * ld<T>(p.q, qi) * expf(G);
-          kt[t * K + c] = ld<T>(p.k, qi) * expf(-G);
+          const int64_t qo = hk * K + c;
+          qt[t * K + c] = p.scale * ld<T>(p.q, tok * p.qs + qo) * expf(G);
+          kt[t * K + c] = ld<T>(p.k, tok * p.ks + qo) * expf(-G);
         } else {
           qt[t * K + c] = 0.f;
           kt[t * K + c] = 0.f;
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(256) fwd_kernel(Prob p, Docs docs, T *o, float
     }
     for (int i = tid; i < SC * SV; i += nt) {
       const int t = i / SV, j = i % SV;
-      vt[i] = (t < L && j < nv) ? ld<T>(p.v, ((a0 + t) * p.H + h) * V + v0 + j) : 0.f;
+      vt[i] = (t < L && j < nv) ? ld<T>(p.v, (a0 + t) * p.vs + h * V + v0 + j) : 0.f;
     }
     __syncthreads();
     for (int i = tid; i < SC * SC; i += nt) {
@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(256)
         if (t < L) {
           const int64_t tok = a0 + t;
           G += gate_at(p, tok, h, c);
-          const int64_t qi = (tok * p.Hqk + hk) * K + c;
-          const float qv = ld<T>(p.q, qi), kv = ld<T>(p.k, qi);
+          const int64_t qo = hk * K + c;
+          const float qv = ld<T>(p.q, tok * p.qs + qo), kv = ld<T>(p.k, tok * p.ks + qo);
           const float e = expf(G), ei = expf(-G);
           q_[idx] = qv;
           k_[idx] = kv;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256)
       const int t = (int)(i / V);
       const int64_t e = i % V;
       const int64_t off = ((a0 + t) * H + h) * V + e;
-      vv[i] = t < L ? ld<T>(p.v, off) : 0.f;
+      vv[i] = t < L ? ld<T>(p.v, (a0 + t) * p.vs + h * V + e) : 0.f;
       dd[i] = t < L ? to_f32(dO[off]) : 0.f;
     }
     if (tid < SC) dgt[tid] = 0.f;

@@ -127,7 +127,12 @@ struct FwdArgs;
 // document) and, when rm / ra are given, the reverse pass (local state
 // gradient at the start of every piece but the first) in one launch.
 cudaError_t launch_piece_states(const FwdMaps &fm, const FwdArgs &fa, const FwdMaps *rm, const FwdArgs *ra,
-                                int64_t units, int64_t H, cudaStream_t st);
+                                int64_t units, int64_t H, cudaStream_t st, bool rev_only = false);
+// Local end state (from zero) and total decay of every document (forward),
+// or, when dO is given, the local state gradient at every document's start
+// (from zero at its end) and its total decay (reverse): the piece passes run
+// with one unit per document.  L [n_docs,H,K,V], D [n_docs,H,K] fp32.
+cudaError_t doc_states(const Prob &pr, const Docs &docs, const void *dO, float *L, float *D, cudaStream_t st);
 cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void *o, float *ht,
                 char *ws, cudaStream_t st);
 cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, const void *dO,

@@ -24,6 +24,17 @@ typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, voi
                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Makes the current device's primary context current in this host thread.
+// The tensor maps are encoded through the driver API, which needs a current
+// context; the runtime binds one only when a runtime call needs it, so a
+// host thread that has made no CUDA call yet would have none.
+inline cudaError_t bind_context() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  return e;
+}
+
 inline EncodeFn encoder() {
   static EncodeFn fn = nullptr;
   if (!fn) {
@@ -39,14 +50,15 @@ inline EncodeFn encoder() {
 
 // 3-D map over a [BT, heads, D] tensor: dims (D, heads, BT), box
 // (box_x, 1, C tokens), 128-byte swizzle (box_x = 64 bf16 or 32 fp32
-// elements: one 128-byte row per token).
+// elements: one 128-byte row per token).  row_stride: elements between
+// consecutive tokens (0: heads * D, contiguous).
 inline bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t D, int64_t heads,
-                     int64_t BT, int box_x) {
+                     int64_t BT, int box_x, int64_t row_stride = 0) {
   EncodeFn enc = encoder();
   if (!enc) return false;
   const int es = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)BT};
-  cuuint64_t strides[2] = {(cuuint64_t)(D * es), (cuuint64_t)(heads * D * es)};
+  cuuint64_t strides[2] = {(cuuint64_t)(D * es), (cuuint64_t)((row_stride ? row_stride : heads * D) * es)};
   cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
@@ -330,31 +342,35 @@ __device__ __forceinline__ void mask_rows_to_smem(uint32_t t_acc, int r0, int la
     }
   }
 }
-// The rounding residue of a masked tile: lo = bf16(x - bf16(x)) for the
-// blocks at or below the diagonal (the masked entries are 0).  With the
-// tile written by mask_tile_to_smem (hi = bf16(x)), hi + lo carries about
-// 16 bits of the fp32 value, so a product with both (two accumulating MMAs)
-// removes the bf16 rounding of the tile itself.  Same TMEM layout, warp
-// roles and zero-initialised blocks as mask_tile_to_smem.
-__device__ __forceinline__ void mask_block_store_lo(uint8_t *tile, int row, int cb, const uint32_t (&r)[16],
-                                                    bool diag, int lane) {
+// The masked tile as two bf16 tiles, hi = bf16(x) and lo = bf16(x - hi):
+// hi + lo carries about 16 bits of the fp32 value, so a product with both
+// (two accumulating MMAs) removes the bf16 rounding of the tile itself.
+__device__ __forceinline__ void mask_block_store_hilo(uint8_t *hi_tile, uint8_t *lo_tile, int row, int cb,
+                                                      const uint32_t (&r)[16], bool diag, int rl) {
 #pragma unroll
   for (int hb = 0; hb < 2; ++hb) {
-    uint32_t w[4];
+    uint32_t w[4], wl[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i0 = hb * 8 + 2 * e;
-      const float x0 = (!diag || i0 <= lane) ? __uint_as_float(r[i0]) : 0.f;
-      const float x1 = (!diag || i0 + 1 <= lane) ? __uint_as_float(r[i0 + 1]) : 0.f;
-      const uint32_t hi = pack_bf16(x0, x1);
-      w[e] = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+      const float x0 = (!diag || i0 <= rl) ? __uint_as_float(r[i0]) : 0.f;
+      const float x1 = (!diag || i0 + 1 <= rl) ? __uint_as_float(r[i0 + 1]) : 0.f;
+      w[e] = pack_bf16(x0, x1);
+      wl[e] = pack_bf16(x0 - __uint_as_float(w[e] << 16), x1 - __uint_as_float(w[e] & 0xffff0000u));
     }
-    st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + hb * 8, 64)), w[0], w[1], w[2], w[3]);
+    const uint32_t off = sw128_off(row, cb * 16 + hb * 8, 64);
+    st_shared_v4(smem_u32(hi_tile + off), w[0], w[1], w[2], w[3]);
+    st_shared_v4(smem_u32(lo_tile + off), wl[0], wl[1], wl[2], wl[3]);
   }
 }
-__device__ __forceinline__ void mask_tile_lo_to_smem(uint32_t t_acc, uint32_t lane_off, int qw, int lane,
-                                                     uint8_t *tile) {
-  const int row = qw * 16 + lane;
+// mask_tile_to_smem into a hi / lo pair of tiles (both set up by
+// mask_tile_init).  The M = 64 accumulator holds a warp's 16 rows in lanes
+// 0..15; lanes 16..31 take the second 16-column block of each pair, shuffled
+// over from lanes 0..15, so every lane writes one block (hi and lo).
+__device__ __forceinline__ void mask_tile_to_smem_hilo(uint32_t t_acc, uint32_t lane_off, int qw, int lane,
+                                                       uint8_t *hi_tile, uint8_t *lo_tile) {
+  const int rl = lane & 15, row = qw * 16 + rl;
+  const bool second = lane >= 16;
 #pragma unroll
   for (int cp = 0; cp < 4; cp += 2) {
     if (cp <= qw) {
@@ -363,10 +379,14 @@ __device__ __forceinline__ void mask_tile_lo_to_smem(uint32_t t_acc, uint32_t la
       tmem_ld16(t_acc + lane_off + cp * 16 + 16, r1);
       tmem_ld_wait(r0);
       tmem_tie(r1);
-      if (lane < 16) {
-        mask_block_store_lo(tile, row, cp, r0, cp == qw, lane);
-        if (cp + 1 <= qw) mask_block_store_lo(tile, row, cp + 1, r1, cp + 1 == qw, lane);
+      uint32_t v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t s = __shfl_sync(0xffffffffu, r1[i], rl);
+        v[i] = second ? s : r0[i];
       }
+      const int cb = cp + (second ? 1 : 0);
+      if (cb <= qw) mask_block_store_hilo(hi_tile, lo_tile, row, cb, v, cb == qw, rl);
     }
   }
 }

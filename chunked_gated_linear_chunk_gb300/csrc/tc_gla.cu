@@ -19,9 +19,15 @@ __global__ void __launch_bounds__(448, 1)
 // host side
 // =========================================================================
 
+// True when the tcgen05 kernels cover this GLA problem (bf16, K = V = 128,
+// any head sharing H % Hqk == 0; a token stride of q / k / v that TMA can
+// address: a multiple of 16 bytes).
+static bool strides_ok(const glacore_problem *p) {
+  return (p->q_stride % 8) == 0 && (p->k_stride % 8) == 0 && (p->v_stride % 8) == 0;
+}
 bool supported(const glacore_problem *p, bool head_gate, bool) {
   if (head_gate) return false;
-  return p->dtype == GLACORE_BF16 && p->K == KD && p->V == VD && p->Hqk == p->H &&
+  return p->dtype == GLACORE_BF16 && p->K == KD && p->V == VD && p->H % p->Hqk == 0 && strides_ok(p) &&
          (p->chunk_size == 0 || p->chunk_size == 64) && p->B * p->T < ((int64_t)1 << 31) &&
          // one-dimensional grids of 2 x units x heads CTAs (units <= documents + pieces)
          4 * p->B * p->T * p->H < ((int64_t)1 << 31);
@@ -34,13 +40,14 @@ size_t workspace_bytes(const glacore_problem *p, bool, bool backward) {
 cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void *o, float *ht,
                 char *ws, cudaStream_t st) {
   if (docs.n == 0) return cudaSuccess;
+  if (const cudaError_t be = bind_context()) return be;
   const TcLayout Lo = tc_layout(p, false);
   FwdMaps maps;
   const int64_t BT = pr.BT;
   memset(&maps, 0, sizeof(maps));
-  if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
-      !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
-      !make_map(&maps.v, pr.v, true, pr.V, pr.H, BT, 64) ||
+  if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64, pr.qs) ||
+      !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64, pr.ks) ||
+      !make_map(&maps.v, pr.v, true, pr.V, pr.H, BT, 64, pr.vs) ||
       (!pr.gate_head && !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32)))
     return cudaErrorInvalidValue;
   FwdArgs a;
@@ -78,6 +85,42 @@ cudaError_t fwd(const Prob &pr, const Docs &docs, const glacore_problem *p, void
   if ((e = launch_pairs(kernel, grid, smem, st, maps, a)) != cudaSuccess) return e;
   mark_launch("gla_fwd_kernel", st);
   return cudaSuccess;
+}
+
+cudaError_t doc_states(const Prob &pr, const Docs &docs, const void *dO, float *L, float *D, cudaStream_t st) {
+  if (docs.n == 0) return cudaSuccess;
+  if (const cudaError_t be = bind_context()) return be;
+  const int64_t BT = pr.BT;
+  FwdMaps fm, rm;
+  memset(&fm, 0, sizeof(fm));
+  if (!make_map(&fm.q, pr.q, true, KD, pr.Hqk, BT, 64, pr.qs) ||
+      !make_map(&fm.k, pr.k, true, KD, pr.Hqk, BT, 64, pr.ks) ||
+      !make_map(&fm.v, pr.v, true, pr.V, pr.H, BT, 64, pr.vs) ||
+      (!pr.gate_head && !make_map(&fm.g, pr.g, false, KD, pr.H, BT, 32)))
+    return cudaErrorInvalidValue;
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.units.docs = docs;  // one unit per document, index order
+  a.H = pr.H;
+  a.hq_div = (int32_t)(pr.H / pr.Hqk);
+  a.gate_head = pr.gate_head;
+  a.vd = (int32_t)pr.V;
+  a.scale = pr.scale;
+  a.g = pr.g;
+  a.err = pr.err;
+  a.lbuf = L;
+  a.dbuf = D;
+  a.all_units = 1;
+  cudaError_t e;
+  if (!dO) {
+    e = launch_piece_states(fm, a, nullptr, nullptr, docs.n, pr.H, st);
+  } else {
+    rm = fm;
+    rm.k = fm.q;  // the reverse pass runs q through the k slot and do through the v slot
+    if (!make_map(&rm.v, dO, true, pr.V, pr.H, BT, 64)) return cudaErrorInvalidValue;
+    e = launch_piece_states(rm, a, &rm, &a, docs.n, pr.H, st, true);
+  }
+  return e;
 }
 
 }  // namespace tc

@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(448, 1)
   const int64_t d = un.doc;
   const int64_t s0 = un.start, s1 = un.end;
   const int nch = (int)((s1 - s0 + C - 1) / C);
-  const int hq = (HG && a.hq_div > 1) ? h / a.hq_div : h;  // head of q and k
+  const int hq = a.hq_div > 1 ? h / a.hq_div : h;  // head of q and k
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, 512);
@@ -1212,14 +1212,15 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
                 const float *dht, void *dq, void *dk, void *dv, float *dg, float *dh0, char *ws,
                 cudaStream_t st) {
   if (docs.n == 0) return cudaSuccess;
+  if (const cudaError_t be = bind_context()) return be;
   const TcLayout Lo = tc_layout(p, true);
   BwdMaps maps;
   memset(&maps, 0, sizeof(maps));
   const int64_t BT = pr.BT;
   float *dgp = (float *)(ws + Lo.off_dgp);
-  if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64) ||
-      !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
-      !make_map(&maps.v, pr.v, true, pr.V, pr.H, BT, 64) ||
+  if (!make_map(&maps.q, pr.q, true, KD, pr.Hqk, BT, 64, pr.qs) ||
+      !make_map(&maps.k, pr.k, true, KD, pr.Hqk, BT, 64, pr.ks) ||
+      !make_map(&maps.v, pr.v, true, pr.V, pr.H, BT, 64, pr.vs) ||
       !make_map(&maps.dO, dO, true, pr.V, pr.H, BT, 64) ||
       !make_map(&maps.dq, dq, true, KD, pr.H, BT, 64) ||
       (!pr.gate_head && !make_map(&maps.g, pr.g, false, KD, pr.H, BT, 32)) ||
@@ -1273,8 +1274,9 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     // their starts (reverse), in one launch; the consumers fold them
     FwdMaps fm, rm;
     memset(&fm, 0, sizeof(fm));
-    if (!make_map(&fm.q, pr.q, true, KD, pr.Hqk, BT, 64) || !make_map(&fm.k, pr.k, true, KD, pr.Hqk, BT, 64) ||
-        !make_map(&fm.v, pr.v, true, pr.V, pr.H, BT, 64) ||
+    if (!make_map(&fm.q, pr.q, true, KD, pr.Hqk, BT, 64, pr.qs) ||
+        !make_map(&fm.k, pr.k, true, KD, pr.Hqk, BT, 64, pr.ks) ||
+        !make_map(&fm.v, pr.v, true, pr.V, pr.H, BT, 64, pr.vs) ||
         (!pr.gate_head && !make_map(&fm.g, pr.g, false, KD, pr.H, BT, 32)))
       return cudaErrorInvalidValue;
     rm = fm;

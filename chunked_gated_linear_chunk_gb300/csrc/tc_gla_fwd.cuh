@@ -14,9 +14,7 @@
 //
 // The masked P enters P V as two bf16 tiles, hi = bf16(P) and
 // lo = bf16(P - hi), so that its own rounding does not add to the error of
-// o (which is rounded to bf16 once more when it is stored).  The lo half is
-// built after the state step and its product issued after the next chunk's
-// readout, so it stays off the chunk-to-chunk chain.
+// o (which is rounded to bf16 once more when it is stored).
 //
 // The fp32 state S never leaves the SM between chunks (FLAT's "keep the
 // state on-chip"; FLA instead writes every chunk state to HBM).  All
@@ -73,6 +71,7 @@ struct FwdArgs {
   float *ht;          // [n_docs,H,K,V] final state (written by the last piece)
   float *lbuf;        // [units,H,K,V] piece end state from zero (written by the piece pass)
   float *dbuf;        // [units,H,K] exp(sum of g over the piece) (written by the piece pass)
+  int32_t all_units;  // piece pass: every unit contributes (state entries), not only pieces that hand on
   __nv_bfloat16 *o;   // [BT, H, vd]
   int *err;
 };
@@ -230,7 +229,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[fsm::NS], empty[fsm::NS], prep_done[fsm::NS], p_full[2], u_full[2],
-      o_full[2], p_ready[2], p_lo_ready[2], s_ready[2], gam_ready[4];
+      o_full[2], p_ready[2], s_ready[2], gam_ready[4];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag, range_flag;
 
@@ -239,7 +238,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   // share the q / k prep (rank = value half)
   // bx = 2 (r H + h) + vb: launch rank r (units in launch order), head h
   const int vb = bx & 1, h = (int)((int64_t)(bx >> 1) % a.H);
-  const int hq = (HG && a.hq_div > 1) ? h / a.hq_div : h;  // head of q and k
+  const int hq = a.hq_div > 1 ? h / a.hq_div : h;  // head of q and k
   const uint32_t peer = (uint32_t)(vb ^ 1);
   const int64_t u = a.units.at((int64_t)(bx >> 1) / a.H);
   const Unit un = a.units.get(u);
@@ -266,7 +265,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       mbar_init(&u_full[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&p_ready[i], 128);
-      mbar_init(&p_lo_ready[i], 128);
       mbar_init(&s_ready[i], 128);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 129);
@@ -326,24 +324,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       constexpr uint32_t idP = idesc_bf16(64, 64, false, false);
       constexpr uint32_t idO = idesc_bf16(64, 64, false, true);
       constexpr uint32_t idU = idesc_bf16(128, 64, true, true);
-      uint32_t ph_prep = 0, ph_pr = 0, ph_sr = 0, ph_lo = 0;  // one parity bit per buffer
-      // the second half of chunk j's P V (the P_lo tile) is issued after
-      // chunk j+1's readout, so that the lo tile is built while the tensor
-      // core runs other work; its commit releases the output tile and the
-      // q / k / v stage of chunk j
-      auto finish = [&](int jj) -> bool {
-        const int bb = jj & 1, sst = jj % fsm::NS;
-        if (!mbar_wait(&p_lo_ready[bb], (ph_lo >> bb) & 1, WAIT_CYCLES)) return false;
-        ph_lo ^= 1u << bb;
-        tc_fence_after();
-        const uint32_t Plo = sbase + fsm::P + bb * 16384 + 8192, vaa = sbase + fsm::V + sst * 8192;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tbase + 256 + 64 * bb, kdesc(Plo, ks, 64), mdesc(vaa, ks, 8192), idO, 1);
-        mma_commit(&o_full[bb]);
-        mma_commit_multicast(&empty[sst], 3);
-        return true;
-      };
+      uint32_t ph_prep = 0, ph_pr = 0, ph_sr = 0;  // one parity bit per buffer
       for (int j = 0; j < nch; ++j) {
         const int b = j & 1, st = j % fsm::NS;
         const uint32_t qa = sbase + fsm::Q + st * 16384, ka = sbase + fsm::K + st * 16384;
@@ -370,13 +351,14 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(qa, ks, 64), mdesc(Sa, ks, 16384), idO, ks);
-        // P V as (P_hi + P_lo) V: the hi half now, the lo half after the
-        // next chunk's readout
+        // P V as (P_hi + P_lo) V: the masked P carried at about 16 bits
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tO, kdesc(Pa, ks, 64), mdesc(va, ks, 8192), idO, 1);
-        if (j >= 1 && !finish(j - 1)) FAIL_AND_BREAK
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) mma_bf16(tO, kdesc(Pa + 8192, ks, 64), mdesc(va, ks, 8192), idO, 1);
+        mma_commit(&o_full[b]);
+        mma_commit_multicast(&empty[st], 3);
       }
-      if (nch > 0 && !*abortp && !finish(nch - 1)) atomicExch(&abort_flag, 1);
       // every commit that targets this CTA's stage barriers has landed
       // before the CTAs leave (the peer's arrive on our barriers and ours on
       // its): wait for the last phase of each stage
@@ -466,55 +448,18 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
     fence_async_smem();
     mbar_arrive(&s_ready[1]);
     uint32_t ph_p = 0, ph_u = 0, ph_o = 0;
-    // S3b: output tile O = qt S_prev + P V of chunk jj, stored one chunk
-    // late (its P_lo half is issued after the next chunk's readout)
-    auto store_o = [&](int jj) -> bool {
-      const int bb = jj & 1;
-      const int64_t tok0 = chunk_tok(jj);
-      const int L = (int)min((int64_t)C, s1 - tok0);
-      const uint32_t tO = tbase + 256 + 64 * bb;
-      if (!mbar_wait(&o_full[bb], (ph_o >> bb) & 1, WAIT_CYCLES)) return false;
-      ph_o ^= 1u << bb;
-      tc_fence_after();
-#pragma unroll
-      for (int cp = 0; cp < 4; cp += 2) {
-        uint32_t r[2][16];
-        tmem_ld16(tO + lane_off + cp * 16, r[0]);
-        tmem_ld16(tO + lane_off + cp * 16 + 16, r[1]);
-        tmem_ld_wait(r[0]);
-        tmem_tie(r[1]);
-        // o has 128 columns, or in the per-head-gate instance a.vd (64 or
-        // 128): a value half at or past them stores nothing
-        const int Lo = (!HG || (int)(blockIdx.x & 1) * 64 < a.vd) ? L : 0;
-        if (lane < 16 && prow < Lo) {
-#pragma unroll
-          for (int hc = 0; hc < 2; ++hc) {
-            __nv_bfloat16 *dst = a.o + ((tok0 + prow) * H + h) * (HG ? (int64_t)a.vd : (int64_t)VD) + v0 + (cp + hc) * 16;
-            const uint32_t *x = r[hc];
-            st_global_v4(dst, pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                         pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                         pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                         pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
-            st_global_v4(dst + 8, pack_bf16(__uint_as_float(x[8]), __uint_as_float(x[9])),
-                         pack_bf16(__uint_as_float(x[10]), __uint_as_float(x[11])),
-                         pack_bf16(__uint_as_float(x[12]), __uint_as_float(x[13])),
-                         pack_bf16(__uint_as_float(x[14]), __uint_as_float(x[15])));
-          }
-        }
-      }
-      tc_fence_before();
-      return true;
-    };
     for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
-      const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b;
-      // S2: P -> causal mask -> bf16 A operand (hi) of the intra-chunk product
+      const int64_t tok0 = chunk_tok(j);
+      const int L = (int)min((int64_t)C, s1 - tok0);
+      const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
+      // S2: P -> causal mask -> bf16 hi / lo A operands of the intra-chunk product
       if (!mbar_wait(&p_full[b], (ph_p >> b) & 1, WAIT_CYCLES)) {
         FAIL_AND_BREAK
       }
       ph_p ^= 1u << b;
       tc_fence_after();
-      mask_tile_to_smem(tP, lane_off, qw, lane, sm + fsm::P + b * 16384);
+      mask_tile_to_smem_hilo(tP, lane_off, qw, lane, sm + fsm::P + b * 16384, sm + fsm::P + b * 16384 + 8192);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[b]);
@@ -543,14 +488,40 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&s_ready[b]);
-      // the rounding residue of P (lo tile), off the readout's path
-      mask_tile_lo_to_smem(tP, lane_off, qw, lane, sm + fsm::P + b * 16384 + 8192);
-      fence_async_smem();
+      // S3b: output tile O = qt S_prev + P V
+      if (!mbar_wait(&o_full[b], (ph_o >> b) & 1, WAIT_CYCLES)) {
+        FAIL_AND_BREAK
+      }
+      ph_o ^= 1u << b;
+      tc_fence_after();
+#pragma unroll
+      for (int cp = 0; cp < 4; cp += 2) {
+        uint32_t r[2][16];
+        tmem_ld16(tO + lane_off + cp * 16, r[0]);
+        tmem_ld16(tO + lane_off + cp * 16 + 16, r[1]);
+        tmem_ld_wait(r[0]);
+        tmem_tie(r[1]);
+        // o has 128 columns, or in the per-head-gate instance a.vd (64 or
+        // 128): a value half at or past them stores nothing
+        const int Lo = (!HG || (int)(blockIdx.x & 1) * 64 < a.vd) ? L : 0;
+        if (lane < 16 && prow < Lo) {
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {
+            __nv_bfloat16 *dst = a.o + ((tok0 + prow) * H + h) * (HG ? (int64_t)a.vd : (int64_t)VD) + v0 + (cp + hc) * 16;
+            const uint32_t *x = r[hc];
+            st_global_v4(dst, pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                         pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                         pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                         pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+            st_global_v4(dst + 8, pack_bf16(__uint_as_float(x[8]), __uint_as_float(x[9])),
+                         pack_bf16(__uint_as_float(x[10]), __uint_as_float(x[11])),
+                         pack_bf16(__uint_as_float(x[12]), __uint_as_float(x[13])),
+                         pack_bf16(__uint_as_float(x[14]), __uint_as_float(x[15])));
+          }
+        }
+      }
       tc_fence_before();
-      mbar_arrive(&p_lo_ready[b]);
-      if (j >= 1 && !store_o(j - 1)) FAIL_AND_BREAK
     }
-    if (nch > 0 && !*abortp && !store_o(nch - 1)) atomicExch(&abort_flag, 1);
     float *dst = a.ht && last_piece ? a.ht + ((d * H + h) * KD + c) * VD + v0 : nullptr;
     if (dst && !*abortp) {
 #pragma unroll

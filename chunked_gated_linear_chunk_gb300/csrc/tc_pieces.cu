@@ -119,7 +119,7 @@ __device__ __forceinline__ void piece_state_body(const FwdMaps &maps, const FwdA
   const int64_t s0 = un.start, s1 = un.end;
   // the forward pass has nothing to hand on from a document's last piece,
   // the reverse pass nothing from its first
-  if (REV ? un.piece == 0 : un.piece == un.npieces - 1) return;
+  if (!a.all_units && (REV ? un.piece == 0 : un.piece == un.npieces - 1)) return;
   const int nch = (int)((s1 - s0 + C - 1) / C);
   if (nch <= 0) return;
   // forward pass: chunks last to first (decay to the piece end); reverse: first to last
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(320, 2)
 }
 
 cudaError_t launch_piece_states(const FwdMaps &fm, const FwdArgs &fa, const FwdMaps *rm, const FwdArgs *ra,
-                                int64_t units, int64_t H, cudaStream_t st) {
+                                int64_t units, int64_t H, cudaStream_t st, bool rev_only) {
   const int smem = psm::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(piece_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -303,8 +303,9 @@ cudaError_t launch_piece_states(const FwdMaps &fm, const FwdArgs &fa, const FwdM
   }
   if (work <= 0) return cudaSuccess;
   const unsigned nfwd = (unsigned)(2 * work);
-  const dim3 grid(rm ? 2 * nfwd : nfwd, (unsigned)H);
-  piece_state_kernel<<<grid, 320, smem, st>>>(fm, fa, rm ? *rm : fm, ra ? *ra : fa, nfwd, npr);
+  if (rev_only && !rm) return cudaErrorInvalidValue;
+  const dim3 grid(rev_only ? nfwd : (rm ? 2 * nfwd : nfwd), (unsigned)H);
+  piece_state_kernel<<<grid, 320, smem, st>>>(fm, fa, rm ? *rm : fm, ra ? *ra : fa, rev_only ? 0u : nfwd, npr);
   mark_launch("piece_state_kernel", st);
   return cudaGetLastError();
 }

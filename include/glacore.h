@@ -27,7 +27,8 @@
  *    library allocates no memory, never synchronises the stream (except
  *    glacore_get_device_error, which says so) and
  *    enqueues all work on `stream` (NULL = legacy default stream).
- *  - Layouts are contiguous row-major.  Offsets are computed in 64-bit.
+ *  - Layouts are row-major; q, k and v may have a token stride (below), all
+ *    other tensors are contiguous.  Offsets are computed in 64-bit.
  *      q, k        [B, T, Hqk, K]   (dtype)
  *      v, o, do    [B, T, H, V]     (dtype)
  *      g, dg       GLA: [B, T, H, K] fp32;  SSD: [B, T, H] fp32  (g <= 0)
@@ -85,13 +86,13 @@ typedef enum { GLACORE_F32 = 0, GLACORE_BF16 = 1 } glacore_dtype;
 
 /* One problem description, shared by the forward and backward entries.
  *   B, T        batch rows and tokens per row (T >= 0; B >= 1)
- *   H           value heads; Hqk heads of q/k (GLA: Hqk == H; SSD: H % Hqk == 0)
+ *   H           value heads; Hqk heads of q/k (H % Hqk == 0; see head sharing below)
  *   K, V        key and value head dims (1..256)
  *   dtype       element type of q, k, v, o, do, dq, dk, dv
  *   chunk_size  chunk length of the chunk-parallel form: 0, 16, 32 or 64
  *               (any other value: GLACORE_ERR_UNSUPPORTED).  The tensor-core
- *               kernels (bf16; GLA with K = V = 128 and one q/k head per
- *               value head; SSD with K = 128 and V of 64 or 128) run chunks
+ *               kernels (bf16; GLA with K = V = 128; SSD with K = 128 and V
+ *               of 64 or 128) run chunks
  *               of 64 and take chunk_size 0 or 64.  Every other problem, and
  *               any problem given chunk_size 16 or 32, runs the CUDA-core
  *               kernels with chunks of chunk_size tokens (0: 16); those take
@@ -103,7 +104,23 @@ typedef enum { GLACORE_F32 = 0, GLACORE_BF16 = 1 } glacore_dtype;
  *   n_seqs      number of documents: B when segment_ids is NULL
  *   initial_state  [n_seqs,H,K,V] fp32 or NULL (zero)
  *   workspace   device scratch of at least *_workspace_size(problem) bytes
- *               (may be NULL when that size is 0); 256-byte aligned */
+ *               (may be NULL when that size is 0); 256-byte aligned
+ *   q_stride, k_stride, v_stride
+ *               elements between consecutive tokens (rows of [B*T]) of q,
+ *               k and v; 0 means contiguous (Hqk*K, Hqk*K, H*V).  Within a
+ *               token the heads stay contiguous ([heads, D]).  This lets q,
+ *               k and v be read in place from one fused projection
+ *               [B, T, 2*Hqk*K + H*V] (FLAT blog, "Forward Kernels / Data
+ *               movement" and "Full Linear Attention Layer": no layout copies
+ *               between the projection and the kernels).  A stride must be
+ *               at least the contiguous one; on the tensor-core path it must
+ *               be a multiple of 8 elements (16 bytes), as must the three
+ *               base addresses.
+ * Head sharing (FLAT blog, "Gated Linear Attention": queries, keys, values
+ * and the gate may use different head counts): Hqk q/k heads serve H value
+ * heads (H % Hqk == 0, value head h reads q/k head h / (H / Hqk)); the gate
+ * and the state are per value head; dq and dk are summed over the heads
+ * that share them. */
 typedef struct glacore_problem {
   int64_t B, T, H, Hqk, K, V;
   int32_t dtype;
@@ -117,6 +134,7 @@ typedef struct glacore_problem {
   const float *initial_state;
   void *workspace;
   size_t workspace_bytes;
+  int64_t q_stride, k_stride, v_stride;
 } glacore_problem;
 
 /* Scratch bytes needed by the matching call (0 if none).  Returns 0 and
@@ -178,6 +196,95 @@ glacore_status gla_bwd_noalloc(const glacore_problem *p, const void *do_,
                                const float *dht, void *dq, void *dk, void *dv,
                                float *dg, float *dh0, glacore_stream_t stream);
 
+/* ---- sequence split across devices (context parallelism) ---------------
+ * JLA product page ("our split is exact", unlike starting each piece from
+ * zero); FLAT blog, "Future work" (sharding the sequence across chips).  The
+ * recurrence is linear in the state, so a sequence cut into R consecutive
+ * pieces (one per device, each holding all heads of its tokens) runs
+ * exactly as a whole:
+ *   1. every piece: gla_fwd_state -> its local end state L (from a zero
+ *      initial state) and total decay D = exp(sum of g over the piece);
+ *   2. gather L and D of all pieces ([R, ...], piece order) on every device;
+ *      glacore_state_scan(reverse = 0, seed = the sequence's initial state)
+ *      gives the state entering piece r;
+ *   3. gla_fwd with that initial state gives the piece's o (and, on the last
+ *      piece, the sequence's final state).
+ * Backward: gla_bwd_state -> the piece's local state gradient at its start
+ * (from a zero gradient at its end) and total decay; gather;
+ * glacore_state_scan(reverse = 1, seed = dht of the sequence) gives the
+ * state gradient leaving piece r; gla_bwd with the entering state as
+ * initial_state and that gradient as dht gives the piece's dq, dk, dv, dg
+ * exactly (dh0 of the first piece is the sequence's).
+ * The two state entries run the tensor-core kernels (GLA, bf16, K = V = 128)
+ * without segment_ids (GLACORE_ERR_UNSUPPORTED otherwise); they take no
+ * workspace.
+ *   L   [n_seqs, H, K, V] fp32, D [n_seqs, H, K] fp32, written
+ *   do_ [B, T, H, V] (dtype) */
+glacore_status gla_fwd_state(const glacore_problem *p, float *L, float *D,
+                             glacore_stream_t stream);
+glacore_status gla_bwd_state(const glacore_problem *p, const void *do_,
+                             float *L, float *D, glacore_stream_t stream);
+/* out = the fold for piece r of R: with s = seed (or 0),
+ *   reverse = 0:  s <- diag(D[q]) s + L[q]  for q = 0 .. r-1
+ *   reverse = 1:  s <- diag(D[q]) s + L[q]  for q = R-1 down to r+1
+ * over every one of `mats` K x V fp32 matrices (L [R, mats, K, V],
+ * D [R, mats, K], seed and out [mats, K, V], device pointers). */
+glacore_status glacore_state_scan(const float *L, const float *D, int64_t R,
+                                  int64_t mats, int64_t K, int64_t V,
+                                  const float *seed, int64_t r, int32_t reverse,
+                                  float *out, glacore_stream_t stream);
+
+/* ---- operations around the recurrence ----------------------------------
+ * Per-head RMSNorm times a swish output gate, on the recurrence's output
+ * (FLAT blog, "Full Linear Attention Layer": the layer's per-head RMSNorm
+ * multiplied by a swish output gate; FLA documentation, "Norm Layers with
+ * Gating").  Over every row of V values (one token and head):
+ *     y = o * rsqrt(mean(o^2) + eps) * w * z * sigmoid(z)
+ *   o, z, y     [rows, V] (dtype; rows = B * T * H for o [B,T,H,V]),
+ *               16-byte aligned
+ *   w           [V] fp32 (one weight per channel, shared by the heads)
+ *   V           8, 16, 32, 64, 128 or 256;  eps >= 0
+ * Backward: do_, dz [rows, V] (dtype) and dw [V] fp32 written.  dw is
+ * reduced deterministically through the workspace (at least
+ * norm_gate_bwd_workspace_size bytes, 256-byte aligned). */
+glacore_status norm_gate_fwd(const void *o, const void *z, const float *w,
+                             int64_t rows, int64_t V, int32_t dtype, float eps,
+                             void *y, glacore_stream_t stream);
+size_t norm_gate_bwd_workspace_size(int64_t rows, int64_t V);
+glacore_status norm_gate_bwd(const void *o, const void *z, const float *w,
+                             const void *dy, int64_t rows, int64_t V,
+                             int32_t dtype, float eps, void *do_, void *dz,
+                             float *dw, void *workspace, size_t workspace_bytes,
+                             glacore_stream_t stream);
+
+/* Depthwise causal short convolution with bias and optional SiLU, the step
+ * before the recurrence (FLAT blog, "Depthwise Causal Short Convolution"):
+ * tap k of Kc reads the input Kc-1-k tokens back inside the token's
+ * document (inputs before a row start or a segment id change read as 0),
+ *     z_t = b + sum_k w[k] (.) x_{t-(Kc-1-k)},   y_t = SiLU(z_t) or z_t
+ *   x, y        [B, T, D] (dtype), 16-byte aligned; D a multiple of 8
+ *               (a fused q/k/v projection is one x of D = 3 H K)
+ *   w           [Kc, D] fp32;  b [D] fp32 or NULL (no bias);  Kc in 1..4
+ *   segment_ids [B, T] int32 or NULL (every row one document)
+ *   activation  1: SiLU, 0: none
+ * Backward: dx [B,T,D] (dtype), dw [Kc,D] and db [D] fp32 written (db is
+ * the bias gradient even when b is NULL).  dw and db are reduced
+ * deterministically through the workspace (at least
+ * short_conv_bwd_workspace_size bytes, 256-byte aligned). */
+glacore_status short_conv_fwd(const void *x, const float *w, const float *b,
+                              const int32_t *segment_ids, int64_t B, int64_t T,
+                              int64_t D, int32_t Kc, int32_t dtype,
+                              int32_t activation, void *y,
+                              glacore_stream_t stream);
+size_t short_conv_bwd_workspace_size(int64_t B, int64_t T, int64_t D,
+                                     int32_t Kc);
+glacore_status short_conv_bwd(const void *x, const float *w, const float *b,
+                              const int32_t *segment_ids, const void *dy,
+                              int64_t B, int64_t T, int64_t D, int32_t Kc,
+                              int32_t dtype, int32_t activation, void *dx,
+                              float *dw, float *db, void *workspace,
+                              size_t workspace_bytes, glacore_stream_t stream);
+
 /* Counts the documents in segment_ids [B,T] (device pointer) and writes
  * the count, as int64, to *n_docs (DEVICE pointer, 8-byte aligned).
  * Asynchronous on `stream`; the caller reads the count after the stream
@@ -200,6 +307,10 @@ glacore_status glacore_get_device_error(glacore_stream_t stream);
  * glacore_get_device_error.  The pages have no counterpart: it exists so
  * that the timeout path of every kernel can be shown to end. */
 glacore_status glacore_selftest_wait(int64_t cycles, glacore_stream_t stream);
+
+/* The CUDA runtime's description of the error behind this host thread's
+ * last GLACORE_ERR_CUDA ("no CUDA error" if there was none; static). */
+const char *glacore_last_cuda_error(void);
 
 /* Static English description of a status code. */
 const char *glacore_status_string(glacore_status s);

@@ -107,6 +107,33 @@ def test_chunk_16_workspace_holds_chunk_states():
     assert lib.gla_bwd_workspace_size(ctypes.byref(p)) >= states
 
 
+@pytest.mark.parametrize("over", [dict(q_stride=-8), dict(k_stride=4 * 128 - 8), dict(v_stride=100)])
+def test_bad_token_strides_rejected(over):
+    lib = glc.load()
+    p = make_problem(**over)
+    o = ctypes.c_void_p(4096)
+    assert lib.gla_bwd(ctypes.byref(p), o, None, o, o, o, o, None, None) == glc.ERR_INVALID_ARG
+    assert lib.gla_fwd_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_fused_projection_strides_accepted():
+    """q, k, v of one projection [B, T, 3 H K]: each token stride is 3 H K."""
+    lib = glc.load()
+    p = make_problem(q_stride=3 * 4 * 128, k_stride=3 * 4 * 128, v_stride=3 * 4 * 128)
+    o = ctypes.c_void_p(4096)
+    assert lib.gla_bwd(ctypes.byref(p), o, None, o, o, o, o, None, None) == glc.ERR_WORKSPACE
+
+
+def test_shared_qk_heads_keep_per_head_gradients_in_the_workspace():
+    """GLA with H / Hqk = 4 on the tensor-core kernels: the backward's
+    workspace holds dq and dk per value head (bf16) before the group sum."""
+    lib = glc.load()
+    p_shared = make_problem(Hqk=1)
+    p_own = make_problem(Hqk=4)
+    extra = 2 * p_shared.B * p_shared.T * p_shared.H * 128 * 2
+    assert lib.gla_bwd_workspace_size(ctypes.byref(p_shared)) >= lib.gla_bwd_workspace_size(ctypes.byref(p_own)) + extra
+
+
 def test_selftest_wait_rejects_bad_limits():
     lib = glc.load()
     assert lib.glacore_selftest_wait(0, None) == glc.ERR_INVALID_ARG
