@@ -77,15 +77,19 @@ struct FwdArgs {
 };
 
 namespace fsm {  // shared-memory carve-up of the forward kernel (bytes)
-constexpr int NS = 3;             // q/k/v pipeline stages
-constexpr uint32_t Q = 0;         // 3 x 16 KB: q, then qt in place
-constexpr uint32_t K = 49152;     // 3 x 16 KB: k, then kt in place
-constexpr uint32_t V = 98304;     // 3 x 8 KB (64 value columns)
-constexpr uint32_t P = 122880;    // 2 x 16 KB: masked P as bf16 hi (+0) and lo (+8 KB) tiles (K-major A)
-constexpr uint32_t S = 155648;    // 2 x 16 KB: S (bf16, rows = key channel)
-constexpr uint32_t GAM = 188416;  // 4 x 128 fp32: exp(chunk gate total)
-constexpr uint32_t XCH = 190464;  // 8 KB: token-group gate products (two buffers per prep group)
-constexpr uint32_t BYTES = 198656;
+constexpr int NS = 4;             // q/k/v pipeline stages
+constexpr uint32_t Q = 0;         // 4 x 16 KB: q, then qt in place
+constexpr uint32_t K = 65536;     // 4 x 16 KB: k, then kt in place
+constexpr uint32_t V = 131072;    // 4 x 8 KB (64 value columns)
+// masked P as bf16 hi (+0) and lo (+8 KB) tiles (K-major A).  One buffer:
+// the mask step of chunk j writes it only after P(j) has landed, whose
+// commit follows the P V products of chunk j - 1 that read it.
+constexpr uint32_t P = 163840;
+constexpr uint32_t S = 180224;    // 2 x 16 KB: S (bf16, rows = key channel)
+constexpr uint32_t GAM = 212992;  // 8 x 128 fp32: exp(chunk gate total), ring over chunks
+constexpr int NGAM = 8;
+constexpr uint32_t XCH = 217088;  // 8 KB: token-group gate products (two buffers per prep group)
+constexpr uint32_t BYTES = 225280;
 }  // namespace fsm
 
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
@@ -229,7 +233,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[fsm::NS], empty[fsm::NS], prep_done[fsm::NS], p_full[2], u_full[2],
-      o_full[2], p_ready[2], s_ready[2], gam_ready[4];
+      o_full[2], p_ready[2], s_ready[2], gam_ready[fsm::NGAM];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag, range_flag;
 
@@ -267,7 +271,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       mbar_init(&p_ready[i], 128);
       mbar_init(&s_ready[i], 128);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&gam_ready[i], 129);
+    for (int i = 0; i < fsm::NGAM; ++i) mbar_init(&gam_ready[i], 129);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -325,32 +329,56 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       constexpr uint32_t idO = idesc_bf16(64, 64, false, true);
       constexpr uint32_t idU = idesc_bf16(128, 64, true, true);
       uint32_t ph_prep = 0, ph_pr = 0, ph_sr = 0;  // one parity bit per buffer
-      for (int j = 0; j < nch; ++j) {
-        const int b = j & 1, st = j % fsm::NS;
-        const uint32_t qa = sbase + fsm::Q + st * 16384, ka = sbase + fsm::K + st * 16384;
-        const uint32_t va = sbase + fsm::V + st * 8192;
-        const uint32_t Pa = sbase + fsm::P + b * 16384, Sa = sbase + fsm::S + (b ^ 1) * 16384;
-        const uint32_t tP = tbase + 64 * b, tU = tbase + 128 + 64 * b, tO = tbase + 256 + 64 * b;
-        if (!mbar_wait_cluster(&prep_done[st], (ph_prep >> st) & 1, WAIT_CYCLES)) {
-          FAIL_AND_BREAK
-        }
-        ph_prep ^= 1u << st;
+      // Issue order: while chunk j's causal mask is being applied, the
+      // products of chunk j + 1 that need no state (P, and U once the
+      // state step of j - 1 has read U's tile) and q_j S_{j-1} are already
+      // running, so that after the mask step only the two P V products stand
+      // between it and the output tile, and the next mask step finds its P.
+      // (The epilogue writes the masked P of chunk j + 1 into the one P tile
+      // only after it has stored output j, so P V of chunk j has read it.)
+      auto issue_p = [&](int jj) -> bool {  // P of chunk jj, once it is prepared
+        const int sj = jj % fsm::NS;
+        if (!mbar_wait_cluster(&prep_done[sj], (ph_prep >> sj) & 1, WAIT_CYCLES)) return false;
+        ph_prep ^= 1u << sj;
         tc_fence_after();
+        const uint32_t qa = sbase + fsm::Q + sj * 16384, ka = sbase + fsm::K + sj * 16384;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) mma_bf16(tP, kdesc(qa, ks, 64), kdesc(ka, ks, 64), idP, ks);
-        mma_commit(&p_full[b]);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16(tbase + 64 * (jj & 1), kdesc(qa, ks, 64), kdesc(ka, ks, 64), idP, ks);
+        mma_commit(&p_full[jj & 1]);
+        return true;
+      };
+      auto issue_u = [&](int jj) {  // U = kt^T v of chunk jj
+        const int sj = jj % fsm::NS;
+        const uint32_t ka = sbase + fsm::K + sj * 16384, va = sbase + fsm::V + sj * 8192;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) mma_bf16(tU, mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, ks);
-        mma_commit(&u_full[b]);
-        if (!mbar_wait(&p_ready[b], (ph_pr >> b) & 1, WAIT_CYCLES) ||
-            !mbar_wait(&s_ready[b ^ 1], (ph_sr >> (b ^ 1)) & 1, WAIT_CYCLES)) {
-          FAIL_AND_BREAK
-        }
-        ph_pr ^= 1u << b;
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tbase + 128 + 64 * (jj & 1), mdesc(ka, ks, 8192), mdesc(va, ks, 8192), idU, ks);
+        mma_commit(&u_full[jj & 1]);
+      };
+      if (nch > 0) {
+        if (issue_p(0))
+          issue_u(0);
+        else
+          atomicExch(&abort_flag, 1);
+      }
+      for (int j = 0; j < nch && !*abortp; ++j) {
+        const int b = j & 1, st = j % fsm::NS;
+        const uint32_t qa = sbase + fsm::Q + st * 16384, va = sbase + fsm::V + st * 8192;
+        const uint32_t Pa = sbase + fsm::P, Sa = sbase + fsm::S + (b ^ 1) * 16384;
+        const uint32_t tO = tbase + 256 + 64 * b;
+        const bool next = j + 1 < nch;
+        if (next && !issue_p(j + 1)) FAIL_AND_BREAK
+        // S_{j-1} in shared memory; U's tile (j + 1) & 1 read by its state step
+        if (!mbar_wait(&s_ready[b ^ 1], (ph_sr >> (b ^ 1)) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
         ph_sr ^= 1u << (b ^ 1);
         tc_fence_after();
+        if (next) issue_u(j + 1);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tO, kdesc(qa, ks, 64), mdesc(Sa, ks, 16384), idO, ks);
+        if (!mbar_wait(&p_ready[b], (ph_pr >> b) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
+        ph_pr ^= 1u << b;
+        tc_fence_after();
         // P V as (P_hi + P_lo) V: the masked P carried at about 16 bits
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tO, kdesc(Pa, ks, 64), mdesc(va, ks, 8192), idO, 1);
@@ -404,10 +432,10 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       if (!mbar_wait(&full[s], (j / fsm::NS) & 1, WAIT_CYCLES)) FAIL_AND_BREAK
       // this CTA's 64-column block of q, k and its gate totals (byte offsets)
       const uint32_t qo = fsm::Q + s * 16384 + vb * 8192, ko = fsm::K + s * 16384 + vb * 8192,
-                     go = fsm::GAM + (j & 3) * 512 + vb * 256;
+                     go = fsm::GAM + (j % fsm::NGAM) * 512 + vb * 256;
       const float2 gam = prep_chunk_pair<16>(
           sbase + fsm::Q + s * 16384, sbase + fsm::K + s * 16384, x,
-          reinterpret_cast<float *>(sm + fsm::GAM + (j & 3) * 512),
+          reinterpret_cast<float *>(sm + fsm::GAM + (j % fsm::NGAM) * 512),
           reinterpret_cast<float *>(sm + fsm::XCH) + (2 * grp + ((j >> 1) & 1)) * 512, tg, lane, vb, L, a.scale,
           true, false, false, make_float2(1.f, 1.f), 1 + grp, 128);
       // decay outside the range of the chunk-local factorisation (NaN too)
@@ -419,7 +447,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       named_bar(1 + grp, 128);
       if (tg == 0 && lane == 0) {
         const uint32_t pbar = mapa_shared(smem_u32(&prep_done[s]), peer);
-        const uint32_t gbar = mapa_shared(smem_u32(&gam_ready[j & 3]), peer);
+        const uint32_t gbar = mapa_shared(smem_u32(&gam_ready[j % fsm::NGAM]), peer);
         mbar_arrive_expect_tx_cluster(pbar, 16384u);
         bulk_copy_to_cluster(rem + qo, sbase + qo, 8192, pbar);
         bulk_copy_to_cluster(rem + ko, sbase + ko, 8192, pbar);
@@ -427,7 +455,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
         bulk_copy_to_cluster(rem + go, sbase + go, 256, gbar);
       }
       mbar_arrive(&prep_done[s]);
-      mbar_arrive(&gam_ready[j & 3]);
+      mbar_arrive(&gam_ready[j % fsm::NGAM]);
     }
   } else {
     // ---------------- epilogue warpgroup ----------------
@@ -443,7 +471,7 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       const float *h0row = a.h0 ? a.h0 + ((d * H + h) * KD + c) * VD : nullptr;
       piece_state_in<64>(S, h0row, a.lbuf, a.dbuf, u - un.piece, un.piece, H, h, c, v0);
     }
-    for (int t = 0; t < 4; ++t) mask_tile_init(sm + fsm::P + t * 8192, qw, lane);
+    for (int t = 0; t < 2; ++t) mask_tile_init(sm + fsm::P + t * 8192, qw, lane);
     store_state_bf16(sm + fsm::S + 16384, c, S);
     fence_async_smem();
     mbar_arrive(&s_ready[1]);
@@ -459,18 +487,18 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
       }
       ph_p ^= 1u << b;
       tc_fence_after();
-      mask_tile_to_smem_hilo(tP, lane_off, qw, lane, sm + fsm::P + b * 16384, sm + fsm::P + b * 16384 + 8192);
+      mask_tile_to_smem_hilo(tP, lane_off, qw, lane, sm + fsm::P, sm + fsm::P + 8192);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[b]);
       // S3a: state update S <- exp(Gam) (S + kt^T V), bf16 copy for the next readout
       if (!mbar_wait(&u_full[b], (ph_u >> b) & 1, WAIT_CYCLES) ||
-          !mbar_wait_cluster(&gam_ready[j & 3], (j >> 2) & 1, WAIT_CYCLES)) {
+          !mbar_wait_cluster(&gam_ready[j % fsm::NGAM], (j / fsm::NGAM) & 1, WAIT_CYCLES)) {
         FAIL_AND_BREAK
       }
       ph_u ^= 1u << b;
       tc_fence_after();
-      const float eG = reinterpret_cast<const float *>(sm + fsm::GAM)[(j & 3) * 128 + c];
+      const float eG = reinterpret_cast<const float *>(sm + fsm::GAM)[(j % fsm::NGAM) * 128 + c];
 #pragma unroll
       for (int cp = 0; cp < 4; cp += 2) {
         uint32_t r[16], r2[16];
