@@ -9,6 +9,7 @@
 
 #include "internal.cuh"
 #include "tc.cuh"
+#include "tc_ssd.cuh"
 #include "tc_ptx.cuh"
 
 namespace glacore {
@@ -176,6 +177,7 @@ __global__ void state_scan_kernel(const float *L, const float *D, int64_t R, int
 namespace {
 
 struct Layout {
+  bool ssd;            // SSD tensor-core kernels (one gate per head, V = 64)
   bool tc;             // tensor-core path
   bool ssdx;           // SSD through the GLA tensor-core kernels (states padded in the workspace)
   int chunk;           // chunk length of the state workspace / doc table
@@ -248,9 +250,10 @@ bool ssdx_supported(const glacore_problem *p, bool head_gate, bool backward) {
 Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
   Layout L;
   memset(&L, 0, sizeof(L));
-  L.tc = tc::supported(p, head_gate, backward);
-  L.ssdx = !L.tc && ssdx_supported(p, head_gate, backward);
-  L.chunk = (L.tc || L.ssdx) ? tc::C : simt_chunk(p);
+  L.ssd = head_gate && !backward && ssd::supported(p);
+  L.tc = !L.ssd && tc::supported(p, head_gate, backward);
+  L.ssdx = !L.ssd && !L.tc && ssdx_supported(p, head_gate, backward);
+  L.chunk = (L.ssd || L.tc || L.ssdx) ? tc::C : simt_chunk(p);
   const int64_t BT = p->B * p->T, n = p->n_seqs;
   size_t off = 0;
   if (p->segment_ids) {
@@ -259,7 +262,10 @@ Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
     L.off_cbase = off;
     off = align256(off + sizeof(int64_t) * (n + 1));
   }
-  if (L.ssdx) {
+  if (L.ssd) {
+    L.off_tc = off;
+    off = align256(off + ssd::workspace_bytes(p, backward));
+  } else if (L.ssdx) {
     const size_t rows = (size_t)BT * p->H, bf = rows * 128 * 2, f32 = rows * 128 * 4;
     const size_t st = (size_t)n * p->H * 128 * 128 * 4;
     auto take = [&](size_t &o, size_t bytes) {
@@ -356,9 +362,9 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
   const int64_t BT = p->B * p->T;
   if (BT > 0 && !o) return GLACORE_ERR_INVALID_ARG;
   const Layout L = layout(p, head_gate, false);
-  if (!L.tc && !L.ssdx && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
+  if (!L.ssd && !L.tc && !L.ssdx && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
   if ((s = check_ws(p, L))) return s;
-  if ((L.tc || L.ssdx) && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
+  if ((L.ssd || L.tc || L.ssdx) && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
                 aligned16(o) && aligned16(ht) && aligned16(p->initial_state)))
     return GLACORE_ERR_INVALID_ARG;
   if (BT == 0) return GLACORE_OK;
@@ -370,6 +376,7 @@ glacore_status run_fwd(const glacore_problem *p, bool head_gate, void *o, float 
     if (e != cudaSuccess) return status_of(e);
   }
   const Docs docs = make_docs(p, L, ws);
+  if (L.ssd) return cuda_status(ssd::fwd(make_prob(p, true), docs, p, o, ht, ws + L.off_tc, st));
   if (L.ssdx) {
     const int64_t mats = p->n_seqs * p->H;
     // q, k of the head groups, the per-head gate and the V-column v are read

@@ -184,17 +184,15 @@ def test_binding_refuses_cpu_tensors():
         glc.gla_fwd(x, x, x, torch.zeros(1, 4, 1, 8))
 
 
-def test_ssd_tensor_core_path_has_no_broadcast_copies():
-    """SSD with one B/C group (workload 3's shape) runs the tensor-core kernels
-    on the grouped q / k, the per-head gate and the 64-column v in place: its
-    forward workspace holds the padded final states and the kernels' own
-    scratch, far below one copy of q broadcast to every head."""
+def test_ssd_forward_needs_no_copies():
+    """SSD with one B/C group and V = 64 (workload 3's shape) runs its own
+    tensor-core forward on the grouped q / k, the per-head gate and v in
+    place: no workspace for plain rows, only the launch order (one int32 per
+    document) for a packed batch."""
     lib = glc.load()
     B, T, H, K, V = 4, 4096, 32, 128, 64
     p = make_problem(B=B, T=T, H=H, Hqk=1, K=K, V=V, n_seqs=B, scale=1.0)
-    ws = lib.ssd_fwd_workspace_size(ctypes.byref(p))
-    one_copy = B * T * H * K * 2
-    assert 0 < ws < one_copy // 4
-    # V below 64 runs the CUDA-core kernels, which need no forward workspace here
-    p_small = make_problem(B=B, T=T, H=H, Hqk=1, K=K, V=32, n_seqs=B, scale=1.0)
-    assert lib.ssd_fwd_workspace_size(ctypes.byref(p_small)) < ws
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(p)) == 0
+    packed = make_problem(B=B, T=T, H=H, Hqk=1, K=K, V=V, n_seqs=100, scale=1.0, segment_ids=2048)
+    ws = lib.ssd_fwd_workspace_size(ctypes.byref(packed))
+    assert 100 * 4 <= ws <= 4096

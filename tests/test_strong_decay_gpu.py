@@ -1,11 +1,14 @@
 """Strong decay on the GPU, against the fp64 oracle.
 
-Inside a chunk the kernels factor the decay between tokens t >= s as
+Inside a chunk the GLA kernels factor the decay between tokens t >= s as
 exp(G_t) * exp(-G_s), with G the prefix sum of the log-decay from the chunk
 start (FLAT blog, "Gated Linear Attention"; "Backward Kernels" names strong
 decay as the method's precision edge).  The factors stay in the fp32 / bf16
 exponent range while every chunk's summed log-decay in every channel is at
-least -80.  These tests check the three sides of that bound:
+least -80.  The SSD forward needs no such bound: with one decay per head it
+applies exp(G_t - G_s) (s <= t) as one factor or as a product of factors
+that are each at most 1 (FLAT blog, "Mamba-2"), so Mamba-2 gates of any
+strength run on the tensor cores.  These tests check the sides of the bound:
 
 - inside it, with decay far stronger than the workloads' (GLA's gate without
   its 1/16 normaliser, per-chunk sums near -52), the tensor-core kernels
@@ -123,10 +126,13 @@ PAST = {
     "gla_const3_pieces": lambda: gate(case(5, 54, B=1, T=2000, H=1, Hqk=1), "const3", 0),
     "gla_sum200_300_pieces_packed": lambda: gate(case(4, 55, B=1, T=3000, H=1, Hqk=1, doc_mean=700),
                                                  "sum200_300", 7),
+}
+# Mamba-2 gates past the GLA kernels' range
+SSD_STRONG = {
     "ssd_g2": lambda: gate(case(3, 56, B=1, T=200, H=4), "ssd2", 8),
     "ssd_g2_packed": lambda: gate(case(3, 57, B=2, T=150, H=4, packed=True, doc_mean=40, initial_state=True,
                                        final_state=True), "ssd2", 9),
-    "ssd_sum200_300_pieces": lambda: gate(case(3, 58, B=1, T=2000, H=2), "sum200_300", 10),
+    "ssd_sum200_300": lambda: gate(case(3, 58, B=1, T=2000, H=2), "sum200_300", 10),
 }
 
 
@@ -151,9 +157,22 @@ def test_decay_past_the_tensor_core_range_is_reported(cuda_ok, name):
     glc.get_device_error()  # cleared
 
 
-@pytest.mark.parametrize("name", sorted(PAST))
+@pytest.mark.parametrize("name", sorted(SSD_STRONG))
+def test_ssd_strong_decay_forward_on_tensor_cores(cuda_ok, name):
+    d = SSD_STRONG[name]()
+    x = inputs.to_device(d, "cuda")
+    glc.get_device_error()
+    o, ht = glc.ssd_fwd(x["q"], x["k"], x["v"], x["g"], d["scale"], x["segment_ids"], x["h0"], True, 0,
+                        d["n_seqs"], poison=True)
+    torch.cuda.synchronize()
+    glc.get_device_error()
+    ro, rht = oracle.fwd(d["q"], d["k"], d["v"], d["g"], d["scale"], d["segment_ids"], d["h0"])
+    compare(dict(o=np64(o), ht=np64(ht)), dict(o=ro, ht=rht))
+
+
+@pytest.mark.parametrize("name", sorted(PAST) + sorted(SSD_STRONG))
 def test_decay_past_the_tensor_core_range_with_chunk_16(cuda_ok, name):
-    d = PAST[name]()
+    d = (PAST.get(name) or SSD_STRONG[name])()
     compare(run_gpu(d, 16), run_oracle(d))
 
 
