@@ -570,6 +570,20 @@ def run_glacore(args, w):
     return 0
 
 
+def run_fusions_only(args):
+    import torch
+
+    import chunked_gated_linear_chunk_gb300 as glc
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    glc.load()
+    out = {name: measure_fusion(name, spec, dev, args.steps, not args.no_cpu_baseline)
+           for name, spec in FUSIONS.items()}
+    print(json.dumps({"fusions": out}), flush=True)
+    return 0
+
+
 def run_e2e(args, w, d, dev, world, fwd_fn, bwd_fn, scale, n_seqs, nf, nb):
     """End to end through the public API from pinned host buffers: every step
     copies its inputs host -> device, runs the forward and backward, and
@@ -724,6 +738,8 @@ def main(argv=None):
                     help="skip the per-workload entries (all five workloads, timed after the headline one)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX, choices=[1, 2, 3, 4, 5],
                     help="synthetic workload (default 2: GLA B4 H16 T2048 d128 bf16, the headline)")
+    ap.add_argument("--fusions-only", action="store_true",
+                    help="time only the two fused operations around the recurrence (one JSON line)")
     ap.add_argument("--ingest-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.json from an ncu DRAM-bytes capture and exit")
     args = ap.parse_args(argv)
@@ -734,6 +750,8 @@ def main(argv=None):
     from chunked_gated_linear_chunk_gb300 import inputs
 
     w = inputs.WORKLOADS[args.workload]
+    if args.fusions_only:
+        return run_fusions_only(args)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_glacore(args, w)
