@@ -250,7 +250,7 @@ bool ssdx_supported(const glacore_problem *p, bool head_gate, bool backward) {
 Layout layout(const glacore_problem *p, bool head_gate, bool backward) {
   Layout L;
   memset(&L, 0, sizeof(L));
-  L.ssd = head_gate && !backward && ssd::supported(p);
+  L.ssd = head_gate && ssd::supported(p);
   L.tc = !L.ssd && tc::supported(p, head_gate, backward);
   L.ssdx = !L.ssd && !L.tc && ssdx_supported(p, head_gate, backward);
   L.chunk = (L.ssd || L.tc || L.ssdx) ? tc::C : simt_chunk(p);
@@ -405,9 +405,9 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
   const int64_t BT = p->B * p->T;
   if (BT > 0 && (!dO || !dq || !dk || !dv || !dg)) return GLACORE_ERR_INVALID_ARG;
   const Layout L = layout(p, head_gate, true);
-  if (!L.tc && !L.ssdx && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
+  if (!L.ssd && !L.tc && !L.ssdx && !simt_supported(p)) return GLACORE_ERR_UNSUPPORTED;
   if ((s = check_ws(p, L))) return s;
-  if ((L.tc || L.ssdx) && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
+  if ((L.ssd || L.tc || L.ssdx) && !(aligned16(p->q) && aligned16(p->k) && aligned16(p->v) && aligned16(p->g) &&
                 aligned16(dO) && aligned16(dht) && aligned16(dq) && aligned16(dk) &&
                 aligned16(dv) && aligned16(dg) && aligned16(dh0) &&
                 aligned16(p->initial_state)))
@@ -421,6 +421,8 @@ glacore_status run_bwd(const glacore_problem *p, bool head_gate, const void *dO,
     if (e != cudaSuccess) return status_of(e);
   }
   const Docs docs = make_docs(p, L, ws);
+  if (L.ssd)
+    return cuda_status(ssd::bwd(make_prob(p, true), docs, p, dO, dht, dq, dk, dv, dg, dh0, ws + L.off_tc, st));
   if (L.ssdx) {
     const int64_t rows = BT * p->H, mats = p->n_seqs * p->H;
     // q, k of the head groups, the per-head gate, the V-column v and do are

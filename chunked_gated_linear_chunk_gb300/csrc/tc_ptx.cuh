@@ -176,6 +176,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *s
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Element-wise add of a shared-memory tile into global memory, done by the
+// TMA unit at L2 (the map's element type, here fp32; same bulk group as
+// tma_store_3d).  Rows outside the map's extent are not written.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *m, const void *src, int x, int y, int z) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   (uint64_t)m),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the issuing thread's committed stores have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read_all() {
@@ -337,6 +346,19 @@ __device__ __forceinline__ uint32_t sw128_off_f32(uint32_t r, uint32_t c, uint32
 // Named barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// The same barrier, also OR-ing a predicate over the participating threads:
+// every thread gets the same answer, so a loop that contains named barriers
+// can leave on it without stranding the others at the next barrier.
+__device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, %3, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 }  // namespace ptx

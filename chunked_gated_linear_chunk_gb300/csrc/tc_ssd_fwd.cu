@@ -48,118 +48,13 @@ constexpr uint32_t V = 98304;      // 3 x 8 KB
 constexpr uint32_t VT = 122880;    // 2 x 8 KB: v (.) exp(Gam - G_s)
 constexpr uint32_t P = 139264;     // 2 x 16 KB: masked P, bf16 hi (+0) and lo (+8 KB)
 constexpr uint32_t S = 172032;     // 2 x 16 KB: S as bf16 (rows = channel)
-constexpr uint32_t GS = 204800;    // 3 gate slots of GSLOT bytes
-constexpr int NG = 3;
-constexpr uint32_t GSLOT = 7680;
-constexpr uint32_t BYTES = GS + NG * GSLOT;
-// gate slot (floats):
-//   EG [0, 64)      scale exp(G_t) (0 past the chunk's end)
-//   EGR [64, 128)   exp(Gam - G_s) (0 past the end)
-//   B [128, 192)    exp(G_r - G_s), r the last token of s's 16-token block
-//   EGAM at 192     exp(Gam)
-//   A [196, 452)    row t, block b < t / 16: scale exp(G_t - G_r), r the
-//                   last token of block b (4 per row)
-//   G [452, 516)    G
-//   DD [516, 1796)  diagonal blocks: [4][16][20], scale exp(G_t - G_s) for
-//                   s <= t in the same block, 0 above (row stride 20), as
-//                   products of the per-token factors exp(g)
-//   E [1796, 1860)  exp(g_t)
-// Off the diagonal, exp(G_t - G_s) = exp(G_t - G_r) exp(G_r - G_s) with
-// t > r >= s: both factors in (0, 1].
-constexpr int G_EG = 0, G_EGR = 64, G_B = 128, G_EGAM = 192, G_A = 196, G_G = 452, G_DD = 516, G_E = 1796;
+constexpr uint32_t GS = 204800;    // gsl::NG gate slots
+constexpr uint32_t BYTES = GS + gsl::NG * gsl::GSLOT;
 }  // namespace ffs
-
-// The decayed causal P of one chunk as bf16 hi / lo tiles (K-major A of the
-// P v product):  P[t,s] = QK[t,s] F[t,s], F = scale exp(G_t - G_s) for
-// s <= t, else 0, from the gate slot's factor tables.  The M = 64
-// accumulator holds warp qw's rows 16 qw .. 16 qw + 15 in lanes 0..15;
-// lanes 16..31 take the second 16-column block of each pair (shuffled
-// over), so every lane writes one block.  Blocks above the diagonal stay
-// zero (written once by mask_tile_init).
-__device__ __forceinline__ void decay_mask_hilo(uint32_t t_acc, uint32_t lane_off, int qw, int lane,
-                                                uint8_t *hi, uint8_t *lo, const float *gs) {
-  using namespace ffs;
-  const int rl = lane & 15, row = qw * 16 + rl;
-  const bool second = lane >= 16;
-  uint32_t r[2][16], x[2][16];
-#pragma unroll
-  for (int cp = 0; cp < 4; cp += 2)
-    if (cp <= qw) {
-      tmem_ld16(t_acc + lane_off + cp * 16, r[cp / 2]);
-      tmem_ld16(t_acc + lane_off + cp * 16 + 16, x[cp / 2]);
-    }
-  tmem_ld_wait(r[0]);
-  tmem_tie(x[0]);
-  if (qw >= 2) {
-    tmem_tie(r[1]);
-    tmem_tie(x[1]);
-  }
-  const float4 arow = *reinterpret_cast<const float4 *>(gs + G_A + 4 * row);
-#pragma unroll
-  for (int cp = 0; cp < 4; cp += 2) {
-    if (cp <= qw) {
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t sh = __shfl_sync(0xffffffffu, x[cp / 2][i], rl);
-        v[i] = __uint_as_float(second ? sh : r[cp / 2][i]);
-      }
-      const int cb = cp + (second ? 1 : 0);
-      if (cb <= qw) {
-        float f[16];
-        if (cb < qw) {
-          const float a = cb == 0 ? arow.x : (cb == 1 ? arow.y : arow.z);
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 b = *reinterpret_cast<const float4 *>(gs + G_B + cb * 16 + i);
-            f[i] = a * b.x;
-            f[i + 1] = a * b.y;
-            f[i + 2] = a * b.z;
-            f[i + 3] = a * b.w;
-          }
-        } else {
-          const float *dd = gs + G_DD + (qw * 16 + rl) * 20;
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 b = *reinterpret_cast<const float4 *>(dd + i);
-            f[i] = b.x;
-            f[i + 1] = b.y;
-            f[i + 2] = b.z;
-            f[i + 3] = b.w;
-          }
-        }
-        uint32_t w[8], wl[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float x0 = v[2 * e] * f[2 * e], x1 = v[2 * e + 1] * f[2 * e + 1];
-          w[e] = pack_bf16(x0, x1);
-          wl[e] = pack_bf16(x0 - __uint_as_float(w[e] << 16), x1 - __uint_as_float(w[e] & 0xffff0000u));
-        }
-        const uint32_t o0 = sw128_off(row, cb * 16, 64), o1 = sw128_off(row, cb * 16 + 8, 64);
-        st_shared_v4(smem_u32(hi + o0), w[0], w[1], w[2], w[3]);
-        st_shared_v4(smem_u32(hi + o1), w[4], w[5], w[6], w[7]);
-        st_shared_v4(smem_u32(lo + o0), wl[0], wl[1], wl[2], wl[3]);
-        st_shared_v4(smem_u32(lo + o1), wl[4], wl[5], wl[6], wl[7]);
-      }
-    }
-  }
-}
-
-// Row c (channel) of the bf16 state tile (128 rows x 64 columns, 128-byte
-// swizzle): the B operand of q S, MN-major.
-__device__ __forceinline__ void store_state_row(uint8_t *St, int c, const float (&S)[64]) {
-#pragma unroll
-  for (int n = 0; n < 64; n += 8)
-    st_shared_v4(smem_u32(St + sw128_off(c, n, 128)), pack_bf16(S[n], S[n + 1]), pack_bf16(S[n + 2], S[n + 3]),
-                 pack_bf16(S[n + 4], S[n + 5]), pack_bf16(S[n + 6], S[n + 7]));
-}
-
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t x, float f) {
-  return pack_bf16(__uint_as_float(x << 16) * f, __uint_as_float(x & 0xffff0000u) * f);
-}
 
 __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
   using namespace ffs;
+  using namespace gsl;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[NS], empty[NS], gready[NG], gfree[NG], qk_full[2], u_full[2], qs_full[2], pv_full[2],
@@ -331,7 +226,7 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
         break;
       }
       tc_fence_after();
-      decay_mask_hilo(tQK(bb), lane_off, qw, lane, sm + P + bb * 16384, sm + P + bb * 16384 + 8192, slot_of(j));
+      decay_mask<true>(tQK(bb), lane_off, qw, lane, sm + P + bb * 16384, sm + P + bb * 16384 + 8192, slot_of(j));
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready[bb]);
@@ -458,55 +353,18 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
       float *gs = slot_of(jj);
       // the slot was last read by the mask, state and output steps of
       // jj - NG; vt's buffer by U(jj - 2)
-      if (jj >= NG && !mbar_wait(&gfree[gsl], ((jj / NG) - 1) & 1, WAIT_CYCLES)) return false;
-      if (jj >= 2 && !mbar_wait(&u_full[bb], ((jj - 2) >> 1) & 1, WAIT_CYCLES)) return false;
-      const int t = tid, blk = t >> 4, r = t & 15;
+      bool good = true;
+      if (jj >= NG && !mbar_wait(&gfree[gsl], ((jj / NG) - 1) & 1, WAIT_CYCLES)) good = false;
+      if (jj >= 2 && !mbar_wait(&u_full[bb], ((jj - 2) >> 1) & 1, WAIT_CYCLES)) good = false;
+      const int t = tid;
       const float gt = gnext;
       gnext = gnext2;
       gnext2 = load_g(jj + 2);
-      // G: inclusive prefix sum over the chunk (warp 15 adds warp 14's total)
-      float Gt = gt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, Gt, o);
-        if (lane >= o) Gt += y;
-      }
-      if (t == 31) gs[G_EGAM + 2] = Gt;
-      named_bar(2, 64);
-      if (t >= 32) Gt += gs[G_EGAM + 2];
-      gs[G_G + t] = Gt;
-      gs[G_E + t] = __expf(gt);
-      if (t == L - 1) {
-        gs[G_EGAM] = __expf(Gt);
-        gs[G_EGAM + 1] = Gt;
-      }
-      named_bar(2, 64);
-      const float Gam = gs[G_EGAM + 1];
-      const float egr = t < L ? __expf(Gam - Gt) : 0.f;
-      gs[G_EG + t] = t < L ? a.scale * __expf(Gt) : 0.f;
-      gs[G_EGR + t] = egr;
-      gs[G_B + t] = __expf(gs[G_G + (t | 15)] - Gt);
-      {  // row factors of row t (blocks before t's own)
-        float av[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) av[b] = (b < blk) ? a.scale * __expf(Gt - gs[G_G + 16 * b + 15]) : 0.f;
-        *reinterpret_cast<float4 *>(gs + G_A + 4 * t) = make_float4(av[0], av[1], av[2], av[3]);
-      }
-      {  // row t of its diagonal block: scale exp(G_t - G_c) = scale prod_{c < i <= t} exp(g_i)
-        const float *e = gs + G_E + 16 * blk;
-        float dv[16];
-        float run = a.scale;
-#pragma unroll
-        for (int c = 15; c >= 0; --c) {
-          dv[c] = c <= r ? run : 0.f;
-          if (c <= r && c > 0) run *= e[c];
-        }
-        float *dd = gs + G_DD + t * 20;
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4 *>(dd + i) = make_float4(dv[i], dv[i + 1], dv[i + 2], dv[i + 3]);
-      }
+      float egr, eg;
+      gate_factors(gs, t, lane, L, a.scale, gt, 2, egr, eg);
+      (void)eg;
       // vt = v (.) exp(Gam - G_s): row t
-      if (!mbar_wait(&full[s], (jj / NS) & 1, WAIT_CYCLES)) return false;
+      if (!good || !mbar_wait(&full[s], (jj / NS) & 1, WAIT_CYCLES)) return false;
       {
         const uint8_t *src = sm + V + s * 8192;
         uint8_t *dst = sm + VT + bb * 8192;
@@ -522,8 +380,13 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
       mbar_arrive(&gready[gsl]);
       return true;
     };
+    // the 64 threads leave the loop together (gate_factors holds named
+    // barriers): a failed wait only stops the loop at the next chunk
     bool ok = true;
-    for (int j = 0; ok && j < nch && !*abortp; ++j) ok = prep(j);
+    for (int j = 0; j < nch; ++j) {
+      if (named_bar_any(2, 64, !ok || *abortp)) break;
+      ok = prep(j) && ok;
+    }
     if (!ok) atomicExch(&abort_flag, 1);
   }
 #undef SSD_FAIL
@@ -550,9 +413,9 @@ bool supported(const glacore_problem *p) {
 static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 size_t workspace_bytes(const glacore_problem *p, bool backward) {
+  if (backward) return bwd_workspace_bytes(p);
   size_t off = 0;
   if (p->segment_ids) off = al256(off + (size_t)p->n_seqs * sizeof(int32_t));  // launch order
-  (void)backward;
   return off;
 }
 

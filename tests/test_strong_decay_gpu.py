@@ -5,10 +5,10 @@ exp(G_t) * exp(-G_s), with G the prefix sum of the log-decay from the chunk
 start (FLAT blog, "Gated Linear Attention"; "Backward Kernels" names strong
 decay as the method's precision edge).  The factors stay in the fp32 / bf16
 exponent range while every chunk's summed log-decay in every channel is at
-least -80.  The SSD forward needs no such bound: with one decay per head it
-applies exp(G_t - G_s) (s <= t) as one factor or as a product of factors
-that are each at most 1 (FLAT blog, "Mamba-2"), so Mamba-2 gates of any
-strength run on the tensor cores.  These tests check the sides of the bound:
+least -80.  The SSD kernels need no such bound: with one decay per head
+they apply exp(G_t - G_s) (s <= t) as one factor or as a product of
+factors that are each at most 1 (FLAT blog, "Mamba-2"), so Mamba-2 gates
+of any strength run forward and backward on the tensor cores.  These tests check the sides of the bound:
 
 - inside it, with decay far stronger than the workloads' (GLA's gate without
   its 1/16 normaliser, per-chunk sums near -52), the tensor-core kernels
@@ -158,16 +158,9 @@ def test_decay_past_the_tensor_core_range_is_reported(cuda_ok, name):
 
 
 @pytest.mark.parametrize("name", sorted(SSD_STRONG))
-def test_ssd_strong_decay_forward_on_tensor_cores(cuda_ok, name):
+def test_ssd_strong_decay_on_tensor_cores(cuda_ok, name):
     d = SSD_STRONG[name]()
-    x = inputs.to_device(d, "cuda")
-    glc.get_device_error()
-    o, ht = glc.ssd_fwd(x["q"], x["k"], x["v"], x["g"], d["scale"], x["segment_ids"], x["h0"], True, 0,
-                        d["n_seqs"], poison=True)
-    torch.cuda.synchronize()
-    glc.get_device_error()
-    ro, rht = oracle.fwd(d["q"], d["k"], d["v"], d["g"], d["scale"], d["segment_ids"], d["h0"])
-    compare(dict(o=np64(o), ht=np64(ht)), dict(o=ro, ht=rht))
+    compare(run_gpu(d, 0), run_oracle(d))
 
 
 @pytest.mark.parametrize("name", sorted(PAST) + sorted(SSD_STRONG))
