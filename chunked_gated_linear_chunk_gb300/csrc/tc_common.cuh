@@ -53,13 +53,13 @@ inline EncodeFn encoder() {
 // elements: one 128-byte row per token).  row_stride: elements between
 // consecutive tokens (0: heads * D, contiguous).
 inline bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t D, int64_t heads,
-                     int64_t BT, int box_x, int64_t row_stride = 0) {
+                     int64_t BT, int box_x, int64_t row_stride = 0, int box_rows = C) {
   EncodeFn enc = encoder();
   if (!enc) return false;
   const int es = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)BT};
   cuuint64_t strides[2] = {(cuuint64_t)(D * es), (cuuint64_t)((row_stride ? row_stride : heads * D) * es)};
-  cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
+  cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                    const_cast<void *>(base), dims, strides, box, estr,

@@ -176,6 +176,11 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *s
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Four fp32 adds to consecutive global words (16-byte aligned), done at L2.
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 // Element-wise add of a shared-memory tile into global memory, done by the
 // TMA unit at L2 (the map's element type, here fp32; same bulk group as
 // tma_store_3d).  Rows outside the map's extent are not written.

@@ -63,7 +63,7 @@ constexpr uint32_t VT = 98304;    // 2 x 8 KB: v (.) exp(Gam - G_s)
 constexpr uint32_t DOT = 114688;  // 2 x 8 KB: do (.) scale exp(G_t)
 constexpr uint32_t DAF = 131072;  // 2 x 8 KB: dA (bf16, K-major A of dA k)
 constexpr uint32_t S = 147456;    // 2 x 16 KB: S as bf16
-constexpr uint32_t DQT = 180224;  // 16 KB: half of the dq_h tile (fp32, two 32-column blocks)
+constexpr uint32_t DQT = 180224;  // 16 KB: 2 KB staging buffers, two per output warp
 constexpr uint32_t GS = 196608;
 constexpr uint32_t BYTES = GS + gsl::NG * gsl::GSLOT;
 }  // namespace pas
@@ -79,67 +79,64 @@ constexpr uint32_t DOT = 114688;  // 2 x 8 KB
 constexpr uint32_t A = 131072;    // 8 KB: A (bf16)
 constexpr uint32_t DAF = 139264;  // 8 KB: dA (bf16)
 constexpr uint32_t DS = 147456;   // 2 x 16 KB: dS as bf16 (rows = channel)
-constexpr uint32_t DKT = 180224;  // 16 KB: half of the dk_h tile (fp32)
+constexpr uint32_t DKT = 180224;  // 16 KB: 2 KB staging buffers, two per output warp
 constexpr uint32_t GS = 196608;
 constexpr uint32_t BYTES = GS + gsl::NG * gsl::GSLOT;
 }  // namespace pbs
 
-// Adds this CTA's 64 x 128 fp32 tile of a per-head gradient (M = 64
-// accumulator t_acc, 128 columns) into the group accumulator (map m, rows
-// tok0 .., head group hq) in two rounds of 64 channels through a 16 KB
-// staging tile, by TMA reduce-add; rows at or past L are added as zeros.
-// Returns this lane's share of sum_c x[row, c] acc[row, c], x the bf16 tile
-// (q or k of the chunk: two 64-column blocks, 128-byte swizzle).  Called
-// by the 128 threads of one warpgroup (named barrier `bar`).
-__device__ __forceinline__ float reduce_tile_rows(uint32_t t_acc, uint32_t lane_off, int qw, int lane, int L,
-                                                  uint8_t *stage, const uint8_t *xt, const CUtensorMap *m, int hq,
-                                                  int tok0, int bar, bool leader) {
+// Adds one warp's 16 rows (16 qw .. 16 qw + 15) of this CTA's 64 x 128
+// fp32 tile of a per-head gradient (M = 64 accumulator t_acc, 128 columns)
+// into the group accumulator (map m: boxes of 32 channels x 16 rows; rows
+// tok0 + 16 qw .., head group hq), by TMA reduce-add at L2, in four rounds
+// of 32 channels through the warp's two 2 KB staging buffers (stg, used in
+// turn: a buffer is rewritten once the reduce issued from it two rounds
+// earlier has read it).  Rows at or past L are added as zeros.  Returns
+// this lane's share of sum_c x[row, c] acc[row, c], x the bf16 tile (q or
+// k of the chunk: two 64-column blocks, 128-byte swizzle).  Lanes r and
+// r + 16 share row 16 qw + r (the first and second 16 columns of a round).
+__device__ __forceinline__ float reduce_warp_rows(uint32_t t_acc, uint32_t lane_off, int qw, int lane, int L,
+                                                  uint8_t *stg, const uint8_t *xt, const CUtensorMap *m, int hq,
+                                                  int tok0) {
   const int rl = lane & 15, row = qw * 16 + rl;
-  const bool second = lane >= 16;
+  const bool second = lane >= 16, live = row < L;
   float dot = 0.f;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    uint32_t a[4][16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tmem_ld16(t_acc + lane_off + 64 * k + 16 * i, a[i]);
-    tmem_ld_wait(a[0]);
-    tmem_tie(a[1]);
-    tmem_tie(a[2]);
-    tmem_tie(a[3]);
-    // lanes 0..15: columns 64 k + 0..31, lanes 16..31: 64 k + 32..63
-    float y[32];
+  for (int r = 0; r < 4; ++r) {
+    uint32_t a0[16], a1[16];
+    tmem_ld16(t_acc + lane_off + 32 * r, a0);
+    tmem_ld16(t_acc + lane_off + 32 * r + 16, a1);
+    tmem_ld_wait(a0);
+    tmem_tie(a1);
+    float y[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const uint32_t s2 = __shfl_sync(0xffffffffu, a[2][i], rl), s3 = __shfl_sync(0xffffffffu, a[3][i], rl);
-      y[i] = __uint_as_float(second ? s2 : a[0][i]);
-      y[16 + i] = __uint_as_float(second ? s3 : a[1][i]);
+      const uint32_t sh = __shfl_sync(0xffffffffu, a1[i], rl);
+      y[i] = __uint_as_float(second ? sh : a0[i]);
     }
-    const int c0 = 64 * k + (second ? 32 : 0);
-    const bool live = row < L;
+    const int c0 = 32 * r + (second ? 16 : 0);
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
+    for (int i = 0; i < 16; i += 8) {
       const uint4 xv = *reinterpret_cast<const uint4 *>(xt + sw128_off(row, c0 + i, 64));
       dot += __uint_as_float(xv.x << 16) * y[i] + __uint_as_float(xv.x & 0xffff0000u) * y[i + 1] +
              __uint_as_float(xv.y << 16) * y[i + 2] + __uint_as_float(xv.y & 0xffff0000u) * y[i + 3] +
              __uint_as_float(xv.z << 16) * y[i + 4] + __uint_as_float(xv.z & 0xffff0000u) * y[i + 5] +
              __uint_as_float(xv.w << 16) * y[i + 6] + __uint_as_float(xv.w & 0xffff0000u) * y[i + 7];
     }
-    // staging tile: block (second ? 1 : 0) of 32 columns, 64 rows
+    uint8_t *buf = stg + (r & 1) * 2048;
+    if (lane == 0) bulk_wait_read_all_but_one();  // the reduce from this buffer, two rounds back
+    __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const uint32_t off = (second ? 8192u : 0u) + sw128_off_f32(row, i, 64);
-      st_shared_v4(smem_u32(stage + off), __float_as_uint(live ? y[i] : 0.f), __float_as_uint(live ? y[i + 1] : 0.f),
+    for (int i = 0; i < 16; i += 4) {
+      const uint32_t off = sw128_off_f32(rl, (second ? 16 : 0) + i, 16);
+      st_shared_v4(smem_u32(buf + off), __float_as_uint(live ? y[i] : 0.f), __float_as_uint(live ? y[i + 1] : 0.f),
                    __float_as_uint(live ? y[i + 2] : 0.f), __float_as_uint(live ? y[i + 3] : 0.f));
     }
     fence_async_smem();
-    named_bar(bar, 128);
-    if (leader) {
-      tma_reduce_add_3d(m, stage, 64 * k, hq, tok0);
-      tma_reduce_add_3d(m, stage + 8192, 64 * k + 32, hq, tok0);
+    __syncwarp();
+    if (lane == 0) {
+      tma_reduce_add_3d(m, buf, 32 * r, hq, tok0 + 16 * qw);
       bulk_commit();
-      bulk_wait_read_all();
     }
-    named_bar(bar, 128);
   }
   return dot;
 }
@@ -373,17 +370,17 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_a_kernel(const __grid_constant
     // ---------------- dq_h out, q . dq_h ----------------
     const int qw = warp & 3, rl = lane & 15, row = qw * 16 + rl;
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    const bool leader = threadIdx.x == 320;
     bool ok = true;
-    for (int j = 0; j < nch; ++j) {
-      // the 128 threads leave together (named barriers below)
-      if (named_bar_any(3, 128, !ok || *abortp)) break;
+    for (int j = 0; j < nch && !*abortp; ++j) {
       const int b = j & 1, s = j % NS;
-      if (!mbar_wait(&dq_full[b], (j >> 1) & 1, WAIT_CYCLES)) ok = false;
+      if (!mbar_wait(&dq_full[b], (j >> 1) & 1, WAIT_CYCLES)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const int L = chunk_len(j);
-      float dot = reduce_tile_rows(tDQ(b), lane_off, qw, lane, L, sm + DQT, sm + Q + s * 16384, &maps.dqa, hq,
-                                   (int)chunk_tok(j), 3, leader);
+      float dot = reduce_warp_rows(tDQ(b), lane_off, qw, lane, L, sm + DQT + qw * 4096, sm + Q + s * 16384,
+                                   &maps.dqa, hq, (int)chunk_tok(j));
       tc_fence_before();
       mbar_arrive(&dq_free[b]);
       mbar_arrive(&empty[s]);
@@ -391,7 +388,7 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_a_kernel(const __grid_constant
       if (lane < 16 && row < L) a.qdq[(chunk_tok(j) + row) * H + h] = dot;
     }
     if (!ok) atomicExch(&abort_flag, 1);
-    if (leader) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   } else {
     // ---------------- gate ----------------
     const int tid = (int)threadIdx.x - 448;
@@ -456,8 +453,9 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_a_kernel(const __grid_constant
 //   warp 1       MMA: QK = q k^T, dP = do v^T, W = q^T dot,
 //                dV1 = A^T do, dV2 = k dS, dK = dA^T q + vt dS^T
 //   warps 2..5   mask: A = QK (.) F, dA = dP (.) F (bf16)
-//   warps 6..9   state: dS (fp32 in registers), bf16 copy, dh0 at the end
-//   warps 10..13 dv out; dk_h tile -> reduce-add; dg
+//   warps 6..9   state: dS (fp32 in registers), bf16 copy, dh0 at the end;
+//                then dv of the chunk
+//   warps 10..13 dk_h tile -> reduce-add; dg
 //   warps 14, 15 gate: the gate slot, vt, dot
 // TMEM: QK at 0, dP at 64, W at 128 (M = 128), dV1 at 192, dV2 at 256,
 // dK at 320 (64 x 128).
@@ -507,7 +505,7 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
     mbar_init(&p_ready, 128);
     mbar_init(&ds_ready[0], 128);
     mbar_init(&ds_ready[1], 128);
-    mbar_init(&tm_free, 128);
+    mbar_init(&tm_free, 256);  // dv (state warpgroup) and dk (output warpgroup) read out
     mbar_init(&drain, 1);
     fence_mbar_init();
   }
@@ -667,36 +665,17 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
       }
       tc_fence_before();
       mbar_arrive(&ds_ready[nb]);
-      mbar_arrive(&gfree[i % NG]);
-    }
-    if (!ok) atomicExch(&abort_flag, 1);
-    if (a.dh0 && !*abortp) {
-      float *dst = a.dh0 + ((d * H + h) * KD + c) * VD;
-#pragma unroll
-      for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(Dr[i], Dr[i + 1], Dr[i + 2], Dr[i + 3]);
-    }
-  } else if (warp < 14) {
-    // ---------------- dv, dk_h, dg ----------------
-    const int qw = warp & 3, rl = lane & 15, row = qw * 16 + rl;
-    const bool second = lane >= 16;
-    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    const bool leader = threadIdx.x == 320;
-    float carry = a.dht ? a.sdht[d * H + h] : 0.f;  // sum over later tokens + <dht, S_T>
-    bool ok = true;
-    for (int i = 0; i < nch; ++i) {
-      // the 128 threads leave together (named barriers below)
-      if (named_bar_any(3, 128, !ok || *abortp)) break;
-      const int s = i % NS;
-      if (!mbar_wait(&dv_full, i & 1, WAIT_CYCLES) || !mbar_wait(&dk_full, i & 1, WAIT_CYCLES) ||
-          !mbar_wait(&gready[i % NG], (i / NG) & 1, WAIT_CYCLES))
-        ok = false;
-      tc_fence_after();
-      const int L = chunk_len(i);
-      const int64_t tok0 = chunk_tok(i);
       // dv = A^T do + exp(Gam - G_s) (k dS)_s
+      if (!mbar_wait(&dv_full, i & 1, WAIT_CYCLES)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       {
+        const int rl = lane & 15, row = qw * 16 + rl, L = chunk_len(i);
+        const bool second = lane >= 16;
         const float egr = slot_of(i)[G_EGR + row];
-        __nv_bfloat16 *vrow = a.dv + ((tok0 + row) * H + h) * VD;
+        __nv_bfloat16 *vrow = a.dv + ((chunk_tok(i) + row) * H + h) * VD;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           uint32_t xa[16], xb[16], pa[16], pb[16];
@@ -723,8 +702,32 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
           }
         }
       }
-      float kdk = reduce_tile_rows(tDK, lane_off, qw, lane, L, sm + DKT, sm + K + s * 16384, &maps.dka, hq, (int)tok0,
-                                   3, leader);
+      tc_fence_before();
+      mbar_arrive(&tm_free);
+      mbar_arrive(&gfree[i % NG]);
+    }
+    if (!ok) atomicExch(&abort_flag, 1);
+    if (a.dh0 && !*abortp) {
+      float *dst = a.dh0 + ((d * H + h) * KD + c) * VD;
+#pragma unroll
+      for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(Dr[i], Dr[i + 1], Dr[i + 2], Dr[i + 3]);
+    }
+  } else if (warp < 14) {
+    // ---------------- dk_h, dg ----------------
+    const int qw = warp & 3, rl = lane & 15, row = qw * 16 + rl;
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    float carry = a.dht ? a.sdht[d * H + h] : 0.f;  // sum over later tokens + <dht, S_T>
+    bool ok = true;
+    for (int i = 0; i < nch; ++i) {
+      // the 128 threads leave together (named barriers below)
+      if (named_bar_any(3, 128, !ok || *abortp)) break;
+      const int s = i % NS;
+      if (!mbar_wait(&dk_full, i & 1, WAIT_CYCLES)) ok = false;
+      tc_fence_after();
+      const int L = chunk_len(i);
+      const int64_t tok0 = chunk_tok(i);
+      float kdk = reduce_warp_rows(tDK, lane_off, qw, lane, L, sm + DKT + qw * 4096, sm + K + s * 16384, &maps.dka,
+                                   hq, (int)tok0);
       tc_fence_before();
       mbar_arrive(&tm_free);
       mbar_arrive(&empty[s]);
@@ -749,7 +752,7 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
       mbar_arrive(&gfree[i % NG]);
     }
     if (!ok) atomicExch(&abort_flag, 1);
-    if (leader) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   } else {
     // ---------------- gate ----------------
     const int tid = (int)threadIdx.x - 448;
@@ -855,7 +858,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
       !make_map(&maps.k, pr.k, true, KD, pr.Hqk, pr.BT, 64, pr.ks) ||
       !make_map(&maps.v, pr.v, true, VD, pr.H, pr.BT, 64, pr.vs) ||
       !make_map(&maps.dout, dO, true, VD, pr.H, pr.BT, 64) ||
-      !make_map(&maps.dqa, dqa, false, KD, pr.Hqk, pr.BT, 32) || !make_map(&maps.dka, dka, false, KD, pr.Hqk, pr.BT, 32))
+      !make_map(&maps.dqa, dqa, false, KD, pr.Hqk, pr.BT, 32, 0, 16) ||
+      !make_map(&maps.dka, dka, false, KD, pr.Hqk, pr.BT, 32, 0, 16))
     return cudaErrorInvalidValue;
   BwdArgs a;
   memset(&a, 0, sizeof(a));
