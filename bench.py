@@ -691,7 +691,9 @@ def kernel_source_sha():
 
 # ncu kernel names -> the library's launch labels (template argument: mode)
 NCU_LABELS = (("gla_fwd_kernel", "gla_fwd_kernel"), ("piece_state_kernel", "piece_state_kernel"),
-              ("gla_bwd_rev_kernel", "gla_bwd_rev_kernel"), ("gla_bwd_dq_kernel", "gla_bwd_dq_kernel"))
+              ("gla_bwd_rev_kernel", "gla_bwd_rev_kernel"), ("gla_bwd_dq_kernel", "gla_bwd_dq_kernel"),
+              ("ssd_fwd_kernel", "ssd_fwd_kernel"), ("ssd_bwd_a_kernel", "ssd_bwd_a_kernel"),
+              ("ssd_bwd_b_kernel", "ssd_bwd_b_kernel"))
 
 
 def ingest_traffic(csv_path):

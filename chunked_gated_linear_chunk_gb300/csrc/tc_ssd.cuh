@@ -81,7 +81,8 @@ __device__ __forceinline__ void decay_mask(uint32_t t_acc, uint32_t lane_off, in
     tmem_tie(r[1]);
     tmem_tie(x[1]);
   }
-  const float4 arow = *reinterpret_cast<const float4 *>(gs + G_A + 4 * row);
+  const uint32_t ga = smem_u32(gs);
+  const float4 arow = lds_f4(ga + 4u * (G_A + 4 * row));
 #pragma unroll
   for (int cp = 0; cp < 4; cp += 2) {
     if (cp <= qw) {
@@ -98,17 +99,17 @@ __device__ __forceinline__ void decay_mask(uint32_t t_acc, uint32_t lane_off, in
           const float a = cb == 0 ? arow.x : (cb == 1 ? arow.y : arow.z);
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
-            const float4 b = *reinterpret_cast<const float4 *>(gs + G_B + cb * 16 + i);
+            const float4 b = lds_f4(ga + 4u * (G_B + cb * 16 + i));
             f[i] = a * b.x;
             f[i + 1] = a * b.y;
             f[i + 2] = a * b.z;
             f[i + 3] = a * b.w;
           }
         } else {
-          const float *dd = gs + G_DD + (qw * 16 + rl) * 20;
+          const uint32_t dd = ga + 4u * (G_DD + (qw * 16 + rl) * 20);
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
-            const float4 b = *reinterpret_cast<const float4 *>(dd + i);
+            const float4 b = lds_f4(dd + 4u * i);
             f[i] = b.x;
             f[i + 1] = b.y;
             f[i + 2] = b.z;
@@ -166,7 +167,8 @@ __device__ __forceinline__ void gate_factors(float *gs, int t, int lane, int L, 
   }
   if (t == 31) gs[G_EGAM + 2] = Gt;
   named_bar(bar, 64);
-  if (t >= 32) Gt += gs[G_EGAM + 2];
+  const uint32_t ga = smem_u32(gs);
+  if (t >= 32) Gt += lds_f1(ga + 4u * (G_EGAM + 2));
   gs[G_G + t] = Gt;
   gs[G_E + t] = __expf(gt);
   if (t == L - 1) {
@@ -174,26 +176,35 @@ __device__ __forceinline__ void gate_factors(float *gs, int t, int lane, int L, 
     gs[G_EGAM + 1] = Gt;
   }
   named_bar(bar, 64);
-  const float Gam = gs[G_EGAM + 1];
+  const float Gam = lds_f1(ga + 4u * (G_EGAM + 1));
   egr = t < L ? __expf(Gam - Gt) : 0.f;
   eg = t < L ? scale * __expf(Gt) : 0.f;
   gs[G_EG + t] = eg;
   gs[G_EGR + t] = egr;
-  gs[G_B + t] = __expf(gs[G_G + (t | 15)] - Gt);
+  gs[G_B + t] = __expf(lds_f1(ga + 4u * (G_G + (t | 15))) - Gt);
   {  // row factors of row t (blocks before t's own)
     float av[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) av[b] = (b < blk && t < L) ? scale * __expf(Gt - gs[G_G + 16 * b + 15]) : 0.f;
+    for (int b = 0; b < 4; ++b) av[b] = (b < blk && t < L) ? scale * __expf(Gt - lds_f1(ga + 4u * (G_G + 16 * b + 15))) : 0.f;
     *reinterpret_cast<float4 *>(gs + G_A + 4 * t) = make_float4(av[0], av[1], av[2], av[3]);
   }
   {  // row t of its diagonal block: scale exp(G_t - G_c) = scale prod_{c < i <= t} exp(g_i)
-    const float *e = gs + G_E + 16 * blk;
+    const uint32_t e = ga + 4u * (G_E + 16 * blk);
+    float ev[16];
+#pragma unroll
+    for (int c = 0; c < 16; c += 4) {
+      const float4 x = lds_f4(e + 4u * c);
+      ev[c] = x.x;
+      ev[c + 1] = x.y;
+      ev[c + 2] = x.z;
+      ev[c + 3] = x.w;
+    }
     float dv[16];
     float run = scale;
 #pragma unroll
     for (int c = 15; c >= 0; --c) {
       dv[c] = (c <= r && t < L) ? run : 0.f;
-      if (c <= r && c > 0) run *= e[c];
+      if (c <= r && c > 0) run *= ev[c];
     }
     float *dd = gs + G_DD + t * 20;
 #pragma unroll

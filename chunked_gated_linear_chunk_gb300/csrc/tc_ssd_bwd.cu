@@ -116,7 +116,7 @@ __device__ __forceinline__ float reduce_warp_rows(uint32_t t_acc, uint32_t lane_
     const int c0 = 32 * r + (second ? 16 : 0);
 #pragma unroll
     for (int i = 0; i < 16; i += 8) {
-      const uint4 xv = *reinterpret_cast<const uint4 *>(xt + sw128_off(row, c0 + i, 64));
+      const uint4 xv = lds_u4(smem_u32(xt) + sw128_off(row, c0 + i, 64));
       dot += __uint_as_float(xv.x << 16) * y[i] + __uint_as_float(xv.x & 0xffff0000u) * y[i + 1] +
              __uint_as_float(xv.y << 16) * y[i + 2] + __uint_as_float(xv.y & 0xffff0000u) * y[i + 3] +
              __uint_as_float(xv.z << 16) * y[i + 4] + __uint_as_float(xv.z & 0xffff0000u) * y[i + 5] +
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_a_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      const float eGam = slot_of(j)[G_EGAM];
+      const float eGam = lds_f1(smem_u32(slot_of(j)) + 4u * G_EGAM);
 #pragma unroll
       for (int cp = 0; cp < 64; cp += 32) {
         uint32_t r[32];
@@ -424,10 +424,10 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_a_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 64; c += 8) {
           const uint32_t off = sw128_off(tid, c, 64);
-          const uint4 x = *reinterpret_cast<const uint4 *>(vs + off);
+          const uint4 x = lds_u4(smem_u32(vs) + off);
           st_shared_v4(smem_u32(vd + off), scale_bf16x2(x.x, egr), scale_bf16x2(x.y, egr), scale_bf16x2(x.z, egr),
                        scale_bf16x2(x.w, egr));
-          const uint4 y = *reinterpret_cast<const uint4 *>(ds + off);
+          const uint4 y = lds_u4(smem_u32(ds) + off);
           st_shared_v4(smem_u32(dd + off), scale_bf16x2(y.x, eg), scale_bf16x2(y.y, eg), scale_bf16x2(y.z, eg),
                        scale_bf16x2(y.w, eg));
         }
@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      const float eGam = slot_of(i)[G_EGAM];
+      const float eGam = lds_f1(smem_u32(slot_of(i)) + 4u * G_EGAM);
 #pragma unroll
       for (int cp = 0; cp < 64; cp += 32) {
         uint32_t r[32];
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
       {
         const int rl = lane & 15, row = qw * 16 + rl, L = chunk_len(i);
         const bool second = lane >= 16;
-        const float egr = slot_of(i)[G_EGR + row];
+        const float egr = lds_f1(smem_u32(slot_of(i)) + 4u * (G_EGR + row));
         __nv_bfloat16 *vrow = a.dv + ((chunk_tok(i) + row) * H + h) * VD;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -787,10 +787,10 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 64; c += 8) {
           const uint32_t off = sw128_off(tid, c, 64);
-          const uint4 x = *reinterpret_cast<const uint4 *>(vs + off);
+          const uint4 x = lds_u4(smem_u32(vs) + off);
           st_shared_v4(smem_u32(vd + off), scale_bf16x2(x.x, egr), scale_bf16x2(x.y, egr), scale_bf16x2(x.z, egr),
                        scale_bf16x2(x.w, egr));
-          const uint4 y = *reinterpret_cast<const uint4 *>(ds + off);
+          const uint4 y = lds_u4(smem_u32(ds) + off);
           st_shared_v4(smem_u32(dd + off), scale_bf16x2(y.x, eg), scale_bf16x2(y.y, eg), scale_bf16x2(y.z, eg),
                        scale_bf16x2(y.w, eg));
         }

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
         break;
       }
       tc_fence_after();
-      const float eGam = slot_of(j)[G_EGAM];
+      const float eGam = lds_f1(smem_u32(slot_of(j)) + 4u * G_EGAM);
 #pragma unroll
       for (int cp = 0; cp < 64; cp += 32) {
         uint32_t r[32];
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
           !mbar_wait(&gready[jj % NG], (jj / NG) & 1, WAIT_CYCLES))
         return false;
       tc_fence_after();
-      const float eg = slot_of(jj)[G_EG + row];
+      const float eg = lds_f1(smem_u32(slot_of(jj)) + 4u * (G_EG + row));
       const int L = chunk_len(jj);
       __nv_bfloat16 *orow = a.o + ((chunk_tok(jj) + row) * H + h) * VD;
 #pragma unroll
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < 64; c += 8) {
           const uint32_t off = sw128_off(t, c, 64);
-          const uint4 x = *reinterpret_cast<const uint4 *>(src + off);
+          const uint4 x = lds_u4(smem_u32(src) + off);
           st_shared_v4(smem_u32(dst + off), scale_bf16x2(x.x, egr), scale_bf16x2(x.y, egr), scale_bf16x2(x.z, egr),
                        scale_bf16x2(x.w, egr));
         }

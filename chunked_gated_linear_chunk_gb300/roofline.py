@@ -89,12 +89,12 @@ def kernel_bytes(s: Shape, label: str) -> int:
     """Algorithmic bytes of one launch of the named kernel: the inputs it
     must read and the outputs it must write (each once)."""
     ins5 = 2 * s.qk_bytes() + 2 * s.v_bytes() + s.gate_bytes()
-    if label in ("gla_fwd_kernel", "simt_fwd"):
+    if label in ("gla_fwd_kernel", "simt_fwd", "ssd_fwd_kernel"):
         return fwd_bytes(s)
-    if label == "gla_bwd_dq_kernel":  # reads q, k, v, g, do (+h0, dht); writes dq
+    if label in ("gla_bwd_dq_kernel", "ssd_bwd_a_kernel"):  # reads q, k, v, g, do (+h0, dht); writes dq
         return ins5 + s.qk_bytes() + (s.state_bytes() if s.initial_state else 0) + (
             s.state_bytes() if s.dht else 0)
-    if label == "gla_bwd_rev_kernel":  # reads q, k, v, g, do (+dht); writes dk, dv, dg (+dh0)
+    if label in ("gla_bwd_rev_kernel", "ssd_bwd_b_kernel"):  # reads q, k, v, g, do (+dht); writes dk, dv, dg (+dh0)
         return ins5 + s.qk_bytes() + s.v_bytes() + s.gate_bytes() + (
             s.state_bytes() if s.dht else 0) + (s.state_bytes() if s.initial_state else 0)
     if label == "simt_state_pass":  # reads k, v, g (+h0)
