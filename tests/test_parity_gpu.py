@@ -87,10 +87,19 @@ SMALL = {
     "gla_bf16_pieces_T1000_nostate": lambda: case(2, 14, B=1, T=1000, H=1, Hqk=1),
     "gla_bf16_pieces_packed": lambda: case(4, 15, B=1, T=3000, H=1, Hqk=1, doc_mean=700),
     "gla_bf16_pieces_B2_H2": lambda: case(5, 16, B=2, T=1500, H=2, Hqk=2),
-    # SSD split into pieces (the piece passes in their grouped-head and
-    # per-head-gate modes), two heads on one B / C group
-    "ssd_bf16_pieces_T2000": lambda: case(3, 17, B=1, T=2000, H=2),
-    # SSD with V = 128 (both value halves stored) and two B / C groups
+    # SSD (V = 64: its own kernels, one CTA per document and head): a long
+    # document on two heads of one B / C group
+    "ssd_bf16_T2000": lambda: case(3, 17, B=1, T=2000, H=2),
+    # every head its own B / C, both states
+    "ssd_bf16_own_bc_h0_dht": lambda: case(3, 20, B=2, T=130, H=4, Hqk=4, initial_state=True,
+                                           final_state=True),
+    # two B / C groups of two heads, a length past a chunk boundary
+    "ssd_bf16_groups2_T257": lambda: case(3, 21, B=1, T=257, H=4, Hqk=2, final_state=True),
+    # many short packed documents (most shorter than one 16-token block)
+    "ssd_bf16_short_docs": lambda: case(3, 22, B=2, T=200, H=2, packed=True, doc_mean=10, initial_state=True,
+                                        final_state=True),
+    # SSD with V = 128 (the GLA tensor-core kernels in their per-head-gate
+    # mode, both value halves stored) and two B / C groups
     "ssd_bf16_V128_groups2": lambda: case(3, 18, B=1, T=200, H=4, Hqk=2, V=128),
     # SSD with V < 64: the fp32 CUDA-core kernels
     "ssd_bf16_V32": lambda: case(3, 19, B=1, T=130, H=2, V=32),
