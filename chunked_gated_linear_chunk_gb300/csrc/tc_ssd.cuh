@@ -135,6 +135,73 @@ __device__ __forceinline__ void decay_mask(uint32_t t_acc, uint32_t lane_off, in
   }
 }
 
+// decay_mask<false> in two steps, so that the tile can be computed while
+// the products that read the previous tile are still running: the packed
+// bf16 words of the lane's two 16-column blocks (2 k, plus 1 for lanes
+// 16..31, k = 0, 1; valid where the block is at or below the diagonal) ...
+__device__ __forceinline__ void decay_tile_regs(uint32_t t_acc, uint32_t lane_off, int qw, int lane, const float *gs,
+                                                uint32_t (&w)[2][8]) {
+  using namespace gsl;
+  const int rl = lane & 15, row = qw * 16 + rl;
+  const bool second = lane >= 16;
+  const uint32_t ga = smem_u32(gs);
+  const float4 arow = lds_f4(ga + 4u * (G_A + 4 * row));
+#pragma unroll
+  for (int cp = 0; cp < 4; cp += 2) {
+    if (cp <= qw) {
+      uint32_t r0[16], r1[16];
+      tmem_ld16(t_acc + lane_off + cp * 16, r0);
+      tmem_ld16(t_acc + lane_off + cp * 16 + 16, r1);
+      tmem_ld_wait(r0);
+      tmem_tie(r1);
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t sh = __shfl_sync(0xffffffffu, r1[i], rl);
+        v[i] = __uint_as_float(second ? sh : r0[i]);
+      }
+      const int cb = cp + (second ? 1 : 0);
+      float f[16];
+      if (cb < qw) {
+        const float a = cb == 0 ? arow.x : (cb == 1 ? arow.y : arow.z);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 b = lds_f4(ga + 4u * (G_B + cb * 16 + i));
+          f[i] = a * b.x;
+          f[i + 1] = a * b.y;
+          f[i + 2] = a * b.z;
+          f[i + 3] = a * b.w;
+        }
+      } else {
+        const uint32_t dd = ga + 4u * (G_DD + (qw * 16 + rl) * 20);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 b = lds_f4(dd + 4u * i);
+          f[i] = b.x;
+          f[i + 1] = b.y;
+          f[i + 2] = b.z;
+          f[i + 3] = b.w;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[cp / 2][e] = pack_bf16(v[2 * e] * f[2 * e], v[2 * e + 1] * f[2 * e + 1]);
+    }
+  }
+}
+// ... and their store into the tile.
+__device__ __forceinline__ void decay_tile_store(uint8_t *tile, int qw, int lane, const uint32_t (&w)[2][8]) {
+  const int rl = lane & 15, row = qw * 16 + rl;
+  const int sb = lane >= 16 ? 1 : 0;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int cb = 2 * k + sb;
+    if (2 * k <= qw && cb <= qw) {
+      st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16, 64)), w[k][0], w[k][1], w[k][2], w[k][3]);
+      st_shared_v4(smem_u32(tile + sw128_off(row, cb * 16 + 8, 64)), w[k][4], w[k][5], w[k][6], w[k][7]);
+    }
+  }
+}
+
 // Row c (channel) of the bf16 state tile (128 rows x 64 columns, 128-byte
 // swizzle): the B operand of q S, MN-major.
 __device__ __forceinline__ void store_state_row(uint8_t *St, int c, const float (&S)[64]) {

@@ -451,7 +451,8 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_a_kernel(const __grid_constant
 // pass B: chunks in reverse (iteration i takes chunk nch - 1 - i)
 //   warp 0       TMA (q, k, v, do; 2 stages)
 //   warp 1       MMA: QK = q k^T, dP = do v^T, W = q^T dot,
-//                dV1 = A^T do, dV2 = k dS, dK = dA^T q + vt dS^T
+//                dV1 = A^T do, dV2 = k dS, dK = dA^T q + vt dS^T (QK / dP
+//                of the next chunk go before dV / dK of this one)
 //   warps 2..5   mask: A = QK (.) F, dA = dP (.) F (bf16)
 //   warps 6..9   state: dS (fp32 in registers), bf16 copy, dh0 at the end;
 //                then dv of the chunk
@@ -554,18 +555,32 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
       constexpr uint32_t idV2 = idesc_bf16(64, 64, false, true);    // k dS
       constexpr uint32_t idK1 = idesc_bf16(64, 128, true, true);    // dA^T q
       constexpr uint32_t idK2 = idesc_bf16(64, 128, false, false);  // vt dS^T
-      for (int i = 0; i < nch && !*abortp; ++i) {
-        const int s = i % NS, b = i & 1;
-        const uint32_t qa = sbase + Q + s * 16384, ka = sbase + K + s * 16384, va = sbase + V + s * 8192,
-                       da = sbase + DO + s * 8192;
-        // QK, dP: their TMEM was read by the mask step of i - 1 (p_ready below)
-        if (!mbar_wait(&full[s], (i / NS) & 1, WAIT_CYCLES)) SSD_FAIL
-        tc_fence_after();
+      // QK, dP of a chunk (their TMEM was read by the mask step of the chunk before)
+      auto issue_qkdp = [&](int ii) {
+        const int si = ii % NS;
+        const uint32_t qa = sbase + Q + si * 16384, ka = sbase + K + si * 16384, va = sbase + V + si * 8192,
+                       da = sbase + DO + si * 8192;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tQK, kdesc(qa, ks, 64), kdesc(ka, ks, 64), idKK, ks);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) mma_bf16(tDP, kdesc(da, ks, 64), kdesc(va, ks, 64), idKK, ks);
         mma_commit(&pd_full);
+      };
+      if (nch > 0) {
+        const bool ok0 = mbar_wait(&full[0], 0, WAIT_CYCLES);
+        tc_fence_after();
+        if (ok0)
+          issue_qkdp(0);
+        else
+          atomicExch(&abort_flag, 1);
+      }
+      // Order per chunk i: W(i); then, once the mask step of i has read QK /
+      // dP, QK / dP of i + 1 if its tiles have landed (so that the next mask
+      // step overlaps dV / dK of i), dV / dK of i, and QK / dP of i + 1 if
+      // they were not issued before.
+      for (int i = 0; i < nch && !*abortp; ++i) {
+        const int s = i % NS, b = i & 1;
+        const uint32_t qa = sbase + Q + s * 16384, ka = sbase + K + s * 16384, da = sbase + DO + s * 8192;
         // W = q^T dot; the state step of i - 1 has read W (it wrote dS_i after)
         if (!mbar_wait(&gready[i % NG], (i / NG) & 1, WAIT_CYCLES) ||
             !mbar_wait(&ds_ready[b], (i >> 1) & 1, WAIT_CYCLES))
@@ -577,10 +592,18 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
           for (int ks = 0; ks < 4; ++ks) mma_bf16(tW, mdesc(qa, ks, 8192), mdesc(dot, ks, 8192), idW, ks);
           mma_commit(&w_full);
         }
-        // dV, dK: A and dA masked; their TMEM read out by the output step of i - 1
+        // A and dA masked (QK / dP read); dV / dK TMEM read out by the steps of i - 1
         if (!mbar_wait(&p_ready, i & 1, WAIT_CYCLES) || (i >= 1 && !mbar_wait(&tm_free, (i - 1) & 1, WAIT_CYCLES)))
           SSD_FAIL
         tc_fence_after();
+        // QK / dP of i + 1 first if its tiles are in (never wait for them here:
+        // their stage is released by the output step of i - 1)
+        bool next_done = i + 1 >= nch;
+        if (!next_done && mbar_test_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1)) {
+          tc_fence_after();
+          issue_qkdp(i + 1);
+          next_done = true;
+        }
         {
           const uint32_t Aa = sbase + A, dfa = sbase + DAF, dsa = sbase + DS + b * 16384, vt = sbase + VT + b * 8192;
 #pragma unroll
@@ -595,6 +618,11 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
           mma_commit(&dk_full);
           mma_commit(&empty[s]);
         }
+        if (!next_done) {
+          if (!mbar_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1, WAIT_CYCLES)) SSD_FAIL
+          tc_fence_after();
+          issue_qkdp(i + 1);
+        }
       }
       mma_commit(&drain);
       if (!mbar_wait(&drain, 0, WAIT_CYCLES)) atomicExch(&abort_flag, 1);
@@ -607,14 +635,21 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
     mask_tile_init(sm + DAF, qw, lane);
     bool ok = true;
     for (int i = 0; i < nch && !*abortp; ++i) {
-      // A and dA were read by dV / dK of i - 1, which completed before QK(i)
       if (!mbar_wait(&pd_full, i & 1, WAIT_CYCLES) || !mbar_wait(&gready[i % NG], (i / NG) & 1, WAIT_CYCLES)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      decay_mask<false>(tQK, lane_off, qw, lane, sm + A, nullptr, slot_of(i));
-      decay_mask<false>(tDP, lane_off, qw, lane, sm + DAF, nullptr, slot_of(i));
+      uint32_t wa[2][8], wd[2][8];
+      decay_tile_regs(tQK, lane_off, qw, lane, slot_of(i), wa);
+      decay_tile_regs(tDP, lane_off, qw, lane, slot_of(i), wd);
+      // A and dA tiles: read by dV / dK of i - 1, which may still be running
+      if (i >= 1 && (!mbar_wait(&dv_full, (i - 1) & 1, WAIT_CYCLES) || !mbar_wait(&dk_full, (i - 1) & 1, WAIT_CYCLES))) {
+        ok = false;
+        break;
+      }
+      decay_tile_store(sm + A, qw, lane, wa);
+      decay_tile_store(sm + DAF, qw, lane, wd);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_ready);
