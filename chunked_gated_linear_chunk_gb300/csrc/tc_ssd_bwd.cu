@@ -84,6 +84,71 @@ constexpr uint32_t GS = 196608;
 constexpr uint32_t BYTES = GS + gsl::NG * gsl::GSLOT;
 }  // namespace pbs
 
+// One warp's 16 rows (16 qw .. 16 qw + 15) of an M = 64 accumulator with
+// 128 columns, read out of TMEM whole: y[r][i] is column 32 r + i of row
+// 16 qw + (lane & 15) for lanes 0..15, column 32 r + 16 + i for lanes 16..31.
+__device__ __forceinline__ void tmem_rows128(uint32_t t_acc, uint32_t lane_off, int lane, float (&y)[4][16]) {
+  const int rl = lane & 15;
+  const bool second = lane >= 16;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    uint32_t a0[16], a1[16];
+    tmem_ld16(t_acc + lane_off + 32 * r, a0);
+    tmem_ld16(t_acc + lane_off + 32 * r + 16, a1);
+    tmem_ld_wait(a0);
+    tmem_tie(a1);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t sh = __shfl_sync(0xffffffffu, a1[i], rl);
+      y[r][i] = __uint_as_float(second ? sh : a0[i]);
+    }
+  }
+}
+
+// Adds those rows (y, as tmem_rows128 leaves them) of this CTA's 64 x 128
+// fp32 tile of a per-head gradient into the group accumulator (map m: boxes
+// of 32 channels x 16 rows; rows tok0 + 16 qw .., head group hq), by TMA
+// reduce-add at L2, in four rounds of 32 channels through the warp's two
+// 2 KB staging buffers (stg, used in turn: a buffer is rewritten once the
+// reduce issued from it two rounds earlier has read it).  Rows at or past L
+// are added as zeros.  Returns this lane's share of sum_c x[row, c] y[row, c],
+// x the bf16 tile (q or k of the chunk: two 64-column blocks, 128-byte
+// swizzle).
+__device__ __forceinline__ float reduce_rows(const float (&y)[4][16], int qw, int lane, int L, uint8_t *stg,
+                                             const uint8_t *xt, const CUtensorMap *m, int hq, int tok0) {
+  const int rl = lane & 15, row = qw * 16 + rl;
+  const bool second = lane >= 16, live = row < L;
+  float dot = 0.f;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c0 = 32 * r + (second ? 16 : 0);
+#pragma unroll
+    for (int i = 0; i < 16; i += 8) {
+      const uint4 xv = lds_u4(smem_u32(xt) + sw128_off(row, c0 + i, 64));
+      dot += __uint_as_float(xv.x << 16) * y[r][i] + __uint_as_float(xv.x & 0xffff0000u) * y[r][i + 1] +
+             __uint_as_float(xv.y << 16) * y[r][i + 2] + __uint_as_float(xv.y & 0xffff0000u) * y[r][i + 3] +
+             __uint_as_float(xv.z << 16) * y[r][i + 4] + __uint_as_float(xv.z & 0xffff0000u) * y[r][i + 5] +
+             __uint_as_float(xv.w << 16) * y[r][i + 6] + __uint_as_float(xv.w & 0xffff0000u) * y[r][i + 7];
+    }
+    uint8_t *buf = stg + (r & 1) * 2048;
+    if (lane == 0) bulk_wait_read_all_but_one();  // the reduce from this buffer, two rounds back
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const uint32_t off = sw128_off_f32(rl, (second ? 16 : 0) + i, 16);
+      st_shared_v4(smem_u32(buf + off), __float_as_uint(live ? y[r][i] : 0.f), __float_as_uint(live ? y[r][i + 1] : 0.f),
+                   __float_as_uint(live ? y[r][i + 2] : 0.f), __float_as_uint(live ? y[r][i + 3] : 0.f));
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_reduce_add_3d(m, buf, 32 * r, hq, tok0 + 16 * qw);
+      bulk_commit();
+    }
+  }
+  return dot;
+}
+
 // Adds one warp's 16 rows (16 qw .. 16 qw + 15) of this CTA's 64 x 128
 // fp32 tile of a per-head gradient (M = 64 accumulator t_acc, 128 columns)
 // into the group accumulator (map m: boxes of 32 channels x 16 rows; rows
@@ -757,18 +822,23 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
       // the 128 threads leave together (named barriers below)
       if (named_bar_any(3, 128, !ok || *abortp)) break;
       const int s = i % NS;
-      if (!mbar_wait(&dk_full, i & 1, WAIT_CYCLES)) ok = false;
-      tc_fence_after();
       const int L = chunk_len(i);
       const int64_t tok0 = chunk_tok(i);
-      float kdk = reduce_warp_rows(tDK, lane_off, qw, lane, L, sm + DKT + qw * 4096, sm + K + s * 16384, &maps.dka,
-                                   hq, (int)tok0);
+      // q . dq_h of the row (pass A's result), loaded while dk_h is computed
+      const float qdq = row < L ? ldg_early(a.qdq + (tok0 + row) * H + h) : 0.f;
+      if (!mbar_wait(&dk_full, i & 1, WAIT_CYCLES)) ok = false;
+      tc_fence_after();
+      // dk_h leaves TMEM first, so that the next chunk's products need not
+      // wait for the reduce
+      float y[4][16];
+      tmem_rows128(tDK, lane_off, lane, y);
       tc_fence_before();
       mbar_arrive(&tm_free);
+      float kdk = reduce_rows(y, qw, lane, L, sm + DKT + qw * 4096, sm + K + s * 16384, &maps.dka, hq, (int)tok0);
       mbar_arrive(&empty[s]);
       // dg: reverse sum over the chunk of q . dq_h - k . dk_h, plus the carry
       kdk += __shfl_xor_sync(0xffffffffu, kdk, 16);
-      float x = (row < L) ? a.qdq[(tok0 + row) * H + h] - kdk : 0.f;
+      float x = (row < L) ? qdq - kdk : 0.f;
       // suffix sum over the warp's 16 rows (lanes 0..15; lanes 16..31 mirror them)
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) {

@@ -11,10 +11,11 @@
 //                tiles
 //   warps 6..9   state warpgroup: S (fp32 in registers, thread c holds
 //                channel row c), bf16 copy of S for the next readout
-//   warps 10..13 output warpgroup: o = scale exp(G_t) (q S)_t + (P v)_t
+//   warps 10..13 output warpgroup: o = scale exp(G_t) (q S)_t + (P v)_t,
+//                and two chunks ahead v scaled by exp(Gam - G_s)
 //   warps 14, 15 gate warps: up to two chunks ahead, the prefix sums G and
 //                every decay factor of the chunk (one slot of a 3-slot
-//                ring) and v scaled by exp(Gam - G_s)
+//                ring)
 // TMEM (512 columns): QK[2] at 0/64, U[2] at 128/192, QS[2] at 256/320,
 // PV[2] at 384/448 (M = 64 tiles: row r in lane 32 (r / 16) + r % 16).
 #include "tc_ssd.cuh"
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[NS], empty[NS], gready[NG], gfree[NG], qk_full[2], u_full[2], qs_full[2], pv_full[2],
-      p_ready[2], s_ready[2], o_free[2], drain;
+      p_ready[2], s_ready[2], o_free[2], vt_ready[2], drain;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
       mbar_init(&p_ready[i], 128);
       mbar_init(&s_ready[i], 128);
       mbar_init(&o_free[i], 128);
+      mbar_init(&vt_ready[i], 128);
     }
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -134,6 +136,16 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
         tma_load_3d(sm + K + s * 16384, &maps.k, 0, hq, tok, &full[s]);
         tma_load_3d(sm + K + s * 16384 + 8192, &maps.k, 64, hq, tok, &full[s]);
         tma_load_3d(sm + V + s * 8192, &maps.v, 0, h, tok, &full[s]);
+        // the tiles of chunk j + 2 into L2: their load is issued about two
+        // chunk periods from now, once a stage frees up
+        if (j + 2 < nch) {
+          const int tp = (int)chunk_tok(j + 2);
+          tma_prefetch_l2_3d(&maps.q, 0, hq, tp);
+          tma_prefetch_l2_3d(&maps.q, 64, hq, tp);
+          tma_prefetch_l2_3d(&maps.k, 0, hq, tp);
+          tma_prefetch_l2_3d(&maps.k, 64, hq, tp);
+          tma_prefetch_l2_3d(&maps.v, 0, h, tp);
+        }
         issued = j + 1;
       }
       // every load issued has landed before the CTA leaves
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
         bool ok = mbar_wait(&full[0], 0, WAIT_CYCLES);
         tc_fence_after();
         if (ok) issue_qk(0);
-        ok = ok && mbar_wait(&gready[0], 0, WAIT_CYCLES);
+        ok = ok && mbar_wait(&vt_ready[0], 0, WAIT_CYCLES);
         tc_fence_after();
         if (ok) issue_u(0);
         if (!ok) atomicExch(&abort_flag, 1);
@@ -202,8 +214,8 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
           mma_commit(&empty[s]);
         }
         if (j + 1 < nch) {
-          // U's buffer (j + 1) & 1 was read by the state step of j - 1 (s_ready above)
-          if (!mbar_wait(&gready[(j + 1) % NG], ((j + 1) / NG) & 1, WAIT_CYCLES)) SSD_FAIL
+          // U's buffer (j + 1) & 1 was read by the state step of j - 1 (s_ready above); vt of j + 1 written
+          if (!mbar_wait(&vt_ready[(j + 1) & 1], ((j + 1) >> 1) & 1, WAIT_CYCLES)) SSD_FAIL
           tc_fence_after();
           issue_u(j + 1);
         }
@@ -331,10 +343,33 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
       mbar_arrive(&o_free[bb]);
       return true;
     };
+    // vt = v (.) exp(Gam - G_s) of chunk jj: thread row t, 32 of its 64 columns
+    auto make_vt = [&](int jj) -> bool {
+      const int bb = jj & 1, s = jj % NS;
+      // the gate step of jj, v of jj, and vt's buffer (read by U(jj - 2))
+      if (!mbar_wait(&gready[jj % NG], (jj / NG) & 1, WAIT_CYCLES) || !mbar_wait(&full[s], (jj / NS) & 1, WAIT_CYCLES) ||
+          (jj >= 2 && !mbar_wait(&u_full[bb], ((jj - 2) >> 1) & 1, WAIT_CYCLES)))
+        return false;
+      const int tid = (int)threadIdx.x - 320, t = tid >> 1, cb = (tid & 1) * 32;
+      const float egr = lds_f1(smem_u32(slot_of(jj)) + 4u * (G_EGR + t));
+      const uint32_t src = smem_u32(sm + V + s * 8192), dst = smem_u32(sm + VT + bb * 8192);
+#pragma unroll
+      for (int c = cb; c < cb + 32; c += 8) {
+        const uint32_t off = sw128_off(t, c, 64);
+        const uint4 x = lds_u4(src + off);
+        st_shared_v4(dst + off, scale_bf16x2(x.x, egr), scale_bf16x2(x.y, egr), scale_bf16x2(x.z, egr),
+                     scale_bf16x2(x.w, egr));
+      }
+      fence_async_smem();
+      mbar_arrive(&vt_ready[bb]);
+      return true;
+    };
     bool ok = true;
+    for (int jj = 0; ok && jj < 2 && jj < nch; ++jj) ok = make_vt(jj);
     for (int j = 0; ok && j < nch && !*abortp; ++j) {
       ok = output(j);
       mbar_arrive(&gfree[j % NG]);
+      if (ok && j + 2 < nch) ok = make_vt(j + 2);
     }
     if (!ok) atomicExch(&abort_flag, 1);
   } else {
@@ -347,36 +382,22 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
       return ldg_early(a.g + (chunk_tok(jj) + tid) * H + h);
     };
     float gnext = load_g(0), gnext2 = load_g(1);
-    // the gate slot and vt of chunk jj
+    // the gate slot of chunk jj
     auto prep = [&](int jj) -> bool {
-      const int gsl = jj % NG, bb = jj & 1, s = jj % NS, L = chunk_len(jj);
+      const int gsl = jj % NG, L = chunk_len(jj);
       float *gs = slot_of(jj);
-      // the slot was last read by the mask, state and output steps of
-      // jj - NG; vt's buffer by U(jj - 2)
+      // the slot was last read by the mask, state and output steps of jj - NG
       bool good = true;
       if (jj >= NG && !mbar_wait(&gfree[gsl], ((jj / NG) - 1) & 1, WAIT_CYCLES)) good = false;
-      if (jj >= 2 && !mbar_wait(&u_full[bb], ((jj - 2) >> 1) & 1, WAIT_CYCLES)) good = false;
       const int t = tid;
       const float gt = gnext;
       gnext = gnext2;
       gnext2 = load_g(jj + 2);
       float egr, eg;
       gate_factors(gs, t, lane, L, a.scale, gt, 2, egr, eg);
+      (void)egr;
       (void)eg;
-      // vt = v (.) exp(Gam - G_s): row t
-      if (!good || !mbar_wait(&full[s], (jj / NS) & 1, WAIT_CYCLES)) return false;
-      {
-        const uint8_t *src = sm + V + s * 8192;
-        uint8_t *dst = sm + VT + bb * 8192;
-#pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-          const uint32_t off = sw128_off(t, c, 64);
-          const uint4 x = lds_u4(smem_u32(src) + off);
-          st_shared_v4(smem_u32(dst + off), scale_bf16x2(x.x, egr), scale_bf16x2(x.y, egr), scale_bf16x2(x.z, egr),
-                       scale_bf16x2(x.w, egr));
-        }
-      }
-      fence_async_smem();
+      if (!good) return false;
       mbar_arrive(&gready[gsl]);
       return true;
     };
