@@ -152,8 +152,7 @@ constexpr uint32_t DP = 131072;    // 8 KB masked dP (bf16 [t][s])
 constexpr uint32_t GT = 139264;    // 2 x 32 KB gate tiles g [t][c] (fp32, TMA box 32 x 64)
 constexpr uint32_t QT = 204800;    // 16 KB qt = scale q exp(G) (bf16, store source for pass B)
 constexpr uint32_t XCH = 221184;   // 2 x 2 x 128 fp32 gate products
-constexpr uint32_t XQ = 223232;    // 2 x 128 fp32: token-half totals of q (.) dq
-constexpr uint32_t BYTES = 224256;
+constexpr uint32_t BYTES = 223232;
 }  // namespace asm_
 
 // Thread roles: warp 0 lane 0 TMA loads of k, v, do; lane 1 TMA loads of
@@ -162,13 +161,14 @@ constexpr uint32_t BYTES = 224256;
 // threads instead); lane 4 TMA stores of kt.  Pass B takes the gated
 // operands qt, kt from here instead of gating q and k again.  Warp 1
 // MMA + TMEM.  Warps 2..9 per-channel warps (key channel c = lane of the
-// warp's TMEM quarter, token half th): gate work and kt for chunk j, then
-// the dq / q (.) dq epilogue of chunk j-1 for their half, written to shared
-// memory for the TMA stores.  Warps 10..13 mask dP and scale the state.
+// warp's TMEM quarter, token half th): gate work and kt of each chunk.
+// Warps 10..13 mask dP and scale the state.  Warps 14..17 the dq / q (.) dq
+// epilogue (key channel c, all tokens of the chunk), written to shared
+// memory for the TMA stores, so that it overlaps the next chunk's gate work.
 // HG: one gate per head (g is [BT, H]); the per-channel instance has none of
 // its branches.
 template <bool HG>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(576, 1)
     gla_bwd_dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -206,15 +206,15 @@ __global__ void __launch_bounds__(448, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&dq_full[i], 1);
-      mbar_init(&dq_free[i], 256);
+      mbar_init(&dq_free[i], 128);   // epilogue warps
       mbar_init(&eg_ready[i], 256);
-      mbar_init(&eg_free[i], 128);
+      mbar_init(&eg_free[i], 256);   // state and epilogue warps
     }
     mbar_init(&dp_full, 1);
     mbar_init(&dp_ready, 128);
     mbar_init(&u_full, 1);
     mbar_init(&s_ready, 128);
-    mbar_init(&out_ready, 256);
+    mbar_init(&out_ready, 128);
     mbar_init(&stg_free, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&g_full[i], 1);
@@ -244,18 +244,6 @@ __global__ void __launch_bounds__(448, 1)
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
-        if (j + 2 < nch) {
-          const int tp = tok + 2 * C;
-          for (int x = 0; x < 128; x += 64) {
-            tma_prefetch_3d(&maps.k, x, hq, tp);
-            if (x < a.vd) {  // v and do have vd columns
-              tma_prefetch_3d(&maps.v, x, h, tp);
-              tma_prefetch_3d(&maps.dO, x, h, tp);
-            }
-          }
-          if (!HG)
-            for (int x = 0; x < 128; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
-        }
         mbar_expect_tx(&full[st], 3 * 16384);
         for (int x = 0; x < 2; ++x) {
           tma_load_3d(sm + asm_::K + st * 16384 + x * 8192, &maps.k, 64 * x, hq, tok, &full[st]);
@@ -271,10 +259,6 @@ __global__ void __launch_bounds__(448, 1)
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
-        if (j + 2 < nch) {
-          tma_prefetch_3d(&maps.q, 0, hq, tok + 2 * C);
-          tma_prefetch_3d(&maps.q, 64, hq, tok + 2 * C);
-        }
         mbar_expect_tx(&qfull[st], 16384);
         for (int x = 0; x < 2; ++x)
           tma_load_3d(sm + asm_::Q + st * 16384 + x * 8192, &maps.q, 64 * x, hq, tok, &qfull[st]);
@@ -379,7 +363,7 @@ __global__ void __launch_bounds__(448, 1)
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
     const int64_t gc0 = unit_chunk0(a.units, un);
-    uint32_t ph_full = 0, ph_free = 0, ph_dqf = 0;
+    uint32_t ph_full = 0, ph_free = 0;
     const ColF32 gcol(sbase + asm_::GT, 32 * th, c);  // buffer 0; buffer 1 is 32 KB on
     // one gate per head: thread (th = 0, c < 64) fetches token c's gate two
     // chunks ahead and stages it in the gate buffer of its chunk before the
@@ -395,9 +379,9 @@ __global__ void __launch_bounds__(448, 1)
       gnext = gate_of(1);
     }
     if (HG) named_bar(1, 256);
-    // iteration j: gate work and kt of chunk j, then the epilogue of chunk j-1
-    for (int j = 0; j <= nch; ++j) {
-      if (j < nch) {
+    // gate work and kt of chunk j
+    for (int j = 0; j < nch; ++j) {
+      {
         const int st = j % asm_::NS, b = j & 1;
         const int64_t tok0 = s0 + (int64_t)j * C;
         const int L = (int)min((int64_t)C, s1 - tok0);
@@ -485,79 +469,8 @@ __global__ void __launch_bounds__(448, 1)
         mbar_arrive(&prep_done[st]);
         mbar_arrive(&eg_ready[b]);
       }
-      if (j >= 1) {
-        // dq epilogue of chunk jj for this thread's half:
-        //   dq_t = scale exp(G_t) acc_t,  dgp_t = sum_{r >= t in chunk} q_r dq_r
-        // Full chunks go to shared memory (dq over the raw q it was computed
-        // from) for the TMA stores; a ragged last chunk is stored directly.
-        const int jj = j - 1, bb = jj & 1, stt = jj % asm_::NS;
-        const int64_t tok0 = s0 + (int64_t)jj * C;
-        const int L = (int)min((int64_t)C, s1 - tok0);
-        if (!mbar_wait(&dq_full[bb], (ph_dqf >> bb) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        ph_dqf ^= 1u << bb;
-        if (!mbar_wait(&qfull[stt], (jj / asm_::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        // the qt staging buffer is free once the previous chunk's stores have read it
-        if (jj >= 1 && !mbar_wait(&stg_free, (jj - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-        tc_fence_after();
-        const ColBf16 qc(sbase + asm_::Q + stt * 16384, 32 * th, c);
-        const ColBf16 qtc(sbase + asm_::QT, 32 * th, c);
-        float sv[32];
-        float suf = 0.f;
-#pragma unroll
-        for (int blk = 1; blk >= 0; --blk) {
-          const int tb = 32 * th + 16 * blk;  // first token of the block
-          uint32_t acc[16], eg[16];
-          tmem_ld16(tDQ + 64 * bb + lane_off + tb, acc);
-          tmem_ld16(tEG + 64 * bb + lane_off + tb, eg);
-          uint16_t qb[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) qb[i] = lds_u16(qc.at(16 * blk + i));
-          tmem_ld_wait(acc);
-          tmem_ld_wait(eg);
-          float dqv[16], qtv[16];
-#pragma unroll
-          for (int i = 15; i >= 0; --i) {
-            const float sg = a.scale * __uint_as_float(eg[i]);
-            const float qf = bf16_bits_to_f32(qb[i]);
-            dqv[i] = sg * __uint_as_float(acc[i]);
-            qtv[i] = sg * qf;  // qt = scale q exp(G), the gated q of pass B
-            if (tb + i < L) suf += qf * dqv[i];
-            sv[16 * blk + i] = suf;
-          }
-          if (L == C) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sts_u16(qc.at(16 * blk + i), f32_to_bf16_bits(dqv[i]));
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sts_u16(qtc.at(16 * blk + i), f32_to_bf16_bits(qtv[i]));
-          } else {
-            transpose_4x4_blocks(dqv, lane);
-            store_block_bf16(a.dq + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, dqv, lane, tb, L);
-            transpose_4x4_blocks(qtv, lane);
-            store_block_bf16(a.qt + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, qtv, lane, tb, L);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&dq_free[bb]);
-        // the low half adds the high half's total
-        float *xq = reinterpret_cast<float *>(sm + asm_::XQ) + bb * 128;
-        if (th == 1) xq[c] = suf;
-        named_bar(2, 256);
-        const float add = th == 0 ? xq[c] : 0.f;
-        {
-          // partials in the chunk-slot layout of the scratch: four tokens of
-          // one channel per 16 bytes, [token quad][channel], so each warp
-          // store covers 512 contiguous bytes (read back the same way by pass B)
-          float4 *dst = reinterpret_cast<float4 *>(a.dgp) + ((gc0 + jj) * H + h) * (int64_t)(KD * C / 4) + c;
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[(8 * th + i) * KD] =
-                make_float4(sv[4 * i] + add, sv[4 * i + 1] + add, sv[4 * i + 2] + add, sv[4 * i + 3] + add);
-        }
-        fence_async_smem();
-        mbar_arrive(&out_ready);
-      }
     }
-  } else {
+  } else if (warp < 14) {
     // ---------------- state warpgroup: thread = key channel c ----------------
     const int qw = warp & 3;
     const int c = 32 * qw + lane;
@@ -611,20 +524,14 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_before();
         mbar_arrive(&eg_free[b]);
         bool waited = false;
-#pragma unroll
-        for (int cb = 0; cb < 4; cb += 2) {
-          uint32_t r[32], r2[32];
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t r[32];
           tmem_ld32(tS + lane_off + 32 * cb, r);
-          tmem_ld32(tS + lane_off + 32 * cb + 32, r2);
           tmem_ld_wait32(r);
-          tmem_ld_wait32(r2);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            r[i] = __float_as_uint(eGam * __uint_as_float(r[i]));
-            r2[i] = __float_as_uint(eGam * __uint_as_float(r2[i]));
-          }
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(eGam * __uint_as_float(r[i]));
           tmem_st32(tS + lane_off + 32 * cb, r);
-          tmem_st32(tS + lane_off + 32 * cb + 32, r2);
           if (!waited) {
             if (!mbar_wait(&dq_full[b], (ph_dqf >> b) & 1, WAIT_CYCLES)) {
               atomicExch(&abort_flag, 1);
@@ -633,14 +540,10 @@ __global__ void __launch_bounds__(448, 1)
             ph_dqf ^= 1u << b;
             waited = true;
           }
-          uint32_t pk[16], pk2[16];
+          uint32_t pk[16];
 #pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            pk[n] = pack_bf16(__uint_as_float(r[2 * n]), __uint_as_float(r[2 * n + 1]));
-            pk2[n] = pack_bf16(__uint_as_float(r2[2 * n]), __uint_as_float(r2[2 * n + 1]));
-          }
+          for (int n = 0; n < 16; ++n) pk[n] = pack_bf16(__uint_as_float(r[2 * n]), __uint_as_float(r[2 * n + 1]));
           tmem_st16(tSb + lane_off + 16 * cb, pk);
-          tmem_st16(tSb + lane_off + 16 * cb + 16, pk2);
         }
         if (*abortp) break;
         tmem_st_wait();
@@ -650,14 +553,14 @@ __global__ void __launch_bounds__(448, 1)
           // [value quad][channel] x 4 columns: each warp store covers 512
           // contiguous bytes
           float *dst = a.ckpt + (slot * H + h) * (int64_t)(KD * VD) + 4 * c;
+#pragma unroll 1
+          for (int cb = 0; cb < 8; ++cb) {
+            uint32_t r[16];
+            tmem_ld16(tS + lane_off + 16 * cb, r);
+            tmem_ld_wait(r);
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb) {
-            uint32_t r[32];
-            tmem_ld32(tS + lane_off + 32 * cb, r);
-            tmem_ld_wait32(r);
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4 *>(dst + (8 * cb + e / 4) * (4 * KD)) =
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4 *>(dst + (4 * cb + e / 4) * (4 * KD)) =
                   make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
                               __uint_as_float(r[e + 3]));
           }
@@ -673,17 +576,88 @@ __global__ void __launch_bounds__(448, 1)
       const float *dhtrow = a.dht ? a.dht + ((d * H + h) * KD + c) * VD : nullptr;
       if (dhtrow || un.piece + 1 < un.npieces) {
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-          float dh[32];
-          piece_grad_out<32>(dh, dhtrow, a.lr, a.dr, u - un.piece, un.piece, un.npieces, H, h, c, 32 * cb);
-          uint32_t r[32];
-          tmem_ld32(tS + lane_off + 32 * cb, r);
-          tmem_ld_wait32(r);
+        for (int cb = 0; cb < 8; ++cb) {
+          float dh[16];
+          piece_grad_out<16>(dh, dhtrow, a.lr, a.dr, u - un.piece, un.piece, un.npieces, H, h, c, 16 * cb);
+          uint32_t r[16];
+          tmem_ld16(tS + lane_off + 16 * cb, r);
+          tmem_ld_wait(r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc += __uint_as_float(r[i]) * dh[i];
+          for (int i = 0; i < 16; ++i) acc += __uint_as_float(r[i]) * dh[i];
         }
       }
       a.bvec[(u * H + h) * KD + c] = acc;
+    }
+  } else {
+    // ---------- epilogue warpgroup: key channel c, all tokens of the chunk ----------
+    //   dq_t = scale exp(G_t) acc_t,  dgp_t = sum_{r >= t in chunk} q_r dq_r
+    // Full chunks go to shared memory (dq over the raw q it was computed
+    // from) for the TMA stores; a ragged last chunk is stored directly.
+    const int qw = warp & 3;
+    const int c = 32 * qw + lane;
+    const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
+    const int64_t gc0 = unit_chunk0(a.units, un);
+    uint32_t ph_dqf = 0, ph_egr = 0;
+    for (int jj = 0; jj < nch; ++jj) {
+      const int bb = jj & 1, stt = jj % asm_::NS;
+      const int64_t tok0 = s0 + (int64_t)jj * C;
+      const int L = (int)min((int64_t)C, s1 - tok0);
+      if (!mbar_wait(&dq_full[bb], (ph_dqf >> bb) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      ph_dqf ^= 1u << bb;
+      if (!mbar_wait(&eg_ready[bb], (ph_egr >> bb) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      ph_egr ^= 1u << bb;
+      if (!mbar_wait(&qfull[stt], (jj / asm_::NS) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      // the qt staging buffer is free once the previous chunk's stores have read it
+      if (jj >= 1 && !mbar_wait(&stg_free, (jj - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
+      tc_fence_after();
+      const ColBf16 qc(sbase + asm_::Q + stt * 16384, 0, c);
+      const ColBf16 qtc(sbase + asm_::QT, 0, c);
+      // partials in the chunk-slot layout of the scratch: four tokens of one
+      // channel per 16 bytes, [token quad][channel], so each warp store
+      // covers 512 contiguous bytes (read back the same way by pass B)
+      float4 *dst = reinterpret_cast<float4 *>(a.dgp) + ((gc0 + jj) * H + h) * (int64_t)(KD * C / 4) + c;
+      float suf = 0.f;
+#pragma unroll 1
+      for (int blk = 3; blk >= 0; --blk) {
+        const int tb = 16 * blk;  // first token of the block
+        uint32_t acc[16], eg[16];
+        tmem_ld16(tDQ + 64 * bb + lane_off + tb, acc);
+        tmem_ld16(tEG + 64 * bb + lane_off + tb, eg);
+        uint16_t qb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qb[i] = lds_u16(qc.a[i & 7] + (uint32_t)(tb + i) * 128u);
+        tmem_ld_wait(acc);
+        tmem_ld_wait(eg);
+        float dqv[16], qtv[16], sv[16];
+#pragma unroll
+        for (int i = 15; i >= 0; --i) {
+          const float sg = a.scale * __uint_as_float(eg[i]);
+          const float qf = bf16_bits_to_f32(qb[i]);
+          dqv[i] = sg * __uint_as_float(acc[i]);
+          qtv[i] = sg * qf;  // qt = scale q exp(G), the gated q of pass B
+          if (tb + i < L) suf += qf * dqv[i];
+          sv[i] = suf;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[(4 * blk + q) * KD] = make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
+        if (L == C) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sts_u16(qc.a[i & 7] + (uint32_t)(tb + i) * 128u, f32_to_bf16_bits(dqv[i]));
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sts_u16(qtc.a[i & 7] + (uint32_t)(tb + i) * 128u, f32_to_bf16_bits(qtv[i]));
+        } else {
+          transpose_4x4_blocks(dqv, lane);
+          store_block_bf16(a.dq + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, dqv, lane, tb, L);
+          transpose_4x4_blocks(qtv, lane);
+          store_block_bf16(a.qt + ((tok0 + tb) * H + h) * KD + 32 * qw, H * KD, qtv, lane, tb, L);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&dq_free[bb]);
+      mbar_arrive(&eg_free[bb]);
+      fence_async_smem();
+      mbar_arrive(&out_ready);
     }
   }
   tc_fence_before();
@@ -792,15 +766,6 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
           BW_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)(s0 + (int64_t)j * C);
-        if (j - 2 >= 0) {
-          const int tp = tok - 2 * C;
-          for (int x = 0; x < 128; x += 64) {
-            tma_prefetch_3d(&maps.qt, x, h, tp);
-            if (x < a.vd) tma_prefetch_3d(&maps.dO, x, h, tp);  // v and do have vd columns
-            tma_prefetch_3d(&maps.kt, x, h, tp);
-            if (x < a.vd) tma_prefetch_3d(&maps.v, x, h, tp);
-          }
-        }
         mbar_expect_tx(&full[st], 2 * 16384);
         for (int x = 0; x < 2; ++x) {
           tma_load_3d(sm + bsm::QD + st * 32768 + x * 16384, &maps.qt, 64 * x, h, tok, &full[st]);
@@ -1299,7 +1264,7 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
     ra.dbuf = (float *)(ws + Lo.off_Dr);
     if ((e = launch_piece_states(fm, fa, &rm, &ra, Lo.max_units, pr.H, st)) != cudaSuccess) return e;
   }
-  dq_kernel<<<grid, 448, smA, st>>>(maps, a);
+  dq_kernel<<<grid, 576, smA, st>>>(maps, a);
   mark_launch("gla_bwd_dq_kernel", st);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gla_bwd_rev_kernel<<<grid, 448, smB, st>>>(maps, a);

@@ -46,10 +46,10 @@ namespace tc {
 // shared memory.  SSD runs the same kernel with one gate per head, q / k
 // shared by a group of heads and V = 64 read as 128 columns (FwdArgs:
 // gate_head, hq_div, vd).
-//   warp 0      TMA producer (3-stage ring of q, k, v tiles; L2 prefetch of
-//               gates and of the tiles two chunks ahead)
+//   warp 0      TMA producer (ring of q, k, v tiles; no L2 prefetches: issued
+//               from this thread they delayed the tile loads behind them)
 //   warp 1      TMEM owner and MMA issuer
-//   warps 2..9  prep: gates straight from L2, prefix/suffix products,
+//   warps 2..9  prep: gates loaded ahead of their chunk, prefix/suffix products,
 //               scaled q / k in place
 //   warps 10..13 epilogue: causal mask of P, state update S (fp32, in
 //               registers, thread c holds row c), output stores
@@ -300,19 +300,6 @@ __device__ __forceinline__ void gla_fwd_body(const FwdMaps &maps, const FwdArgs 
           FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)chunk_tok(j);
-        for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
-          // gates for the prep warps (read from L2); q/k/v ahead of the ring
-          const int tp = (int)chunk_tok(jp);
-          if (!HG)
-            for (int x = 0; x < KD; x += 32) tma_prefetch_3d(&maps.g, x, h, tp);
-          if (jp >= fsm::NS) {
-            tma_prefetch_3d(&maps.q, 0, hq, tp);
-            tma_prefetch_3d(&maps.q, 64, hq, tp);
-            tma_prefetch_3d(&maps.k, 0, hq, tp);
-            tma_prefetch_3d(&maps.k, 64, hq, tp);
-            if (vb * 64 < a.vd) tma_prefetch_3d(&maps.v, vb * 64, h, tp);
-          }
-        }
         // this CTA's half of the q / k channels (the peer writes the other
         // half of the prepared tiles) and its value half of v
         mbar_expect_tx(&full[s], 3 * 8192);

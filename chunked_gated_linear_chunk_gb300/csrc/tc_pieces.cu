@@ -83,10 +83,9 @@ cudaError_t launch_build_units(const Docs &docs, int64_t plen, Unit *units, int6
 //   L[kb rows]^T = V^T khat[:, kb]      (128 value lanes x 64 channel columns)
 // so no CTA needs another's prepared tile.  320 threads, about 100 KB of
 // shared memory and 64 TMEM columns: two CTAs share an SM.
-//   warp 0     TMA: the kb block of k (q) and all of v (do), 4-stage ring;
-//              L2 prefetch of the gates two chunks ahead
+//   warp 0     TMA: the kb block of k (q) and all of v (do), 4-stage ring
 //   warp 1     TMEM owner and MMA issuer
-//   warps 2..9 prep (gates straight from L2, prefix / suffix products, the
+//   warps 2..9 prep (gates loaded a chunk ahead, prefix / suffix products, the
 //              kb block scaled in place), then the store of L and of the
 //              piece's total decay of their channels
 // ---------------------------------------------------------------------------
@@ -162,12 +161,6 @@ __device__ __forceinline__ void piece_state_body(const FwdMaps &maps, const FwdA
         if (j >= psm::NS && !mbar_wait(&empty[s], ((j / psm::NS) - 1) & 1, WAIT_CYCLES)) PS_FAIL_AND_BREAK
         if (*abortp) break;
         const int tok = (int)chunk_tok(j);
-        if (!a.gate_head)
-          for (int jp = (j == 0 ? 0 : j + 2); jp <= j + 2 && jp < nch; ++jp) {
-            const int tp = (int)chunk_tok(jp);
-            tma_prefetch_3d(&maps.g, 64 * kb, h, tp);
-            tma_prefetch_3d(&maps.g, 64 * kb + 32, h, tp);
-          }
         mbar_expect_tx(&full[s], 8192 + 16384);
         tma_load_3d(sm + psm::K + s * 8192, &maps.k, 64 * kb, hq, tok, &full[s]);
         tma_load_3d(sm + psm::V + s * 16384, &maps.v, 0, h, tok, &full[s]);

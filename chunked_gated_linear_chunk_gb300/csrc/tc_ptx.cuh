@@ -184,12 +184,6 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
 // Element-wise add of a shared-memory tile into global memory, done by the
 // TMA unit at L2 (the map's element type, here fp32; same bulk group as
 // tma_store_3d).  Rows outside the map's extent are not written.
-// pull a tile into L2 ahead of its load into shared memory (no completion to wait for)
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *m, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"((uint64_t)m), "r"(x), "r"(y),
-               "r"(z)
-               : "memory");
-}
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *m, const void *src, int x, int y, int z) {
   asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    (uint64_t)m),

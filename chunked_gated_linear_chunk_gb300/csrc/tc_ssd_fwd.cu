@@ -140,11 +140,11 @@ __global__ void __launch_bounds__(512, 1) ssd_fwd_kernel(const __grid_constant__
         // chunk periods from now, once a stage frees up
         if (j + 2 < nch) {
           const int tp = (int)chunk_tok(j + 2);
-          tma_prefetch_l2_3d(&maps.q, 0, hq, tp);
-          tma_prefetch_l2_3d(&maps.q, 64, hq, tp);
-          tma_prefetch_l2_3d(&maps.k, 0, hq, tp);
-          tma_prefetch_l2_3d(&maps.k, 64, hq, tp);
-          tma_prefetch_l2_3d(&maps.v, 0, h, tp);
+          tma_prefetch_3d(&maps.q, 0, hq, tp);
+          tma_prefetch_3d(&maps.q, 64, hq, tp);
+          tma_prefetch_3d(&maps.k, 0, hq, tp);
+          tma_prefetch_3d(&maps.k, 64, hq, tp);
+          tma_prefetch_3d(&maps.v, 0, h, tp);
         }
         issued = j + 1;
       }
