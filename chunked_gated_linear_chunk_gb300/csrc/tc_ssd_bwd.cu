@@ -297,6 +297,16 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_a_kernel(const __grid_constant
         tma_load_3d(sm + K + s * 16384 + 8192, &maps.k, 64, hq, tok, &full[s]);
         tma_load_3d(sm + V + s * 8192, &maps.v, 0, h, tok, &full[s]);
         tma_load_3d(sm + DO + s * 8192, &maps.dout, 0, h, tok, &full[s]);
+        // the tiles of chunk j + 2 into L2 ahead of their load
+        if (j + 2 < nch) {
+          const int tp = (int)chunk_tok(j + 2);
+          tma_prefetch_3d(&maps.q, 0, hq, tp);
+          tma_prefetch_3d(&maps.q, 64, hq, tp);
+          tma_prefetch_3d(&maps.k, 0, hq, tp);
+          tma_prefetch_3d(&maps.k, 64, hq, tp);
+          tma_prefetch_3d(&maps.v, 0, h, tp);
+          tma_prefetch_3d(&maps.dout, 0, h, tp);
+        }
         issued = j + 1;
       }
       for (int j = max(0, issued - NS); j < issued; ++j)
@@ -607,6 +617,16 @@ __global__ void __launch_bounds__(512, 1) ssd_bwd_b_kernel(const __grid_constant
         tma_load_3d(sm + K + s * 16384 + 8192, &maps.k, 64, hq, tok, &full[s]);
         tma_load_3d(sm + V + s * 8192, &maps.v, 0, h, tok, &full[s]);
         tma_load_3d(sm + DO + s * 8192, &maps.dout, 0, h, tok, &full[s]);
+        // the tiles of chunk i + 2 into L2 ahead of their load
+        if (i + 2 < nch) {
+          const int tp = (int)chunk_tok(i + 2);
+          tma_prefetch_3d(&maps.q, 0, hq, tp);
+          tma_prefetch_3d(&maps.q, 64, hq, tp);
+          tma_prefetch_3d(&maps.k, 0, hq, tp);
+          tma_prefetch_3d(&maps.k, 64, hq, tp);
+          tma_prefetch_3d(&maps.v, 0, h, tp);
+          tma_prefetch_3d(&maps.dout, 0, h, tp);
+        }
         issued = i + 1;
       }
       for (int i = max(0, issued - NS); i < issued; ++i)
