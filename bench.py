@@ -54,12 +54,16 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
-def shape_of(w, n_docs=None):
+def shape_of(w, n_docs=None, sms=None):
     from chunked_gated_linear_chunk_gb300 import roofline as rf
 
+    nd = n_docs if n_docs is not None else w.B
+    # the piece split applies to uniform rows (one document per row)
+    plen = rf.piece_len(w.B, w.T, nd, w.H, sms, w.chunk) if sms and nd == w.B else 0
     return rf.Shape(B=w.B, T=w.T, H=w.H, Hqk=w.Hqk, K=w.K, V=w.V, elem=2 if w.dtype == "bf16" else 4,
-                    gate="channel" if w.kind == "gla" else "head", n_docs=n_docs if n_docs is not None else w.B,
-                    initial_state=w.initial_state, final_state=w.final_state, dht=w.final_state, chunk=w.chunk)
+                    gate="channel" if w.kind == "gla" else "head", n_docs=nd,
+                    initial_state=w.initial_state, final_state=w.final_state, dht=w.final_state, chunk=w.chunk,
+                    plen=plen)
 
 
 def job_throughput(ms_local, tokens_per_rank_step, world, device=None):
@@ -322,7 +326,7 @@ def measure_device(w, dev, steps, warmup, world=1, rank_sync=False):
         launches += len(tfs[i].labels) + len(tbs[i].labels)
 
     peaks, peak_kind = load_peaks()
-    shp = shape_of(w, n_seqs)
+    shp = shape_of(w, n_seqs, torch.cuda.get_device_properties(dev).multi_processor_count)
     flops = rf.fwd_flops(shp) + rf.bwd_flops(shp)
     nbytes = rf.fwd_bytes(shp) + rf.bwd_bytes(shp)
     t_roof = rf.roofline_time_s(flops, nbytes, peaks["bf16_tflops"], peaks["hbm_gbs"])

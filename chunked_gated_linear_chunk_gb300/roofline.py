@@ -34,6 +34,7 @@ class Shape:
     final_state: bool = False
     dht: bool = False
     chunk: int = 64
+    plen: int = 0  # piece length of the backward's exact sequence split (0: no split)
 
     @property
     def BT(self):
@@ -97,11 +98,34 @@ def kernel_bytes(s: Shape, label: str) -> int:
     if label in ("gla_bwd_rev_kernel", "ssd_bwd_b_kernel"):  # reads q, k, v, g, do (+dht); writes dk, dv, dg (+dh0)
         return ins5 + s.qk_bytes() + s.v_bytes() + s.gate_bytes() + (
             s.state_bytes() if s.dht else 0) + (s.state_bytes() if s.initial_state else 0)
+    if label == "piece_state_kernel" and s.plen > 0:
+        # the forward piece pass reads k, v, g of every piece but a row's
+        # last, the reverse pass q, do, g of every piece but its first
+        npr = -(-s.T // s.plen)
+        per_tok = s.Hqk * s.K * s.elem + s.H * s.V * s.elem + s.gate_bytes() // s.BT
+        return s.B * ((npr - 1) * s.plen + (s.T - s.plen)) * per_tok
     if label == "simt_state_pass":  # reads k, v, g (+h0)
         return s.qk_bytes() + s.v_bytes() + s.gate_bytes() + (s.state_bytes() if s.initial_state else 0)
     if label == "simt_bwd":
         return bwd_bytes(s)
     return 0
+
+
+def piece_len(B: int, T: int, n_seqs: int, H: int, sms: int, chunk: int = 64) -> int:
+    """The backward's piece length for uniform rows (0: no split), by the
+    library's rule: split only when one CTA per (document, head) leaves more
+    than a quarter of the SMs idle, into about as many pieces as fill one
+    wave, each a whole number of chunks and at least four."""
+    units = n_seqs * H
+    if units <= 0 or units * 4 >= sms * 3:
+        return 0
+    want = sms // units
+    if want < 2:
+        return 0
+    avg = -(-(B * T) // n_seqs)
+    plen = -(-avg // want)
+    plen = max(-(-plen // chunk) * chunk, 4 * chunk)
+    return 0 if plen >= avg else plen
 
 
 def roofline_time_s(flops: float, nbytes: float, peak_tflops: float, peak_gbs: float) -> float:
