@@ -22,11 +22,13 @@
 //     dH <- dHh + qt^T dO;  dh0 = dH at the document start
 //
 // dq, dk, dv are produced transposed (rows = key channel or value column)
-// as M = 128 tcgen05 accumulators, so thread c of the epilogue warpgroup
-// reads row c of TMEM and owns channel c for the suffix sums.  Thread roles
-// as in the forward: warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 prep
-// (thread = one key channel x 32 tokens; it stages exp(+-G) into its own
-// TMEM lane), warps 10..13 epilogue.  SSD runs the same kernels with one
+// as M = 128 tcgen05 accumulators, so the thread that reads row c of TMEM
+// owns channel c for the suffix sums.  Thread roles: warp 0 TMA, warp 1
+// MMA + TMEM owner, warps 2..9 per-channel warps (thread = one key channel
+// x 32 tokens; gate work, exp(+-G) staged in their own TMEM lanes, and in
+// pass B the dk / dv / dg epilogue), warps 10..13 masks and the state; in
+// pass A warps 14..17 run the dq epilogue (thread = one key channel, all 64
+// tokens).  SSD runs the same kernels with one
 // gate per head, q / k shared by a group of heads and V = 64 read as 128
 // columns (BwdArgs: gate_head, hq_div, vd).
 #include <string.h>
