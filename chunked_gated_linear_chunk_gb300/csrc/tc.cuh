@@ -36,7 +36,7 @@ struct TcLayout {
   int64_t plen, max_units, ckpt_slots;
   bool pieces, table;
   size_t off_units, off_order, off_L, off_D, off_Lr, off_Dr, off_dgp, off_bvec, off_ckpt, off_qt, off_kt, off_eng,
-      total;
+      off_egam, total;
 };
 // The backward resets the gate-gradient carry to the exact boundary term
 // (S_end (.) dH_end) 1_V every CKPT_CHUNKS chunks (state written by pass A).

@@ -61,7 +61,9 @@ struct BwdArgs {
                          // starts from zero at their ends, [units,H,K] decays
   float *ckpt;   // [slots, H, V/4, K, 4] fp32 state every CKPT_CHUNKS chunks (pass A -> pass B)
   __nv_bfloat16 *qt, *kt;  // scratch [BT, H, K]: gated q and k (pass A -> pass B)
-  float *eng;    // scratch [chunk slots, H, C/4, K, 4] fp32: exp(-G) (pass A -> pass B)
+  uint16_t *eng;  // scratch [chunk slots, H, C/4, K, 4] bf16: exp(-G) (pass A -> pass B)
+  float *egam;    // scratch [chunk slots, H, K] fp32: each chunk's exp(-Gam) exactly, for the
+                  // state-gradient recurrence (pass A -> pass B)
   int *err;
 };
 
@@ -449,11 +451,16 @@ __global__ void __launch_bounds__(576, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) sts_u16(kc.at(16 * hb + i), kb[i]);
             {
-              // exp(-G) for pass B, chunk-slot layout as the partials
-              float4 *dst = reinterpret_cast<float4 *>(a.eng) + ((gc0 + j) * H + h) * (int64_t)(KD * C / 4) + c;
+              // exp(-G) for pass B in bf16 (it scales dk, which is rounded
+              // to bf16 in turn), chunk-slot layout as the partials: four
+              // tokens of one channel per 8 bytes; the chunk's exp(-Gam)
+              // (token 63) also in fp32, for the state-gradient recurrence
+              uint2 *dst = reinterpret_cast<uint2 *>(a.eng) + ((gc0 + j) * H + h) * (int64_t)(KD * C / 4) + c;
 #pragma unroll
               for (int q = 0; q < 4; ++q)
-                dst[(8 * th + 4 * hb + q) * KD] = make_float4(en[4 * q], en[4 * q + 1], en[4 * q + 2], en[4 * q + 3]);
+                dst[(8 * th + 4 * hb + q) * KD] =
+                    make_uint2(pack_bf16(en[4 * q], en[4 * q + 1]), pack_bf16(en[4 * q + 2], en[4 * q + 3]));
+              if (th == 1 && hb == 1) a.egam[((gc0 + j) * H + h) * KD + c] = en[15];
             }
             if (L < C) {  // ragged chunk: kt rows < L straight to the workspace
               const int tb = 32 * th + 16 * hb;
@@ -700,7 +707,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[bsm::NS], empty[bsm::NS], kfull[bsm::NK], kempty[bsm::NK],
       prep_done[bsm::NS], out_ready[bsm::NK], pdp_full, pdp_ready, dh_ready, dh_full, kv_full, kv_free,
-      eg_ready[2], eg_free[2], bnd_ready[2];
+      bnd_ready[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -731,8 +738,6 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
       mbar_init(&out_ready[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&eg_ready[i], 256);
-      mbar_init(&eg_free[i], 128);
       mbar_init(&bnd_ready[i], 128);
     }
     mbar_init(&pdp_full, 1);
@@ -865,15 +870,17 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
     const int qw = warp & 3, th = (warp - 2) >> 2;
     const int c = 32 * qw + lane;
     const uint32_t lane_off = (uint32_t)(32 * qw) << 16;
-    uint32_t ph_free = 0;
     float carry = a.bvec ? a.bvec[(u * H + h) * KD + c] : 0.f;
     // exp(-G) of the next chunk (in visiting order), this half's tokens, as
-    // written by pass A (chunk-slot layout: [token quad][channel] x 4)
-    float4 en4[8];
+    // written by pass A (bf16, chunk-slot layout: [token quad][channel] x 4)
+    uint2 en4[8];
     auto load_en = [&](int jj) {
-      const float *ep = a.eng + ((gc0 + jj) * H + h) * (int64_t)(KD * C) + 4 * c;
+      const float *ep = reinterpret_cast<const float *>(a.eng + ((gc0 + jj) * H + h) * (int64_t)(KD * C) + 4 * c);
 #pragma unroll
-      for (int w = 0; w < 8; ++w) en4[w] = ldg_early4(ep + (8 * th + w) * (4 * KD));
+      for (int w = 0; w < 8; ++w) {
+        const float2 x = ldg_early2(ep + (8 * th + w) * (2 * KD));
+        en4[w] = make_uint2(__float_as_uint(x.x), __float_as_uint(x.y));
+      }
     };
     if (nch > 0) load_en(nch - 1);
     // iteration i: exp(-G) of chunk nch-1-i, then the epilogue of the previous one
@@ -885,26 +892,23 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         // the q (.) dq partials of this chunk (read by its epilogue in the
         // next iteration) into L2: 32 KB, one 128-byte line per thread
         prefetch_l2(a.dgp + ((gc0 + j) * H + h) * (int64_t)(KD * C) + (th * 128 + c) * 32);
-        float4 e4[8];
+        uint2 e4[8];
 #pragma unroll
         for (int w = 0; w < 8; ++w) e4[w] = en4[w];
         if (j >= 1) load_en(j - 1);
-        // exp(-G) -> TMEM for the dk epilogue and the state step
-        if (i >= 2) {
-          if (!mbar_wait(&eg_free[b], (ph_free >> b) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
-          ph_free ^= 1u << b;
-        }
+        // exp(-G) -> TMEM for the dk epilogue (buffer b was last read by
+        // these threads' epilogue of chunk i - 2)
         tc_fence_after();
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           uint32_t r[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 e = e4[4 * hb + q];
-            r[4 * q] = __float_as_uint(e.x);
-            r[4 * q + 1] = __float_as_uint(e.y);
-            r[4 * q + 2] = __float_as_uint(e.z);
-            r[4 * q + 3] = __float_as_uint(e.w);
+            const uint2 e = e4[4 * hb + q];
+            r[4 * q] = e.x << 16;
+            r[4 * q + 1] = e.x & 0xffff0000u;
+            r[4 * q + 2] = e.y << 16;
+            r[4 * q + 3] = e.y & 0xffff0000u;
           }
           tmem_st16(tEG + 64 * b + lane_off + 32 * th + 16 * hb, r);
         }
@@ -928,7 +932,6 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(&prep_done[st]);
-        mbar_arrive(&eg_ready[b]);
       }
       if (i >= 1) {
         // epilogue of chunk jj (visited at ii = i - 1), this thread's half:
@@ -1057,24 +1060,21 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
       }
       tmem_st_wait();
     }
-    uint32_t ph_egr = 0;
+    // each chunk's exp(-Gam) as pass A wrote it (fp32), one chunk ahead
+    auto load_eg = [&](int jj) -> float { return ldg_early(a.egam + ((gc0 + jj) * H + h) * KD + c); };
+    float egn = nch > 0 ? load_eg(nch - 1) : 1.f;
     for (int i = 0; i < nch; ++i) {
       const int j = nch - 1 - i, b = i & 1;
+      (void)b;
+      const float egc = egn;
+      if (j >= 1) egn = load_eg(j - 1);
       // (1) dHh = exp(Gam) dH in TMEM; its bf16 copy replaces chunk i-1's
       //     once dk/dv of chunk i-1 have read that.  This step does not need
       //     chunk i's P and dP, so it runs while their products complete.
-      if (!mbar_wait(&eg_ready[b], (ph_egr >> b) & 1, WAIT_CYCLES) ||
-          (i >= 1 && !mbar_wait(&dh_full, (i - 1) & 1, WAIT_CYCLES)))
-        BW_FAIL_AND_BREAK
-      ph_egr ^= 1u << b;
+      if (i >= 1 && !mbar_wait(&dh_full, (i - 1) & 1, WAIT_CYCLES)) BW_FAIL_AND_BREAK
       tc_fence_after();
       {
-        uint32_t e1[16];
-        tmem_ld16(tEG + 64 * b + lane_off + 48, e1);
-        tmem_ld_wait(e1);
-        const float eGam = __frcp_rn(__uint_as_float(e1[15]));  // 1 / exp(-Gam)
-        tc_fence_before();
-        mbar_arrive(&eg_free[b]);
+        const float eGam = __frcp_rn(egc);  // 1 / exp(-Gam)
         uint8_t *Dt = sm + bsm::DH;
         const int64_t slot = ckpt_slot(gc0, doc_c0, j, nch);
         // checkpoint rows of channel c ([value quad][channel] x 4 layout)
@@ -1091,7 +1091,7 @@ __device__ __forceinline__ void gla_bwd_rev_body(const BwdMaps &maps, const BwdA
         }
         float bnd = 0.f;
         bool waited = i == 0;
-#pragma unroll
+#pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t r[32];
           float4 cv[8];
@@ -1216,7 +1216,8 @@ cudaError_t bwd(const Prob &pr, const Docs &docs, const glacore_problem *p, cons
   a.bvec = (float *)(ws + Lo.off_bvec);
   a.ckpt = (float *)(ws + Lo.off_ckpt);
   a.qt = (__nv_bfloat16 *)(ws + Lo.off_qt);
-  a.eng = (float *)(ws + Lo.off_eng);
+  a.eng = (uint16_t *)(ws + Lo.off_eng);
+  a.egam = (float *)(ws + Lo.off_egam);
   a.kt = (__nv_bfloat16 *)(ws + Lo.off_kt);
   a.err = pr.err;
   const dim3 grid((unsigned)(Lo.max_units * pr.H));

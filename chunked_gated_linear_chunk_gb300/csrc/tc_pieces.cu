@@ -383,7 +383,7 @@ TcLayout tc_layout(const glacore_problem *p, bool backward) {
   const size_t state = (size_t)KD * VD * sizeof(float);
   size_t off = 0;
   L.off_units = L.off_order = L.off_L = L.off_D = L.off_Lr = L.off_Dr = L.off_dgp = L.off_bvec = L.off_ckpt = 0;
-  L.off_qt = L.off_kt = L.off_eng = 0;
+  L.off_qt = L.off_kt = L.off_eng = L.off_egam = 0;
   // chunks of all documents (upper bound) -> checkpoint slots
   const int64_t chunks = p->segment_ids ? (p->B * p->T + C - 1) / C + p->n_seqs
                                         : p->B * ((p->T + C - 1) / C);
@@ -421,9 +421,12 @@ TcLayout tc_layout(const glacore_problem *p, bool backward) {
     off = al256(off + (size_t)p->B * p->T * H * KD * 2);
     L.off_kt = off;
     off = al256(off + (size_t)p->B * p->T * H * KD * 2);
-    // exp(-G) per chunk slot (pass A -> pass B), laid out as the partials
+    // exp(-G) per chunk slot (pass A -> pass B), bf16, laid out as the partials
     L.off_eng = off;
-    off = al256(off + (size_t)chunks * H * KD * C * sizeof(float));
+    off = al256(off + (size_t)chunks * H * KD * C * sizeof(uint16_t));
+    // each chunk slot's exp(-Gam), fp32
+    L.off_egam = off;
+    off = al256(off + (size_t)chunks * H * KD * sizeof(float));
   }
   L.total = off;
   return L;
